@@ -1,0 +1,328 @@
+"""Float64 CPU oracle of the Kamera reuse operator.
+
+TEST INFRASTRUCTURE ONLY. This module is imported by ``tests/``, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``, and by nothing else. It
+shares no code with the CUDA library: it imports only NumPy and the standard library, and it
+takes plain arrays (bf16 values as ``uint16`` bit patterns) and plain numbers.
+
+What it computes (Kamera: Unified Position-Invariant Multimodal KV Cache for Training-Free
+Reuse, Eq. 1 in §1 and §3; App. A "Forming and applying the patch"):
+
+    KV^(B|A) = R(δ) · KV(B|∅) + U_m · V_mᵀ
+
+  * R(δ) re-rotates the RoPE phase of the stored keys by the integer offset δ = p1 - p0
+    (§3 "Relocate"); RoPE composes, R(δ)R(p0) = R(p1), so this is exact algebra. Values and
+    the MLA latent c_KV are never rotated (§3 "One mechanism for MLA, GQA, and MHA"; Fig. 2).
+  * U_m V_mᵀ is the rank-m patch: U holds U·Σ [T×m], the stored V_m is kept transposed as
+    Vt [m×W] (App. A, ``form_patch`` returns ``U[:, :m] * S[:m], Vt[:m]``); the patch is added
+    after the rotation, in the target frame (App. A ``apply_reuse``: rotate, then add).
+  * The result is written into a paged KV pool at the chunk's new slots (§6 "Recompute-free
+    on a live engine": SGLang's paged KV pool).
+
+Readings where the pages are silent (each is listed in the design doc):
+  * inv_freq_i = θ^(-2i/d), i < d/2, d = rotary dim (head_dim for GQA/MHA, the 64-dim k_pe band
+    for MLA); the angle δ·inv_freq_i is formed in float64 and cos/sin taken in float64.
+  * NeoX-half pairing pairs dim i with i + d/2 inside a rope band; interleaved pairs 2i, 2i+1.
+  * GQA/MHA: every K head is rotated over its whole head_dim; one patch group per (layer,
+    channel) spans all KV heads (W = H_kv·head_dim). MLA: row = c_KV ‖ k_pe (k_pe trailing),
+    group 0 = c_KV (W = latent), group 1 = k_pe (W = rope_dim).
+  * δ = 0 is R(0) = I exactly: no arithmetic, bit patterns kept (signed zeros included).
+    Channels that neither rotate nor receive a patch are byte copies.
+  * One rounding: the float64 result is rounded once, to nearest-even bf16.
+  * slot(req, tok) = page_table[req][tok // page_size] * page_size + tok % page_size.
+"""
+from __future__ import annotations
+
+import math
+from types import SimpleNamespace
+
+import numpy as np
+
+GQA = 0
+MLA = 1
+NEOX_HALF = 0
+INTERLEAVED = 1
+
+
+# ----------------------------------------------------------------------------------------
+# bf16 encode / decode
+# ----------------------------------------------------------------------------------------
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Decode bf16 bit patterns (uint16) to float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """Round float64 values once to the nearest bf16, ties to even; returns uint16 bits.
+
+    bf16 keeps 8 significant bits and float32's exponent range, so the spacing at |x| is
+    2^(e-7) with e = floor(log2|x|) clamped at -126 (subnormal spacing 2^-133). The value is
+    rounded on that grid (NumPy rounds halves to even), overflow goes to infinity, and the
+    (now exactly representable) value is encoded through float32.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    neg = np.signbit(x)
+    finite = np.isfinite(x)
+    safe = np.where(finite, ax, 0.0)
+    _, E = np.frexp(safe)
+    e = np.maximum(E - 1, -126)
+    q = np.ldexp(1.0, e - 7)
+    r = np.round(safe / q) * q
+    big = r >= 2.0 ** 128
+    with np.errstate(over="ignore"):
+        r32 = np.where(big, np.float32(np.inf), r.astype(np.float32))
+    bits = (r32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits = np.where(finite, bits, np.where(np.isnan(x), np.uint16(0x7FC0), np.uint16(0x7F80)))
+    return (bits | (neg.astype(np.uint16) << np.uint16(15))).astype(np.uint16)
+
+
+def factor_f64(a) -> np.ndarray:
+    """A stored factor as float64: bf16 bit patterns (uint16) are decoded, floats are taken as
+    they are (the pins feed float64 factors straight from an SVD)."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_to_f64(a)
+    return a.astype(np.float64)
+
+
+def bf16_ulp(y) -> np.ndarray:
+    """Spacing of bf16 numbers at |y| (the unit in the last place of a bf16 value)."""
+    ay = np.abs(np.asarray(y, dtype=np.float64))
+    _, E = np.frexp(ay)
+    e = np.maximum(E - 1, -126)
+    return np.ldexp(1.0, e - 7)
+
+
+# ----------------------------------------------------------------------------------------
+# RoPE relocation R(δ)
+# ----------------------------------------------------------------------------------------
+
+def inv_freq(theta: float, d: int) -> np.ndarray:
+    """inv_freq_i = θ^(-2i/d) for i < d/2, in float64."""
+    i = np.arange(d // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / d)
+
+
+def rope_pairs(d: int, style: int):
+    """Index arrays (a, b) of the rotation pairs of a d-dim band; pair k uses frequency k."""
+    k = np.arange(d // 2)
+    if style == NEOX_HALF:
+        return k, k + d // 2
+    if style == INTERLEAVED:
+        return 2 * k, 2 * k + 1
+    raise ValueError("unknown rope style")
+
+
+def rotate_band(x, delta: int, theta: float, style: int) -> np.ndarray:
+    """Apply R(δ) to the last axis of ``x`` (a full rope band of even width d).
+
+    Each pair (a, b) turns by φ_k = δ·inv_freq_k:  a' = a cos φ - b sin φ,  b' = b cos φ + a sin φ
+    (§3 "Relocate": re-rotate B's keys by δ). δ = 0 returns the input unchanged.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    if delta == 0:
+        return out
+    d = x.shape[-1]
+    phi = float(delta) * inv_freq(theta, d)
+    c, s = np.cos(phi), np.sin(phi)
+    ia, ib = rope_pairs(d, style)
+    a, b = x[..., ia], x[..., ib]
+    out[..., ia] = a * c - b * s
+    out[..., ib] = b * c + a * s
+    return out
+
+
+# ----------------------------------------------------------------------------------------
+# layout reading: content | rope split (§3, Fig. 2)
+# ----------------------------------------------------------------------------------------
+
+def widths(layout):
+    """(row of channel 0, row of channel 1 or 0, group widths (W0, W1))."""
+    if layout.kind == GQA:
+        w = layout.num_kv_heads * layout.head_dim
+        return w, w, (w, w)
+    return layout.latent_dim + layout.rope_dim, 0, (layout.latent_dim, layout.rope_dim)
+
+
+def rope_bands(layout):
+    """(first column, width) of every rope band of the channel-0 row (K, or c_KV ‖ k_pe)."""
+    if layout.kind == GQA:
+        return [(h * layout.head_dim, layout.head_dim) for h in range(layout.num_kv_heads)]
+    return [(layout.latent_dim, layout.rope_dim)]
+
+
+def channel_groups(layout, channel: int):
+    """Patch groups of a channel's row as (first column, width, group index)."""
+    if layout.kind == GQA:
+        w = layout.num_kv_heads * layout.head_dim
+        return [(0, w, channel)]
+    return [(0, layout.latent_dim, 0), (layout.latent_dim, layout.rope_dim, 1)]
+
+
+def vt_of_group(layout, vt_layer, m: int, g: int) -> np.ndarray:
+    """V_mᵀ of group g from one layer's packed factor ([m×W0] then [m×W1])."""
+    _, _, (w0, w1) = widths(layout)
+    flat = np.asarray(vt_layer)
+    if g == 0:
+        return flat[: m * w0].reshape(m, w0)
+    return flat[m * w0: m * (w0 + w1)].reshape(m, w1)
+
+
+# ----------------------------------------------------------------------------------------
+# the operator
+# ----------------------------------------------------------------------------------------
+
+def layer_patched(item, layer: int) -> bool:
+    return item.patch_m > 0 and item.patch_l0 <= layer < item.patch_l1
+
+
+def reuse_layer(layout, item, layer: int, channel: int, tokens=None):
+    """Exact result of one (item, layer, channel) before rounding.
+
+    Returns (values float64 [t][row], copy_mask bool [row]) where ``copy_mask`` marks the
+    columns that no arithmetic touches (bytes copied verbatim). ``tokens`` selects rows.
+    """
+    canon = item.canon_k if channel == 0 else item.canon_v
+    rows = np.asarray(canon[layer])
+    if tokens is not None:
+        rows = rows[np.asarray(tokens)]
+    x = bf16_to_f64(rows)
+    copy_mask = np.ones(x.shape[-1], dtype=bool)
+    if channel == 0 and item.delta != 0:
+        for c0, d in rope_bands(layout):
+            x[:, c0:c0 + d] = rotate_band(x[:, c0:c0 + d], item.delta, layout.rope_theta,
+                                          layout.rope_style)
+            copy_mask[c0:c0 + d] = False
+    if layer_patched(item, layer):
+        m = item.patch_m
+        li = layer - item.patch_l0
+        for c0, w, g in channel_groups(layout, channel):
+            u = factor_f64(item.patch_u[li][g])
+            if tokens is not None:
+                u = u[np.asarray(tokens)]
+            vt = factor_f64(vt_of_group(layout, item.patch_vt[li], m, g))
+            x[:, c0:c0 + w] = x[:, c0:c0 + w] + u @ vt
+            copy_mask[c0:c0 + w] = False
+    return x, copy_mask
+
+
+def reuse_layer_bits(layout, item, layer: int, channel: int, tokens=None) -> np.ndarray:
+    """bf16 bits the operator writes for one (item, layer, channel): one rounding, byte copy
+    where nothing is computed."""
+    vals, copy_mask = reuse_layer(layout, item, layer, channel, tokens)
+    canon = item.canon_k if channel == 0 else item.canon_v
+    src = np.asarray(canon[layer])
+    if tokens is not None:
+        src = src[np.asarray(tokens)]
+    bits = f64_to_bf16(vals)
+    bits[:, copy_mask] = src[:, copy_mask]
+    return bits
+
+
+def magnitude_layer(layout, item, layer: int, channel: int, tokens=None) -> np.ndarray:
+    """Sum of the magnitudes of the terms that make each result element:
+    |a cos φ| + |b sin φ| on rotated pairs (|x| elsewhere) plus Σ_j |U_tj · Vt_jc|.
+    Float rounding errors of any evaluation order are bounded by a multiple of this."""
+    canon = item.canon_k if channel == 0 else item.canon_v
+    rows = np.asarray(canon[layer])
+    if tokens is not None:
+        rows = rows[np.asarray(tokens)]
+    x = bf16_to_f64(rows)
+    mag = np.abs(x)
+    if channel == 0 and item.delta != 0:
+        for c0, d in rope_bands(layout):
+            phi = float(item.delta) * inv_freq(layout.rope_theta, d)
+            c, s = np.abs(np.cos(phi)), np.abs(np.sin(phi))
+            ia, ib = rope_pairs(d, layout.rope_style)
+            a, b = np.abs(x[:, c0 + ia]), np.abs(x[:, c0 + ib])
+            mag[:, c0 + ia] = a * c + b * s
+            mag[:, c0 + ib] = b * c + a * s
+    if layer_patched(item, layer):
+        m = item.patch_m
+        li = layer - item.patch_l0
+        for c0, w, g in channel_groups(layout, channel):
+            u = np.abs(factor_f64(item.patch_u[li][g]))
+            if tokens is not None:
+                u = u[np.asarray(tokens)]
+            vt = np.abs(factor_f64(vt_of_group(layout, item.patch_vt[li], m, g)))
+            mag[:, c0:c0 + w] += u @ vt
+    return mag
+
+
+def slot_of(page_table, req: int, tok: int, page_size: int) -> int:
+    """Physical slot of logical token ``tok`` of request ``req``."""
+    return int(page_table[req][tok // page_size]) * page_size + tok % page_size
+
+
+def apply_reuse(layout, item, k_pool, v_pool, page_table) -> None:
+    """Write one placed chunk into the pools (``uint16 [L][slots][row]``), every layer."""
+    page = layout.page_size
+    slots = [slot_of(page_table, item.req, item.start_tok + t, page)
+             for t in range(item.num_tokens)]
+    n_ch = 2 if layout.kind == GQA else 1
+    for layer in range(layout.num_layers):
+        for ch in range(n_ch):
+            bits = reuse_layer_bits(layout, item, layer, ch)
+            pool = k_pool if ch == 0 else v_pool
+            for t, s in enumerate(slots):
+                pool[layer, s, :] = bits[t]
+
+
+def batch_reuse(layout, items, k_pool, v_pool, page_table) -> None:
+    for it in items:
+        apply_reuse(layout, it, k_pool, v_pool, page_table)
+
+
+def relocate(layout, k_pool, page_table, req: int, start_tok: int, num_tokens: int,
+             delta: int) -> None:
+    """Survivor relocation in place: rotate the rope columns of K (GQA/MHA) or of the k_pe
+    band (MLA) at the span's slots by δ; all other columns and V are left alone
+    (§5 "Sliding-window survival": keep the survivor's KV as-is and apply R(δ); Fig. 2
+    ``rotate_k_pe_inplace``)."""
+    if delta == 0:
+        return
+    page = layout.page_size
+    for layer in range(layout.num_layers):
+        for t in range(num_tokens):
+            s = slot_of(page_table, req, start_tok + t, page)
+            row = bf16_to_f64(k_pool[layer, s, :])
+            for c0, d in rope_bands(layout):
+                rot = rotate_band(row[c0:c0 + d], delta, layout.rope_theta, layout.rope_style)
+                k_pool[layer, s, c0:c0 + d] = f64_to_bf16(rot)
+
+
+# ----------------------------------------------------------------------------------------
+# compile side, for the pins only (App. A ``form_patch``)
+# ----------------------------------------------------------------------------------------
+
+def form_patch(kv_cond, kv_solo_relocated, m: int):
+    """Δ = KV(B|A) - R(δ)KV(B|∅); keep the top-m SVD factors (U·Σ [T×m], Vt [m×W])."""
+    delta_kv = np.asarray(kv_cond, np.float64) - np.asarray(kv_solo_relocated, np.float64)
+    u, s, vt = np.linalg.svd(delta_kv, full_matrices=False)
+    return u[:, :m] * s[:m], vt[:m]
+
+
+def patch_byte_fraction(T: int, W: int, m: int) -> float:
+    """Bytes of a rank-m patch (U [T×m] and Vt [m×W]) over the bytes of the [T×W] page it
+    patches, same element type on both sides: m·(T + W) / (T·W)."""
+    return m * (T + W) / (T * W)
+
+
+def as_item(**kw) -> SimpleNamespace:
+    """Convenience record with the fields the oracle reads."""
+    base = dict(canon_v=None, patch_u=None, patch_vt=None, patch_m=0, patch_l0=0, patch_l1=0,
+                req=0, start_tok=0)
+    base.update(kw)
+    if "num_tokens" not in base:
+        base["num_tokens"] = int(np.asarray(base["canon_k"]).shape[1])
+    return SimpleNamespace(**base)
+
+
+__all__ = [n for n in dir() if not n.startswith("_") and n not in ("math", "np",
+                                                                  "SimpleNamespace",
+                                                                  "annotations")]

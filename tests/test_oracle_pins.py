@@ -1,0 +1,478 @@
+"""Pins of the float64 oracle against what the Kamera pages and the mathematics fix.
+
+Nothing here retypes the oracle's own formulas: rotations are checked against an explicit
+dense rotation matrix built from scalar ``math`` calls and against complex multiplication,
+the patch against pure-Python sums and Eckart–Young (with singular values taken from an
+eigen-decomposition, not the SVD the oracle calls), rounding against brute-force neighbour
+search and torch's float32 -> bf16 conversion, slots against an independent page expansion,
+and the layout against the shapes printed on the pages (tests/golden/).
+"""
+import cmath
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kamera_oracle as ora
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+def ns_layout(**kw):
+    from types import SimpleNamespace
+    base = dict(kind=ora.GQA, num_layers=1, page_size=4, num_kv_heads=1, head_dim=8,
+                latent_dim=0, rope_dim=8, rope_style=ora.NEOX_HALF, rope_theta=1e4)
+    base.update(kw)
+    return SimpleNamespace(**base)
+
+
+def rand_bf16_bits(shape, scale=1.0, rng=RNG):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------------------------------
+# bf16 rounding
+# ------------------------------------------------------------------------------------------
+
+def test_bf16_known_bit_patterns():
+    vals = [1.0, -2.0, 0.0, -0.0, math.inf, -math.inf, 3.3895313892515355e38, 2.0 ** -133,
+            -(2.0 ** -126), 0.5]
+    want = [0x3F80, 0xC000, 0x0000, 0x8000, 0x7F80, 0xFF80, 0x7F7F, 0x0001, 0x8080, 0x3F00]
+    got = ora.f64_to_bf16(np.array(vals)).tolist()
+    assert got == want
+    assert ora.f64_to_bf16(np.array([math.nan]))[0] & 0x7FFF > 0x7F80
+
+
+def test_bf16_ties_to_even_and_single_rounding():
+    # exact halfway cases go to the even neighbour
+    assert ora.f64_to_bf16(np.array([1 + 2 ** -8]))[0] == 0x3F80
+    assert ora.f64_to_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 0x3F82
+    # just above the halfway point: one rounding goes up; rounding through float32 first
+    # would land exactly on the tie and then on the even value 1.0
+    assert ora.f64_to_bf16(np.array([1 + 2 ** -8 + 2 ** -40]))[0] == 0x3F81
+    assert ora.f64_to_bf16(np.array([-(1 + 2 ** -8 + 2 ** -40)]))[0] == 0xBF81
+    # overflow: above max + half ulp is infinity, below stays max
+    mx = 3.3895313892515355e38
+    half_ulp = 2.0 ** 119
+    assert ora.f64_to_bf16(np.array([mx + half_ulp]))[0] == 0x7F80
+    assert ora.f64_to_bf16(np.array([mx + half_ulp * 0.99]))[0] == 0x7F7F
+
+
+def test_bf16_matches_torch_on_float32_inputs():
+    x = np.concatenate([RNG.standard_normal(50000) * 10.0 ** RNG.integers(-40, 38, 50000),
+                        RNG.standard_normal(2000) * 1e-39,  # subnormal float32 range
+                        RNG.standard_normal(2000)]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = ora.f64_to_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_nearest_by_brute_force_neighbours():
+    y = RNG.standard_normal(4000) * 10.0 ** RNG.uniform(-30, 30, 4000)
+    bits = ora.f64_to_bf16(y)
+    got = ora.bf16_to_f64(bits)
+    # the two neighbours of the chosen value, by stepping the bit pattern
+    mag = bits & 0x7FFF
+    up = ora.bf16_to_f64((bits & 0x8000) | np.minimum(mag + 1, 0x7F7F))
+    dn = ora.bf16_to_f64((bits & 0x8000) | np.maximum(mag.astype(np.int32) - 1, 0).astype(np.uint16))
+    err = np.abs(got - y)
+    assert np.all(err <= np.abs(up - y))
+    assert np.all(err <= np.abs(dn - y))
+    # ties never occur for these draws; the chosen value is strictly nearest or equal
+    assert np.all(err <= 0.5 * ora.bf16_ulp(got) * (1 + 1e-12))
+
+
+def test_bf16_decode_encode_roundtrip_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = ora.bf16_to_f64(bits)
+    back = ora.f64_to_bf16(vals)
+    ok = ~np.isnan(vals)
+    np.testing.assert_array_equal(back[ok], bits[ok])
+
+
+# ------------------------------------------------------------------------------------------
+# RoPE relocation R(δ)
+# ------------------------------------------------------------------------------------------
+
+def dense_rotation(d, delta, theta, style):
+    """Explicit d×d block rotation with 2×2 blocks [[c, -s], [s, c]] on each pair (the
+    textbook RoPE of Su et al.: x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin), built from
+    scalar math calls."""
+    M = [[0.0] * d for _ in range(d)]
+    for k in range(d // 2):
+        phi = delta * math.pow(theta, -2.0 * k / d)
+        c, s = math.cos(phi), math.sin(phi)
+        if style == ora.NEOX_HALF:
+            a, b = k, k + d // 2
+        else:
+            a, b = 2 * k, 2 * k + 1
+        M[a][a], M[a][b] = c, -s
+        M[b][a], M[b][b] = s, c
+    return np.array(M)
+
+
+@pytest.mark.parametrize("style", [ora.NEOX_HALF, ora.INTERLEAVED])
+@pytest.mark.parametrize("d", [2, 4, 8])
+@pytest.mark.parametrize("delta", [1, -7, 1000, 131071])
+def test_rotation_equals_dense_matrix(style, d, delta):
+    x = RNG.standard_normal((3, d))
+    want = x @ dense_rotation(d, delta, 1e4, style).T
+    got = ora.rotate_band(x, delta, 1e4, style)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_rotation_equals_complex_multiplication():
+    d, theta = 16, 1e6
+    x = RNG.standard_normal((5, d))
+    for delta in (3, -576, 32768):
+        got = ora.rotate_band(x, delta, theta, ora.NEOX_HALF)
+        for t in range(5):
+            for k in range(d // 2):
+                z = complex(x[t, k], x[t, k + d // 2])
+                w = z * cmath.exp(1j * delta * theta ** (-2.0 * k / d))
+                assert abs(got[t, k] - w.real) < 1e-12
+                assert abs(got[t, k + d // 2] - w.imag) < 1e-12
+
+
+def test_inv_freq_closed_forms():
+    np.testing.assert_allclose(ora.inv_freq(1e4, 4), [1.0, 0.01], rtol=1e-15)
+    f = ora.inv_freq(1e6, 128)
+    assert f[0] == 1.0 and len(f) == 64
+    np.testing.assert_allclose(f[1:] / f[:-1], 1e6 ** (-2 / 128), rtol=1e-13)
+    np.testing.assert_allclose(f[-1], 1e6 ** (-126 / 128), rtol=1e-13)
+
+
+def test_pair_zero_turns_by_exactly_delta():
+    # inv_freq_0 = 1: the first pair of a unit key turns by δ radians
+    for style in (ora.NEOX_HALF, ora.INTERLEAVED):
+        for delta in (1, -1, 1000, 131071, -131071):
+            e = np.zeros(8)
+            a, b = ora.rope_pairs(8, style)
+            e[a[0]] = 1.0
+            r = ora.rotate_band(e, delta, 1e4, style)
+            assert abs(r[a[0]] - math.cos(delta)) < 1e-12
+            assert abs(r[b[0]] - math.sin(delta)) < 1e-12
+
+
+DELTAS = [0, 1, -1, 576, -576, 32768, -32768, 131071]
+
+
+@pytest.mark.parametrize("style", [ora.NEOX_HALF, ora.INTERLEAVED])
+def test_composition_identity(style):
+    # R(δ) R(p) = R(p + δ)  (§1, §3: RoPE composes exactly)
+    x = RNG.standard_normal((4, 64))
+    for p in DELTAS:
+        xp = ora.rotate_band(x, p, 1e4, style)
+        for d in DELTAS:
+            lhs = ora.rotate_band(xp, d, 1e4, style)
+            rhs = ora.rotate_band(x, p + d, 1e4, style)
+            np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-9)
+
+
+def test_inverse_and_norm_preservation():
+    x = RNG.standard_normal((4, 128))
+    for d in DELTAS:
+        y = ora.rotate_band(x, d, 1e6, ora.NEOX_HALF)
+        np.testing.assert_allclose(ora.rotate_band(y, -d, 1e6, ora.NEOX_HALF), x, atol=1e-12)
+        a, b = ora.rope_pairs(128, ora.NEOX_HALF)
+        np.testing.assert_allclose(np.hypot(y[:, a], y[:, b]), np.hypot(x[:, a], x[:, b]),
+                                   rtol=1e-13)
+
+
+def test_relocation_from_bf16_storage_matches_direct_placement():
+    # keys stored rotated at p (bf16), relocated by δ, against keys rotated directly to p+δ
+    x = RNG.standard_normal((256, 128))
+    for p, d in [(0, 1000), (5000, -576), (100, 131071 - 100)]:
+        stored = ora.f64_to_bf16(ora.rotate_band(x, p, 1e4, ora.NEOX_HALF))
+        moved = ora.f64_to_bf16(ora.rotate_band(ora.bf16_to_f64(stored), d, 1e4, ora.NEOX_HALF))
+        direct = ora.rotate_band(x, p + d, 1e4, ora.NEOX_HALF)
+        got = ora.bf16_to_f64(moved)
+        rel = np.linalg.norm(got - direct) / np.linalg.norm(direct)
+        assert rel < 2 ** -8
+        # the storage rounding (at most half an ulp on each pair member) turns with the pair,
+        # so each element may move by both halves; the final rounding adds half an ulp
+        sv = ora.bf16_to_f64(stored)
+        a, b = ora.rope_pairs(128, ora.NEOX_HALF)
+        pair_err = 0.5 * (ora.bf16_ulp(sv[:, a]) + ora.bf16_ulp(sv[:, b]))
+        bound = np.empty_like(direct)
+        bound[:, a] = pair_err
+        bound[:, b] = pair_err
+        bound += 0.5 * ora.bf16_ulp(got)
+        assert np.all(np.abs(got - direct) <= bound * (1 + 1e-9))
+
+
+# ------------------------------------------------------------------------------------------
+# the operator on items
+# ------------------------------------------------------------------------------------------
+
+def gqa_item(L=2, T=6, H=2, hd=8, m=0, l0=0, l1=0, delta=0, rng=RNG, float_factors=False):
+    lay = ns_layout(num_layers=L, num_kv_heads=H, head_dim=hd, rope_dim=hd)
+    W = H * hd
+    k = rand_bf16_bits((L, T, W), rng=rng)
+    v = rand_bf16_bits((L, T, W), rng=rng)
+    pu = pv = None
+    if m:
+        if float_factors:
+            pu = rng.standard_normal((l1 - l0, 2, T, m))
+            pv = rng.standard_normal((l1 - l0, m * 2 * W))
+        else:
+            pu = rand_bf16_bits((l1 - l0, 2, T, m), rng=rng)
+            pv = rand_bf16_bits((l1 - l0, m * 2 * W), 0.1, rng=rng)
+    it = ora.as_item(canon_k=k, canon_v=v, patch_u=pu, patch_vt=pv, delta=delta, patch_m=m,
+                     patch_l0=l0, patch_l1=l1)
+    return lay, it
+
+
+def test_delta_zero_rank_zero_is_bitwise_identity():
+    lay, it = gqa_item(delta=0)
+    # plant signed zeros and a NaN payload: a byte copy keeps them
+    it.canon_k[0, 0, :4] = [0x8000, 0x0000, 0x8000, 0x7FC3]
+    it.canon_v[1, 2, :2] = [0x8000, 0xFFC1]
+    for layer in range(2):
+        np.testing.assert_array_equal(ora.reuse_layer_bits(lay, it, layer, 0), it.canon_k[layer])
+        np.testing.assert_array_equal(ora.reuse_layer_bits(lay, it, layer, 1), it.canon_v[layer])
+
+
+def test_values_untouched_by_delta():
+    # §3: V is untouched by relocation; with no patch the V bytes equal the stored ones
+    lay, it = gqa_item(delta=12345)
+    for layer in range(2):
+        np.testing.assert_array_equal(ora.reuse_layer_bits(lay, it, layer, 1), it.canon_v[layer])
+        assert not np.array_equal(ora.reuse_layer_bits(lay, it, layer, 0), it.canon_k[layer])
+
+
+def test_patch_by_pure_python_sums():
+    # δ = 0 isolates the patch: out[t][c] = x[t][c] + Σ_j U[t][j] Vt[j][c] per channel group
+    lay, it = gqa_item(L=3, T=3, H=1, hd=4, m=2, l0=1, l1=3, delta=0)
+    W = 4
+    for layer in range(3):
+        for ch in range(2):
+            vals, _ = ora.reuse_layer(lay, it, layer, ch)
+            canon = (it.canon_k if ch == 0 else it.canon_v)[layer]
+            for t in range(3):
+                for c in range(W):
+                    want = float(ora.bf16_to_f64(canon[t, c]))
+                    if 1 <= layer < 3:
+                        li = layer - 1
+                        for j in range(2):
+                            u = float(ora.bf16_to_f64(it.patch_u[li, ch, t, j]))
+                            vt = float(ora.bf16_to_f64(it.patch_vt[li, ch * 2 * W + j * W + c]))
+                            want += u * vt
+                    assert abs(vals[t, c] - want) <= 1e-12 * max(1.0, abs(want))
+
+
+def test_full_rank_patch_reconstructs_conditioned_kv():
+    # App. A: Δ = KV(B|A) - R(δ)KV(B|∅); the patch from the full SVD of Δ added after the
+    # rotation gives back KV(B|A) exactly (float64).
+    T, H, hd = 12, 2, 8
+    W = H * hd
+    delta = 777
+    lay, it = gqa_item(L=1, T=T, H=H, hd=hd, delta=delta)
+    cond_k = RNG.standard_normal((T, W))
+    cond_v = RNG.standard_normal((T, W))
+    solo_k = ora.bf16_to_f64(it.canon_k[0])
+    rel_k = np.concatenate([ora.rotate_band(solo_k[:, h * hd:(h + 1) * hd], delta, 1e4,
+                                            ora.NEOX_HALF) for h in range(H)], axis=1)
+    solo_v = ora.bf16_to_f64(it.canon_v[0])
+    m = min(T, W)
+    uk, vk = ora.form_patch(cond_k, rel_k, m)
+    uv, vv = ora.form_patch(cond_v, solo_v, m)
+    it.patch_u = np.stack([uk, uv])[None]
+    it.patch_vt = np.concatenate([vk.ravel(), vv.ravel()])[None]
+    it.patch_m, it.patch_l0, it.patch_l1 = m, 0, 1
+    got_k, _ = ora.reuse_layer(lay, it, 0, 0)
+    got_v, _ = ora.reuse_layer(lay, it, 0, 1)
+    np.testing.assert_allclose(got_k, cond_k, atol=1e-12)
+    np.testing.assert_allclose(got_v, cond_v, atol=1e-12)
+
+
+def test_low_rank_deficit_recovered_by_any_rank_at_least_r():
+    T, W, r = 20, 16, 3
+    base = RNG.standard_normal((T, W))
+    deficit = RNG.standard_normal((T, r)) @ RNG.standard_normal((r, W))
+    for m in (r, r + 1, W):
+        u, vt = ora.form_patch(base + deficit, base, m)
+        np.testing.assert_allclose(u @ vt, deficit, atol=1e-11)
+
+
+def test_eckart_young_residual():
+    T, W = 40, 24
+    d = RNG.standard_normal((T, W))
+    lam = np.sort(np.linalg.eigvalsh(d.T @ d))[::-1]  # σ_i² from the Gram matrix
+    for m in (1, 4, 8, 23):
+        u, vt = ora.form_patch(d, np.zeros_like(d), m)
+        res = np.linalg.norm(d - u @ vt)
+        assert abs(res - math.sqrt(max(lam[m:].sum(), 0.0))) < 1e-9 * np.linalg.norm(d)
+        # no other rank-m product of random factors does better
+        q = RNG.standard_normal((T, m)) @ RNG.standard_normal((m, W))
+        a = np.linalg.lstsq(q.reshape(-1, 1), d.reshape(-1), rcond=None)[0]
+        assert res <= np.linalg.norm(d - a * q) + 1e-12
+
+
+def test_patch_added_after_rotation_not_rotated():
+    # a patch that only touches one rope pair: rotating it too would change the result
+    lay, it = gqa_item(L=1, T=2, H=1, hd=4, m=1, l0=0, l1=1, delta=3, float_factors=True)
+    it.patch_u = np.zeros((1, 2, 2, 1)); it.patch_u[0, 0, :, 0] = 1.0
+    it.patch_vt = np.zeros((1, 1 * 2 * 4)); it.patch_vt[0, 0] = 1.0  # K column 0 only
+    vals, _ = ora.reuse_layer(lay, it, 0, 0)
+    rot = ora.rotate_band(ora.bf16_to_f64(it.canon_k[0]), 3, 1e4, ora.NEOX_HALF)
+    np.testing.assert_allclose(vals[:, 0], rot[:, 0] + 1.0, atol=1e-14)
+    np.testing.assert_allclose(vals[:, 1:], rot[:, 1:], atol=1e-14)
+
+
+# ------------------------------------------------------------------------------------------
+# MLA
+# ------------------------------------------------------------------------------------------
+
+def mla_item(L=3, T=5, latent=16, rope=8, m=2, l0=1, l1=2, delta=0):
+    from types import SimpleNamespace
+    lay = SimpleNamespace(kind=ora.MLA, num_layers=L, page_size=4, num_kv_heads=0, head_dim=0,
+                          latent_dim=latent, rope_dim=rope, rope_style=ora.NEOX_HALF,
+                          rope_theta=1e4)
+    k = rand_bf16_bits((L, T, latent + rope))
+    pu = rand_bf16_bits((l1 - l0, 2, T, m))
+    pv = rand_bf16_bits((l1 - l0, m * (latent + rope)), 0.1)
+    return lay, ora.as_item(canon_k=k, patch_u=pu, patch_vt=pv, delta=delta, patch_m=m,
+                            patch_l0=l0, patch_l1=l1)
+
+
+def test_mla_latent_copied_byte_exact_and_only_kpe_turns():
+    lay, it = mla_item(delta=-4321)
+    for layer in (0, 2):  # unpatched layers
+        out = ora.reuse_layer_bits(lay, it, layer, 0)
+        np.testing.assert_array_equal(out[:, :16], it.canon_k[layer][:, :16])
+        assert np.mean(out[:, 16:] != it.canon_k[layer][:, 16:]) > 0.5
+
+
+def test_mla_latent_independent_of_delta():
+    lay, a = mla_item(delta=5)
+    b = ora.as_item(**{**vars(a), "delta": -9999})
+    for layer in range(3):
+        oa = ora.reuse_layer_bits(lay, a, layer, 0)
+        ob = ora.reuse_layer_bits(lay, b, layer, 0)
+        np.testing.assert_array_equal(oa[:, :16], ob[:, :16])
+        assert not np.array_equal(oa[:, 16:], ob[:, 16:])
+
+
+def test_mla_kpe_band_gets_its_own_patch_group():
+    lay, it = mla_item(delta=0, m=2, l0=0, l1=3)
+    vals, _ = ora.reuse_layer(lay, it, 1, 0)
+    x = ora.bf16_to_f64(it.canon_k[1])
+    u = ora.bf16_to_f64(it.patch_u[1])
+    vt = ora.bf16_to_f64(it.patch_vt[1])
+    for t in range(5):
+        for c in range(24):
+            g, cc, w = (0, c, 16) if c < 16 else (1, c - 16, 8)
+            off = 0 if g == 0 else 2 * 16
+            want = x[t, c] + sum(u[g, t, j] * vt[off + j * w + cc] for j in range(2))
+            assert abs(vals[t, c] - want) < 1e-12
+
+
+# ------------------------------------------------------------------------------------------
+# slots and the pool
+# ------------------------------------------------------------------------------------------
+
+def test_slots_match_independent_page_expansion():
+    ps = 16
+    pt = RNG.permutation(40).reshape(5, 8).astype(np.int32)
+    flat = (pt[:, :, None].astype(np.int64) * ps + np.arange(ps)).reshape(5, -1)
+    for r in range(5):
+        for t in range(8 * ps):
+            assert ora.slot_of(pt, r, t, ps) == flat[r, t]
+
+
+def test_identity_mode_scatter_is_byte_exact():
+    # δ = 0, m = 0, canonicals encode (item, layer, token): the pool must equal a scatter
+    # built from the page expansion; every other slot keeps the sentinel.
+    ps, L, H, hd = 4, 2, 1, 8
+    lay = ns_layout(num_layers=L, page_size=ps, num_kv_heads=H, head_dim=hd, rope_dim=hd)
+    W = H * hd
+    pt = RNG.permutation(12).reshape(2, 6).astype(np.int32)
+    flat = (pt[:, :, None].astype(np.int64) * ps + np.arange(ps)).reshape(2, -1)
+    k_pool = np.full((L, 48, W), 0x5A5A, np.uint16)
+    v_pool = k_pool.copy()
+    want_k, want_v = k_pool.copy(), v_pool.copy()
+    items = []
+    for i, (req, start, T) in enumerate([(0, 0, 7), (0, 9, 5), (1, 3, 13)]):
+        code = lambda ch: np.array([[[(i << 12) | (l << 10) | (t << 3) | (c & 7) | (ch << 15)
+                                      for c in range(W)] for t in range(T)] for l in range(L)],
+                                   dtype=np.uint16)
+        k, v = code(0), code(1)
+        items.append(ora.as_item(canon_k=k, canon_v=v, delta=0, req=req, start_tok=start,
+                                 num_tokens=T))
+        for l in range(L):
+            for t in range(T):
+                want_k[l, flat[req, start + t]] = k[l, t]
+                want_v[l, flat[req, start + t]] = v[l, t]
+    ora.batch_reuse(lay, items, k_pool, v_pool, pt)
+    np.testing.assert_array_equal(k_pool, want_k)
+    np.testing.assert_array_equal(v_pool, want_v)
+
+
+def test_relocate_in_place_rotates_only_rope_columns():
+    from types import SimpleNamespace
+    lay = SimpleNamespace(kind=ora.MLA, num_layers=2, page_size=4, num_kv_heads=0,
+                          head_dim=0, latent_dim=8, rope_dim=8, rope_style=ora.INTERLEAVED,
+                          rope_theta=1e4)
+    pool = rand_bf16_bits((2, 16, 16))
+    before = pool.copy()
+    pt = np.array([[3, 1, 0, 2]], np.int32)
+    ora.relocate(lay, pool, pt, 0, 2, 9, -576)
+    touched = {ora.slot_of(pt, 0, t, 4) for t in range(2, 11)}
+    for s in range(16):
+        np.testing.assert_array_equal(pool[:, s, :8], before[:, s, :8])
+        if s not in touched:
+            np.testing.assert_array_equal(pool[:, s], before[:, s])
+        else:
+            for l in range(2):
+                want = ora.f64_to_bf16(ora.rotate_band(ora.bf16_to_f64(before[l, s, 8:]), -576,
+                                                       1e4, ora.INTERLEAVED))
+                np.testing.assert_array_equal(pool[l, s, 8:], want)
+
+
+# ------------------------------------------------------------------------------------------
+# shapes and sizes printed on the pages
+# ------------------------------------------------------------------------------------------
+
+def read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("|")[0].strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split("=")
+            out[k.strip()] = int(v)
+    return out
+
+
+def test_layout_reading_matches_printed_shapes():
+    g = read_golden("pages_shapes.txt")
+    qwen = ns_layout(num_kv_heads=g["qwen25vl_kv_heads"], head_dim=g["qwen25vl_head_dim"],
+                     rope_dim=g["qwen25vl_head_dim"])
+    row_k, row_v, (w0, w1) = ora.widths(qwen)
+    assert row_k == row_v == w0 == w1 == g["qwen25vl_k_width"]
+    bands = ora.rope_bands(qwen)
+    assert all(len(ora.rope_pairs(d, ora.NEOX_HALF)[0]) == g["qwen25vl_rope_pairs_per_head"]
+               for _, d in bands)
+    q3 = ns_layout(num_kv_heads=g["qwen3vl_kv_heads"], head_dim=128, rope_dim=128)
+    assert ora.widths(q3)[0] == g["qwen3vl_k_width"]
+    from types import SimpleNamespace
+    kimi = SimpleNamespace(kind=ora.MLA, num_kv_heads=0, head_dim=0,
+                           latent_dim=g["kimivl_ckv_dim"], rope_dim=g["kimivl_krope_dim"])
+    row, _, (c, r) = ora.widths(kimi)
+    assert (c, r) == (512, 64) and row == 576
+    (c0, d), = ora.rope_bands(kimi)
+    assert c0 == 512 and len(ora.rope_pairs(d, ora.NEOX_HALF)[0]) == g["kimivl_krope_pairs"]
+
+
+def test_patch_byte_fraction_matches_printed_values():
+    with open(os.path.join(GOLDEN, "patch_fraction.txt")) as f:
+        rows = [l.split("|")[0] for l in f if l.strip() and not l.startswith("#")]
+    for r in rows:
+        m, frac, tol = (float(x) for x in r.split(","))
+        assert abs(ora.patch_byte_fraction(512, 512, int(m)) - frac) <= tol
