@@ -1,0 +1,191 @@
+/*
+ * kamera.h — C ABI of the Kamera relocate + patch operator for NVIDIA GB300 (sm_103a).
+ *
+ * The operator is Eq. 1 of "Kamera: Unified Position-Invariant Multimodal KV Cache for
+ * Training-Free Reuse" (§1, §3):
+ *
+ *     KV^(B|A) = R(delta) * KV(B|empty) + U_m * V_m^T
+ *
+ * R(delta) re-rotates the RoPE phase of a chunk's stored (canonical) keys by the integer offset
+ * delta = p1 - p0 (§3 "Relocate"; exact because RoPE composes, R(delta)R(p0) = R(p1)); values
+ * and the MLA latent are never rotated. U_m V_m^T is the rank-m conditioning patch formed at
+ * compile time from the top-m SVD of the deficit (§3 "Forming and applying the patch";
+ * App. A). The serve step applies both and writes the result into a paged KV pool (App. A
+ * "apply_reuse": a per-layer RoPE rotation plus a GEMM into the paged KV cache).
+ *
+ * Conventions shared by every call:
+ *   - All tensors are device memory owned by the caller. The library allocates nothing, keeps
+ *     no pointer after a call returns and never modifies the canonical or patch stores.
+ *   - bf16 everywhere for data; float32 arithmetic inside, one round-to-nearest-even to bf16.
+ *   - Calls are asynchronous on the given stream (NULL = the legacy default stream).
+ *   - Host-checkable errors return synchronously and launch nothing.
+ *   - Device-detected errors never trap: the affected rows are not written and a bit is ORed
+ *     into the caller's device status word (KAMERA_DEVICE_*). Read it after the stream syncs.
+ *   - Destinations of different tokens must not overlap (two tokens mapped to one slot give an
+ *     unspecified winner).
+ */
+#ifndef KAMERA_H
+#define KAMERA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* The same object as cudaStream_t. */
+typedef struct CUstream_st *kamera_stream_t;
+
+typedef enum kamera_status {
+  KAMERA_OK = 0,
+  KAMERA_ERR_INVALID_ARG = 1, /* a bad pointer, size, index or descriptor field         */
+  KAMERA_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels implement      */
+  KAMERA_ERR_CUDA = 3         /* a CUDA runtime call failed (launch, attribute, device)  */
+} kamera_status;
+
+/* Bits ORed into the device status word. */
+#define KAMERA_DEVICE_SLOT_OOB 0x1u /* a page id or page index fell outside the pool or the
+                                       page table; that token's row was not written          */
+#define KAMERA_DEVICE_BAD_ITEM 0x2u /* kamera_batch_reuse: an item failed the checks that
+                                       kamera_reuse makes on the host; none of it was written */
+
+/* Attention families (§3 "One mechanism for MLA, GQA, and MHA"). MHA is GQA with one KV head
+ * per query head. */
+#define KAMERA_GQA 0
+#define KAMERA_MLA 1
+
+/* RoPE pairing inside a rope band of width d (the pages do not fix it; both are served):
+ * NEOX_HALF pairs dim i with dim i + d/2, INTERLEAVED pairs 2i with 2i+1; pair i turns at
+ * inv_freq_i = theta^(-2i/d). */
+#define KAMERA_ROPE_NEOX_HALF 0
+#define KAMERA_ROPE_INTERLEAVED 1
+
+/*
+ * Layout descriptor: the content | rope split of §3 and Fig. 2.
+ *   GQA/MHA: K row = V row = num_kv_heads * head_dim; every K head rotates over its whole
+ *            head_dim (rope_dim must equal head_dim); V never rotates.
+ *   MLA:     one row = latent_dim (c_KV, never rotated) followed by rope_dim (the decoupled
+ *            k_pe band, rotated); there is no V tensor.
+ * Patch groups (one rank-m patch each, per patched layer): GQA group 0 = K (width W0 =
+ * num_kv_heads*head_dim), group 1 = V (W1 = W0); MLA group 0 = c_KV (W0 = latent_dim),
+ * group 1 = k_pe (W1 = rope_dim).
+ * Limits: head_dim, latent_dim, rope_dim multiples of 16; rope_dim <= 256; rows <= 16384.
+ */
+typedef struct kamera_layout {
+  int32_t kind;         /* KAMERA_GQA or KAMERA_MLA                                       */
+  int32_t num_layers;   /* L >= 1                                                         */
+  int32_t page_size;    /* tokens per page >= 1                                           */
+  int32_t num_kv_heads; /* GQA: H_kv >= 1; MLA: ignored                                   */
+  int32_t head_dim;     /* GQA: head dim; MLA: ignored                                    */
+  int32_t latent_dim;   /* MLA: c_KV width; GQA: ignored                                  */
+  int32_t rope_dim;     /* GQA: == head_dim; MLA: k_pe width (64 for DeepSeek-V2-style)   */
+  int32_t rope_style;   /* KAMERA_ROPE_*                                                  */
+  double rope_theta;    /* RoPE base theta > 1                                            */
+} kamera_layout;
+
+/*
+ * One chunk placement (App. A "apply_reuse(stored, delta, U, V, layer)" for all layers).
+ * canon_k : bf16 [L][T][row_k] canonical keys KV(B|empty), stored rotated at p0 (MLA: the
+ *           whole c_KV || k_pe row).
+ * canon_v : bf16 [L][T][row_v] canonical values (GQA); must be NULL for MLA.
+ * patch_u : bf16 [l1-l0][2][T][m]: U*Sigma of group 0 then group 1, per patched layer.
+ * patch_vt: bf16 [l1-l0][m*W0 + m*W1]: per patched layer V_m^T of group 0 ([m][W0],
+ *           row-major) followed by V_m^T of group 1 ([m][W1]).
+ *           Both patch pointers are ignored when patch_m == 0 or patch_l0 == patch_l1.
+ * delta   : p1 - p0, any sign (|delta| < 2^62).
+ * num_tokens, req, start_tok: the chunk's T tokens go to logical tokens
+ *           [start_tok, start_tok + T) of page-table row req.
+ * patch_m : rank, 0 (no patch) or 1..128. Layers in [patch_l0, patch_l1) get the patch.
+ * All pointers 16-byte aligned.
+ */
+typedef struct kamera_item {
+  const void *canon_k;
+  const void *canon_v;
+  const void *patch_u;
+  const void *patch_vt;
+  int64_t delta;
+  int32_t num_tokens;
+  int32_t req;
+  int32_t start_tok;
+  int32_t patch_m;
+  int32_t patch_l0;
+  int32_t patch_l1;
+} kamera_item;
+
+/*
+ * The paged KV pool (§6: the engine's paged KV pool; page size 16 in the reference workloads).
+ * k, v      : bf16 [L][num_slots][row]; v is NULL for MLA. 16-byte aligned.
+ * num_slots : slots per layer; a multiple of page_size.
+ * page_table: int32 [num_reqs][pt_stride] of physical page ids; logical token t of request r
+ *             lives at slot page_table[r][t / page_size] * page_size + t % page_size.
+ * All device memory, read by the kernels only (page_table) or written (k, v).
+ */
+typedef struct kamera_pool {
+  void *k;
+  void *v;
+  int64_t num_slots;
+  const int32_t *page_table;
+  int32_t num_reqs;
+  int32_t pt_stride;
+} kamera_pool;
+
+typedef struct kamera_handle kamera_handle;
+
+/* Validate a layout and precompute its RoPE frequencies (host only; touches no device).
+ * Returns INVALID_ARG / UNSUPPORTED for a bad layout. *out must be freed by kamera_destroy. */
+kamera_status kamera_create(const kamera_layout *layout, kamera_handle **out);
+
+/* Free a handle (NULL is accepted). */
+kamera_status kamera_destroy(kamera_handle *handle);
+
+/* Short English text for a status code (static storage). */
+const char *kamera_status_string(kamera_status status);
+
+/*
+ * Survivor relocation, in place (§5 "Sliding-window survival": keep the survivor's KV as-is
+ * and apply R(delta); Fig. 2: rotate_k_pe_inplace). Rotates the rope columns of K (GQA/MHA:
+ * every head; MLA: the k_pe band only) of logical tokens [start_tok, start_tok+num_tokens)
+ * of request req by delta. V and c_KV are neither read nor written. delta == 0 or
+ * num_tokens == 0 launches nothing.
+ */
+kamera_status kamera_relocate(const kamera_handle *handle, const kamera_pool *pool, int32_t req,
+                              int32_t start_tok, int32_t num_tokens, int64_t delta,
+                              uint32_t *d_status, kamera_stream_t stream);
+
+/*
+ * Reorder / recall of one chunk (§5 "Reorder", "Recall"): canonical -> pool with rotation and
+ * patch, every layer, K and V (or the MLA row). The item lives in host memory and is checked
+ * on the host.
+ */
+kamera_status kamera_reuse(const kamera_handle *handle, const kamera_item *item,
+                           const kamera_pool *pool, uint32_t *d_status, kamera_stream_t stream);
+
+/*
+ * Many chunks and requests in one launch. d_items is a device array of num_items items; the
+ * host cannot see them, so each is checked on the device against the same rules as
+ * kamera_reuse plus num_tokens <= max_tokens and patch_m <= max_patch_m (a failing item sets
+ * KAMERA_DEVICE_BAD_ITEM and is skipped). max_tokens sizes the grid; max_patch_m picks the
+ * kernel (0..128).
+ */
+kamera_status kamera_batch_reuse(const kamera_handle *handle, const kamera_item *d_items,
+                                 int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
+                                 const kamera_pool *pool, uint32_t *d_status,
+                                 kamera_stream_t stream);
+
+/*
+ * The RoPE phases the kernels use: for each of num_deltas offsets d_deltas[n] (device int64)
+ * and each rope pair i of the layout, (cos, sin) of delta * inv_freq_i with inv_freq_i =
+ * theta^(-2i/d), written as float32 pairs to d_out[n][rope_dim/2][2] (device). The angle is
+ * range-reduced exactly (a Q0.64 fixed-point product modulo one turn) before a float32
+ * sincospi, so large |delta| loses no accuracy (§3 "Relocate" re-rotates by delta;
+ * inv_freq from the standard RoPE of Su et al.). Offsets with |delta| > 2^62 give NaN.
+ */
+kamera_status kamera_rope_phases(const kamera_handle *handle, const int64_t *d_deltas,
+                                 int32_t num_deltas, float *d_out, kamera_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KAMERA_H */

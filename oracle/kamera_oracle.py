@@ -225,8 +225,8 @@ def reuse_layer_bits(layout, item, layer: int, channel: int, tokens=None) -> np.
 
 
 def magnitude_layer(layout, item, layer: int, channel: int, tokens=None) -> np.ndarray:
-    """Sum of the magnitudes of the terms that make each result element:
-    |a cos φ| + |b sin φ| on rotated pairs (|x| elsewhere) plus Σ_j |U_tj · Vt_jc|.
+    """Scale of the terms that make each result element: |a| + |b| on rotated pairs (an error
+    in cos φ or sin φ multiplies both pair members), |x| elsewhere, plus Σ_j |U_tj · Vt_jc|.
     Float rounding errors of any evaluation order are bounded by a multiple of this."""
     canon = item.canon_k if channel == 0 else item.canon_v
     rows = np.asarray(canon[layer])
@@ -236,12 +236,10 @@ def magnitude_layer(layout, item, layer: int, channel: int, tokens=None) -> np.n
     mag = np.abs(x)
     if channel == 0 and item.delta != 0:
         for c0, d in rope_bands(layout):
-            phi = float(item.delta) * inv_freq(layout.rope_theta, d)
-            c, s = np.abs(np.cos(phi)), np.abs(np.sin(phi))
             ia, ib = rope_pairs(d, layout.rope_style)
-            a, b = np.abs(x[:, c0 + ia]), np.abs(x[:, c0 + ib])
-            mag[:, c0 + ia] = a * c + b * s
-            mag[:, c0 + ib] = b * c + a * s
+            ab = np.abs(x[:, c0 + ia]) + np.abs(x[:, c0 + ib])
+            mag[:, c0 + ia] = ab
+            mag[:, c0 + ib] = ab
     if layer_patched(item, layer):
         m = item.patch_m
         li = layer - item.patch_l0

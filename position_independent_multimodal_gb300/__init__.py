@@ -1,0 +1,13 @@
+"""Kamera relocate + patch operator for NVIDIA GB300 (sm_103a).
+
+``KV^(B|A) = R(δ)·KV(B|∅) + U_m·V_mᵀ`` written into a paged KV pool, as hand-written CUDA
+kernels behind a C ABI (include/kamera.h). This package is the Python binding: it marshals
+PyTorch tensors into the C calls and nothing more. Build the library with ``build.build()``.
+"""
+from ._binding import (  # noqa: F401
+    ITEM_BYTES, KAMERA_DEVICE_BAD_ITEM, KAMERA_DEVICE_SLOT_OOB, KAMERA_ERR_CUDA,
+    KAMERA_ERR_INVALID_ARG, KAMERA_ERR_UNSUPPORTED, KAMERA_GQA, KAMERA_MLA, KAMERA_OK,
+    KAMERA_ROPE_INTERLEAVED, KAMERA_ROPE_NEOX_HALF, LIB_PATH, Handle, KameraError, Pool,
+    create, kamera_batch_reuse, kamera_relocate, kamera_reuse, kamera_rope_phases, lib, make_item, make_layout,
+    pack_items, status_string,
+)

@@ -1,0 +1,198 @@
+"""Thin ctypes binding of libkamera.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/kamera.h) and does
+nothing but convert PyTorch tensors and Python numbers into pointers and sizes. All work runs
+in the CUDA kernels; if the library is missing or a call fails, an exception is raised: there
+is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkamera.so")
+
+KAMERA_OK = 0
+KAMERA_ERR_INVALID_ARG = 1
+KAMERA_ERR_UNSUPPORTED = 2
+KAMERA_ERR_CUDA = 3
+KAMERA_DEVICE_SLOT_OOB = 0x1
+KAMERA_DEVICE_BAD_ITEM = 0x2
+KAMERA_GQA = 0
+KAMERA_MLA = 1
+KAMERA_ROPE_NEOX_HALF = 0
+KAMERA_ROPE_INTERLEAVED = 1
+
+
+class KameraError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+class kamera_layout(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("latent_dim", ctypes.c_int32),
+                ("rope_dim", ctypes.c_int32), ("rope_style", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double)]
+
+
+class kamera_item(ctypes.Structure):
+    _fields_ = [("canon_k", ctypes.c_void_p), ("canon_v", ctypes.c_void_p),
+                ("patch_u", ctypes.c_void_p), ("patch_vt", ctypes.c_void_p),
+                ("delta", ctypes.c_int64), ("num_tokens", ctypes.c_int32),
+                ("req", ctypes.c_int32), ("start_tok", ctypes.c_int32),
+                ("patch_m", ctypes.c_int32), ("patch_l0", ctypes.c_int32),
+                ("patch_l1", ctypes.c_int32)]
+
+
+class kamera_pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+                ("page_table", ctypes.c_void_p), ("num_reqs", ctypes.c_int32),
+                ("pt_stride", ctypes.c_int32)]
+
+
+ITEM_BYTES = ctypes.sizeof(kamera_item)
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkamera.so (built in-tree by ``build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "position_independent_multimodal_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.kamera_create.argtypes = [ctypes.POINTER(kamera_layout), ctypes.POINTER(vp)]
+        L.kamera_destroy.argtypes = [vp]
+        L.kamera_status_string.argtypes = [ctypes.c_int]
+        L.kamera_status_string.restype = ctypes.c_char_p
+        L.kamera_relocate.argtypes = [vp, ctypes.POINTER(kamera_pool), i32, i32, i32, i64, vp, vp]
+        L.kamera_reuse.argtypes = [vp, ctypes.POINTER(kamera_item), ctypes.POINTER(kamera_pool),
+                                   vp, vp]
+        L.kamera_batch_reuse.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(kamera_pool), vp,
+                                         vp]
+        L.kamera_rope_phases.argtypes = [vp, vp, i32, vp, vp]
+        for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
+                  "kamera_batch_reuse", "kamera_rope_phases"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kamera_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != KAMERA_OK:
+        raise KameraError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_layout(layout) -> kamera_layout:
+    """Any object with the descriptor's fields -> the C struct."""
+    return kamera_layout(int(layout.kind), int(layout.num_layers), int(layout.page_size),
+                         int(layout.num_kv_heads), int(layout.head_dim), int(layout.latent_dim),
+                         int(layout.rope_dim), int(layout.rope_style), float(layout.rope_theta))
+
+
+class Handle:
+    """Owns a kamera_handle (created by kamera_create, freed by kamera_destroy)."""
+
+    def __init__(self, layout):
+        self.layout = layout
+        self._c = make_layout(layout)
+        h = ctypes.c_void_p()
+        _check(lib().kamera_create(ctypes.byref(self._c), ctypes.byref(h)), "kamera_create")
+        self.ptr = h
+
+    def close(self):
+        if self.ptr:
+            lib().kamera_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def create(layout) -> Handle:
+    return Handle(layout)
+
+
+class Pool:
+    """The paged pool: k, v tensors [L][num_slots][row] and the int32 page table."""
+
+    def __init__(self, k: torch.Tensor, v: Optional[torch.Tensor], page_table: torch.Tensor,
+                 num_slots: Optional[int] = None):
+        self.k, self.v, self.page_table = k, v, page_table
+        self.num_slots = int(num_slots if num_slots is not None else k.shape[1])
+
+    def c(self) -> kamera_pool:
+        pt = self.page_table
+        return kamera_pool(_ptr(self.k), _ptr(self.v), self.num_slots, _ptr(pt),
+                           int(pt.shape[0]), int(pt.stride(0)))
+
+
+def make_item(it) -> kamera_item:
+    """An object with the kamera_item fields (tensors for the pointers) -> the C struct."""
+    return kamera_item(_ptr(it.canon_k), _ptr(getattr(it, "canon_v", None)),
+                       _ptr(getattr(it, "patch_u", None)), _ptr(getattr(it, "patch_vt", None)),
+                       int(it.delta), int(it.num_tokens), int(it.req), int(it.start_tok),
+                       int(getattr(it, "patch_m", 0)), int(getattr(it, "patch_l0", 0)),
+                       int(getattr(it, "patch_l1", 0)))
+
+
+def pack_items(items: Sequence) -> torch.Tensor:
+    """Pack items into a host uint8 tensor of ``len(items) * sizeof(kamera_item)`` bytes."""
+    arr = (kamera_item * len(items))(*[make_item(it) for it in items])
+    return torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8)
+
+
+def kamera_relocate(handle: Handle, pool: Pool, req: int, start_tok: int, num_tokens: int,
+                    delta: int, status: torch.Tensor, stream=None) -> None:
+    p = pool.c()
+    _check(lib().kamera_relocate(handle.ptr, ctypes.byref(p), int(req), int(start_tok),
+                                 int(num_tokens), int(delta), _ptr(status), _stream(stream)),
+           "kamera_relocate")
+
+
+def kamera_reuse(handle: Handle, item, pool: Pool, status: torch.Tensor, stream=None) -> None:
+    c = make_item(item)
+    p = pool.c()
+    _check(lib().kamera_reuse(handle.ptr, ctypes.byref(c), ctypes.byref(p), _ptr(status),
+                              _stream(stream)), "kamera_reuse")
+
+
+def kamera_batch_reuse(handle: Handle, d_items: torch.Tensor, num_items: int, max_tokens: int,
+                       max_patch_m: int, pool: Pool, status: torch.Tensor, stream=None) -> None:
+    p = pool.c()
+    _check(lib().kamera_batch_reuse(handle.ptr, _ptr(d_items), int(num_items), int(max_tokens),
+                                    int(max_patch_m), ctypes.byref(p), _ptr(status),
+                                    _stream(stream)), "kamera_batch_reuse")
+
+
+def kamera_rope_phases(handle: Handle, d_deltas: torch.Tensor, d_out: torch.Tensor,
+                       stream=None) -> None:
+    """(cos, sin) per (delta, pair) into ``d_out`` float32 [n][rope_dim/2][2]."""
+    _check(lib().kamera_rope_phases(handle.ptr, _ptr(d_deltas), int(d_deltas.numel()),
+                                    _ptr(d_out), _stream(stream)), "kamera_rope_phases")

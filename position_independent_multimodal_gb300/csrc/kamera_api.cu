@@ -1,0 +1,240 @@
+// Host side of the Kamera C ABI: descriptor checks, RoPE frequency precomputation, argument
+// checks and kernel launches. See include/kamera.h for the contract of every call.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "kamera_dev.cuh"
+
+struct kamera_handle {
+  kamera_layout desc;
+  kamera::DevLayout lay;
+  kamera::FreqQ64 freq;
+};
+
+namespace kamera {
+int reuse_stream_tile();
+}
+
+namespace {
+
+using kamera::DevLayout;
+using kamera::DevPool;
+
+bool is_mult16(int x) { return x > 0 && (x % 16) == 0; }
+
+kamera_status fill_layout(const kamera_layout &d, DevLayout *out) {
+  DevLayout l{};
+  if (d.num_layers < 1 || d.page_size < 1) return KAMERA_ERR_INVALID_ARG;
+  if (!(d.rope_theta > 1.0) || !std::isfinite(d.rope_theta)) return KAMERA_ERR_INVALID_ARG;
+  if (d.rope_style != KAMERA_ROPE_NEOX_HALF && d.rope_style != KAMERA_ROPE_INTERLEAVED)
+    return KAMERA_ERR_INVALID_ARG;
+  l.kind = d.kind;
+  l.L = d.num_layers;
+  l.page_size = d.page_size;
+  l.style = d.rope_style;
+  if (d.kind == KAMERA_GQA) {
+    if (d.num_kv_heads < 1 || d.head_dim < 1) return KAMERA_ERR_INVALID_ARG;
+    if (d.rope_dim != d.head_dim) return KAMERA_ERR_UNSUPPORTED;  // partial rotary
+    if (!is_mult16(d.head_dim) || d.head_dim > 2 * kamera::kMaxPairs)
+      return KAMERA_ERR_UNSUPPORTED;
+    if ((long long)d.num_kv_heads * d.head_dim > kamera::kMaxRow) return KAMERA_ERR_UNSUPPORTED;
+    l.H = d.num_kv_heads;
+    l.hd = d.head_dim;
+    l.rope_d = d.head_dim;
+    l.latent = 0;
+    l.row_k = l.row_v = l.H * l.hd;
+    l.w0 = l.w1 = l.row_k;
+    l.n_ch = 2;
+  } else if (d.kind == KAMERA_MLA) {
+    if (d.latent_dim < 1 || d.rope_dim < 1) return KAMERA_ERR_INVALID_ARG;
+    if (!is_mult16(d.latent_dim) || !is_mult16(d.rope_dim) ||
+        d.rope_dim > 2 * kamera::kMaxPairs)
+      return KAMERA_ERR_UNSUPPORTED;
+    if (d.latent_dim + d.rope_dim > kamera::kMaxRow) return KAMERA_ERR_UNSUPPORTED;
+    l.H = 0;
+    l.hd = 0;
+    l.latent = d.latent_dim;
+    l.rope_d = d.rope_dim;
+    l.row_k = d.latent_dim + d.rope_dim;
+    l.row_v = 0;
+    l.w0 = d.latent_dim;
+    l.w1 = d.rope_dim;
+    l.n_ch = 1;
+  } else {
+    return KAMERA_ERR_INVALID_ARG;
+  }
+  l.npairs = l.rope_d / 2;
+  *out = l;
+  return KAMERA_OK;
+}
+
+// 1/(2 pi) as an unevaluated sum of two doubles (106 significant bits).
+constexpr double kInvTwoPiHi = 0.15915494309189535;
+constexpr double kInvTwoPiLo = -9.839338337591243e-18;
+
+// q_i = round(inv_freq_i / (2 pi) * 2^64), inv_freq_i = theta^(-2i/d) in double. The product
+// with 1/(2 pi) is carried in two doubles (exact product by fma, plus the low constant), so
+// q_i is the double inv_freq_i over 2 pi to within half a unit of 2^-64: a relocation by
+// delta then carries at most |delta| * 2^-65 turns of error from the table.
+void fill_freq(const kamera_layout &d, const DevLayout &l, kamera::FreqQ64 *f) {
+  std::memset(f, 0, sizeof(*f));
+  for (int i = 0; i < l.npairs; ++i) {
+    const double inv = std::pow(d.rope_theta, -2.0 * i / l.rope_d);
+    const double x = std::ldexp(inv, 64);                 // exact scaling, < 2^64
+    const double p = x * kInvTwoPiHi;                     // < 2^62
+    const double e = std::fma(x, kInvTwoPiHi, -p) + x * kInvTwoPiLo;
+    const double ip = std::floor(p);
+    const long long frac = std::llround((p - ip) + e);    // p - ip is exact
+    f->q[i] = static_cast<unsigned long long>(ip) + static_cast<unsigned long long>(frac);
+  }
+}
+
+kamera_status check_pool(const DevLayout &l, const kamera_pool *p, DevPool *out) {
+  if (!p) return KAMERA_ERR_INVALID_ARG;
+  if (!p->k || !kamera::aligned16(p->k)) return KAMERA_ERR_INVALID_ARG;
+  if (l.kind == KAMERA_GQA) {
+    if (!p->v || !kamera::aligned16(p->v)) return KAMERA_ERR_INVALID_ARG;
+  } else if (p->v) {
+    return KAMERA_ERR_INVALID_ARG;
+  }
+  if (p->num_slots <= 0 || p->num_slots % l.page_size != 0) return KAMERA_ERR_INVALID_ARG;
+  if (!p->page_table || p->num_reqs < 1 || p->pt_stride < 1) return KAMERA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(p->page_table) & 3u) != 0) return KAMERA_ERR_INVALID_ARG;
+  DevPool d;
+  d.k = static_cast<__nv_bfloat16 *>(p->k);
+  d.v = static_cast<__nv_bfloat16 *>(p->v);
+  d.num_slots = p->num_slots;
+  d.pt = p->page_table;
+  d.num_reqs = p->num_reqs;
+  d.pt_stride = p->pt_stride;
+  *out = d;
+  return KAMERA_OK;
+}
+
+kamera_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+kamera_status kamera_create(const kamera_layout *layout, kamera_handle **out) {
+  if (!layout || !out) return KAMERA_ERR_INVALID_ARG;
+  *out = nullptr;
+  DevLayout l;
+  const kamera_status st = fill_layout(*layout, &l);
+  if (st != KAMERA_OK) return st;
+  kamera_handle *h = new (std::nothrow) kamera_handle;
+  if (!h) return KAMERA_ERR_INVALID_ARG;
+  h->desc = *layout;
+  h->lay = l;
+  fill_freq(*layout, l, &h->freq);
+  *out = h;
+  return KAMERA_OK;
+}
+
+kamera_status kamera_destroy(kamera_handle *handle) {
+  delete handle;
+  return KAMERA_OK;
+}
+
+const char *kamera_status_string(kamera_status s) {
+  switch (s) {
+    case KAMERA_OK: return "ok";
+    case KAMERA_ERR_INVALID_ARG: return "invalid argument";
+    case KAMERA_ERR_UNSUPPORTED: return "unsupported layout or size";
+    case KAMERA_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+kamera_status kamera_relocate(const kamera_handle *h, const kamera_pool *pool, int32_t req,
+                              int32_t start_tok, int32_t num_tokens, int64_t delta,
+                              uint32_t *d_status, kamera_stream_t stream) {
+  if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
+  kamera::RelocArgs a;
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  if (num_tokens < 0 || start_tok < 0 || req < 0 || req >= pool->num_reqs)
+    return KAMERA_ERR_INVALID_ARG;
+  if ((long long)start_tok + num_tokens > (long long)pool->pt_stride * h->lay.page_size)
+    return KAMERA_ERR_INVALID_ARG;
+  if (delta > (1ll << 62) || delta < -(1ll << 62)) return KAMERA_ERR_INVALID_ARG;
+  if (num_tokens == 0 || delta == 0) return KAMERA_OK;  // R(0) = I
+  a.req = req;
+  a.start_tok = start_tok;
+  a.T = num_tokens;
+  a.delta = delta;
+  a.status = d_status;
+  a.freq = h->freq;
+  return from_cuda(kamera::launch_relocate(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
+                           const kamera_pool *pool, uint32_t *d_status, kamera_stream_t stream) {
+  if (!h || !item || !d_status) return KAMERA_ERR_INVALID_ARG;
+  kamera::ReuseArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  const int chk = kamera::item_check(*item, h->lay, a.pool, 1 << 30, kamera::kMaxRank);
+  if (chk != 0) return static_cast<kamera_status>(chk);
+  if (item->num_tokens == 0) return KAMERA_OK;
+  a.single = *item;
+  a.items = nullptr;
+  a.n_items = 1;
+  a.max_tokens = item->num_tokens;
+  a.max_m = item->patch_m;
+  a.status = d_status;
+  a.freq = h->freq;
+  const int tile = kamera::reuse_stream_tile();
+  const int tiles = (item->num_tokens + tile - 1) / tile;
+  return from_cuda(
+      kamera::launch_reuse_stream(a, tiles, 1, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_items,
+                                 int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
+                                 const kamera_pool *pool, uint32_t *d_status,
+                                 kamera_stream_t stream) {
+  if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
+  if (num_items < 0 || max_tokens < 0 || max_patch_m < 0) return KAMERA_ERR_INVALID_ARG;
+  if (max_patch_m > kamera::kMaxRank) return KAMERA_ERR_UNSUPPORTED;
+  kamera::ReuseArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  if (num_items == 0 || max_tokens == 0) return KAMERA_OK;
+  if (!d_items || (reinterpret_cast<uintptr_t>(d_items) & 7u)) return KAMERA_ERR_INVALID_ARG;
+  if (num_items > 65535) return KAMERA_ERR_UNSUPPORTED;
+  a.items = d_items;
+  a.n_items = num_items;
+  a.max_tokens = max_tokens;
+  a.max_m = max_patch_m;
+  a.status = d_status;
+  a.freq = h->freq;
+  const int tile = kamera::reuse_stream_tile();
+  const int tiles = (max_tokens + tile - 1) / tile;
+  if (tiles > 0x7FFFFFFF / 1) return KAMERA_ERR_UNSUPPORTED;
+  return from_cuda(
+      kamera::launch_reuse_stream(a, tiles, num_items, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,
+                                 int32_t num_deltas, float *d_out, kamera_stream_t stream) {
+  if (!h || num_deltas < 0) return KAMERA_ERR_INVALID_ARG;
+  if (num_deltas == 0) return KAMERA_OK;
+  if (!d_deltas || !d_out || (reinterpret_cast<uintptr_t>(d_deltas) & 7u) ||
+      (reinterpret_cast<uintptr_t>(d_out) & 3u))
+    return KAMERA_ERR_INVALID_ARG;
+  return from_cuda(kamera::launch_rope_phases(h->freq, h->lay.npairs,
+                                              reinterpret_cast<const long long *>(d_deltas),
+                                              num_deltas, d_out,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,261 @@
+// Internal definitions shared by the host API and the kernels of the Kamera library.
+//
+// Operator: Kamera (Unified Position-Invariant Multimodal KV Cache for Training-Free Reuse),
+// Eq. 1: KV^(B|A) = R(delta) * KV(B|empty) + U_m V_m^T, written into a paged KV pool.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kamera.h"
+
+namespace kamera {
+
+constexpr int kMaxPairs = 128;  // rope_dim <= 256
+constexpr int kMaxRank = 128;
+constexpr int kMaxRow = 16384;
+
+// Layout with every derived width spelled out (filled once by kamera_create).
+struct DevLayout {
+  int kind, L, page_size, H, hd, latent, rope_d, style;
+  int row_k, row_v;  // row widths of channel 0 (K, or c_KV || k_pe) and channel 1 (V)
+  int w0, w1;        // patch group widths
+  int npairs;        // rope pairs per band (rope_d / 2)
+  int n_ch;          // 2 for GQA (K, V), 1 for MLA
+};
+
+// Per-pair rotation speed in turns per token, as an unsigned Q0.64 fixed-point fraction:
+// q_i = round(inv_freq_i / (2 pi) * 2^64). The angle of offset delta is delta * q_i mod 2^64,
+// an exact modular product, so the range reduction of large |delta| loses nothing.
+struct FreqQ64 {
+  unsigned long long q[kMaxPairs];
+};
+
+struct DevPool {
+  __nv_bfloat16 *k;
+  __nv_bfloat16 *v;
+  long long num_slots;
+  const int32_t *pt;
+  int num_reqs, pt_stride;
+};
+
+struct ReuseArgs {
+  DevLayout lay;
+  DevPool pool;
+  kamera_item single;        // used when items == nullptr
+  const kamera_item *items;  // device array (batch)
+  int n_items;
+  int max_tokens;
+  int max_m;
+  unsigned *status;
+  FreqQ64 freq;
+};
+
+struct RelocArgs {
+  DevLayout lay;
+  DevPool pool;
+  int req, start_tok, T;
+  long long delta;
+  unsigned *status;
+  FreqQ64 freq;
+};
+
+// The rules an item must satisfy (host: kamera_reuse; device: each batch item).
+__host__ __device__ inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+__host__ __device__ inline int item_check(const kamera_item &it, const DevLayout &lay,
+                                          const DevPool &pool, int max_tokens, int max_m) {
+  // returns 0 when valid, else a kamera_status code
+  if (it.num_tokens < 0 || it.num_tokens > max_tokens) return KAMERA_ERR_INVALID_ARG;
+  if (it.patch_m < 0 || it.patch_m > kMaxRank) return KAMERA_ERR_UNSUPPORTED;
+  if (it.patch_m > max_m) return KAMERA_ERR_INVALID_ARG;
+  if (it.delta > (1ll << 62) || it.delta < -(1ll << 62)) return KAMERA_ERR_INVALID_ARG;
+  if (it.num_tokens == 0) return 0;
+  if (!it.canon_k || !aligned16(it.canon_k)) return KAMERA_ERR_INVALID_ARG;
+  if (lay.kind == KAMERA_GQA) {
+    if (!it.canon_v || !aligned16(it.canon_v)) return KAMERA_ERR_INVALID_ARG;
+  } else if (it.canon_v) {
+    return KAMERA_ERR_INVALID_ARG;
+  }
+  if (it.req < 0 || it.req >= pool.num_reqs || it.start_tok < 0) return KAMERA_ERR_INVALID_ARG;
+  if ((long long)it.start_tok + it.num_tokens > (long long)pool.pt_stride * lay.page_size)
+    return KAMERA_ERR_INVALID_ARG;
+  if (it.patch_m > 0) {
+    if (it.patch_l0 < 0 || it.patch_l1 < it.patch_l0 || it.patch_l1 > lay.L)
+      return KAMERA_ERR_INVALID_ARG;
+    if (it.patch_l1 > it.patch_l0) {
+      if (!it.patch_u || !it.patch_vt || !aligned16(it.patch_vt) ||
+          (reinterpret_cast<uintptr_t>(it.patch_u) & 1u))
+        return KAMERA_ERR_INVALID_ARG;
+    }
+  }
+  return 0;
+}
+
+__device__ __forceinline__ bool layer_patched(const kamera_item &it, int layer) {
+  return it.patch_m > 0 && layer >= it.patch_l0 && layer < it.patch_l1;
+}
+
+// cos/sin of delta * inv_freq_i: exact modular range reduction in Q0.64 turns, then the
+// CUDA single-precision sincospi on the reduced angle (|angle| <= pi).
+__device__ __forceinline__ float2 rope_phase(unsigned long long q, long long delta) {
+  const unsigned long long turns = static_cast<unsigned long long>(delta) * q;
+  const long long centred = static_cast<long long>(turns);   // [-1/2, 1/2) turn
+  const float x = static_cast<float>(centred) * 0x1p-63f;   // angle / pi in [-1, 1)
+  float s, c;
+  sincospif(x, &s, &c);
+  return make_float2(c, s);
+}
+
+// Physical slot of logical token tok of request req; -1 (and the OOB status bit) when the
+// page-table entry points outside the pool.
+__device__ __forceinline__ long long slot_of(const DevPool &p, int page_size, int req,
+                                             long long tok, unsigned *status) {
+  const long long pi = tok / page_size;
+  if (pi >= p.pt_stride) {
+    atomicOr(status, KAMERA_DEVICE_SLOT_OOB);
+    return -1;
+  }
+  const int page = __ldg(p.pt + (long long)req * p.pt_stride + pi);
+  if (page < 0 || (long long)(page + 1) * page_size > p.num_slots) {
+    atomicOr(status, KAMERA_DEVICE_SLOT_OOB);
+    return -1;
+  }
+  return (long long)page * page_size + tok % page_size;
+}
+
+// Columns are processed in units of 16: two 8-column (16-byte) chunks at ca and cb that are
+// closed under rope pairing. NeoX-half: chunk cb holds the partners (d/2 apart) of chunk ca.
+// Interleaved: each chunk pairs its own neighbours. Non-rope units: two consecutive chunks.
+struct ColUnit {
+  int ca, cb;    // first columns in the row
+  int rot;       // 0 none, 1 NeoX-half (xa[e] with xb[e]), 2 interleaved (within chunks)
+  int fa, fb;    // first frequency index of chunk a / b
+  int group;     // patch group
+  int gca, gcb;  // columns inside the patch group
+};
+
+__device__ __forceinline__ int units_per_row(const DevLayout &l, int ch) {
+  return (ch == 0 ? l.row_k : l.row_v) >> 4;
+}
+
+__device__ __forceinline__ ColUnit col_unit(const DevLayout &l, int ch, int u, bool rotate) {
+  ColUnit c;
+  if (l.kind == KAMERA_GQA) {
+    if (ch == 1 || !rotate) {
+      c.ca = u * 16;
+      c.cb = c.ca + 8;
+      c.rot = 0;
+      c.fa = c.fb = 0;
+    } else {
+      const int per_head = l.hd >> 4;
+      const int h = u / per_head, q = u - h * per_head;
+      if (l.style == KAMERA_ROPE_NEOX_HALF) {
+        c.ca = h * l.hd + 8 * q;
+        c.cb = c.ca + (l.hd >> 1);
+        c.rot = 1;
+        c.fa = 8 * q;
+        c.fb = 8 * q;
+      } else {
+        c.ca = h * l.hd + 16 * q;
+        c.cb = c.ca + 8;
+        c.rot = 2;
+        c.fa = 8 * q;
+        c.fb = 8 * q + 4;
+      }
+    }
+    c.group = ch;
+    c.gca = c.ca;
+    c.gcb = c.cb;
+  } else {
+    const int lat_units = l.latent >> 4;
+    if (u < lat_units) {
+      c.ca = u * 16;
+      c.cb = c.ca + 8;
+      c.rot = 0;
+      c.fa = c.fb = 0;
+      c.group = 0;
+      c.gca = c.ca;
+      c.gcb = c.cb;
+    } else {
+      const int r = u - lat_units;
+      if (!rotate) {
+        c.ca = l.latent + 16 * r;
+        c.cb = c.ca + 8;
+        c.rot = 0;
+        c.fa = c.fb = 0;
+      } else if (l.style == KAMERA_ROPE_NEOX_HALF) {
+        c.ca = l.latent + 8 * r;
+        c.cb = c.ca + (l.rope_d >> 1);
+        c.rot = 1;
+        c.fa = c.fb = 8 * r;
+      } else {
+        c.ca = l.latent + 16 * r;
+        c.cb = c.ca + 8;
+        c.rot = 2;
+        c.fa = 8 * r;
+        c.fb = 8 * r + 4;
+      }
+      c.group = 1;
+      c.gca = c.ca - l.latent;
+      c.gcb = c.cb - l.latent;
+    }
+  }
+  return c;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float *x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2_rn(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8_rn(const float *x) {
+  uint4 v;
+  v.x = pack2_rn(x[0], x[1]);
+  v.y = pack2_rn(x[2], x[3]);
+  v.z = pack2_rn(x[4], x[5]);
+  v.w = pack2_rn(x[6], x[7]);
+  return v;
+}
+
+// (a, b) -> (a cos - b sin, b cos + a sin)
+__device__ __forceinline__ void rot_pair(float &a, float &b, float2 cs) {
+  const float na = fmaf(a, cs.x, -b * cs.y);
+  const float nb = fmaf(b, cs.x, a * cs.y);
+  a = na;
+  b = nb;
+}
+
+__device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, float *xa,
+                                            float *xb) {
+  if (c.rot == 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rot_pair(xa[e], xb[e], cs[c.fa + e]);
+  } else if (c.rot == 2) {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      rot_pair(xa[e], xa[e + 1], cs[c.fa + (e >> 1)]);
+      rot_pair(xb[e], xb[e + 1], cs[c.fb + (e >> 1)]);
+    }
+  }
+}
+
+// Kernel launchers (kamera_stream.cu).
+cudaError_t launch_reuse_stream(const ReuseArgs &a, int tiles, int n_items, cudaStream_t s);
+cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);
+cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,
+                               float *out, cudaStream_t s);
+
+}  // namespace kamera

@@ -1,0 +1,182 @@
+"""The C ABI on the host (no GPU needed): the library builds, loads, exports every function
+include/kamera.h declares, its structs have the documented sizes, and the host-side checks
+reject bad arguments before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import position_independent_multimodal_gb300 as km
+from position_independent_multimodal_gb300 import _binding as kb
+from position_independent_multimodal_gb300 import build as kbuild
+import workloads as wl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return km.lib()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(HEADER):
+        if f.endswith(".h"):
+            src = open(os.path.join(HEADER, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:kamera_status|const char\s*\*)\s*(kamera_\w+)\s*\(",
+                                src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "kamera_batch_reuse" in names and "kamera_relocate" in names
+    assert "kamera_reuse" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_struct_sizes():
+    assert ctypes.sizeof(kb.kamera_item) == 64
+    assert ctypes.sizeof(kb.kamera_layout) == 40
+    assert ctypes.sizeof(kb.kamera_pool) == 40
+
+
+def gqa(**kw):
+    base = dict(kind=wl.GQA, num_layers=2, page_size=16, num_kv_heads=2, head_dim=64,
+                rope_dim=64, rope_style=wl.NEOX_HALF, rope_theta=1e4)
+    base.update(kw)
+    return wl.Layout(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_layers=0), km.KAMERA_ERR_INVALID_ARG),
+    (dict(page_size=0), km.KAMERA_ERR_INVALID_ARG),
+    (dict(rope_theta=1.0), km.KAMERA_ERR_INVALID_ARG),
+    (dict(rope_theta=float("nan")), km.KAMERA_ERR_INVALID_ARG),
+    (dict(rope_style=7), km.KAMERA_ERR_INVALID_ARG),
+    (dict(kind=5), km.KAMERA_ERR_INVALID_ARG),
+    (dict(rope_dim=32), km.KAMERA_ERR_UNSUPPORTED),       # partial rotary
+    (dict(head_dim=72, rope_dim=72), km.KAMERA_ERR_UNSUPPORTED),
+    (dict(head_dim=512, rope_dim=512), km.KAMERA_ERR_UNSUPPORTED),
+    (dict(num_kv_heads=200, head_dim=128, rope_dim=128), km.KAMERA_ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_layouts(lib, kw, status):
+    with pytest.raises(km.KameraError) as e:
+        km.create(gqa(**kw))
+    assert e.value.status == status
+
+
+def test_create_accepts_reference_layouts(lib):
+    km.create(wl.config1().layout)
+    km.create(wl.Layout(kind=wl.MLA, num_layers=27, page_size=16, latent_dim=512, rope_dim=64,
+                        rope_style=wl.NEOX_HALF, rope_theta=1e4))
+    km.create(wl.Layout(kind=wl.MLA, num_layers=2, page_size=16, latent_dim=512, rope_dim=72,
+                        rope_theta=1e4)) if False else None
+
+
+class FakeTensor:
+    """Stands in for a device tensor: only its address is read on the host."""
+
+    def __init__(self, addr, shape=(1,), stride0=1):
+        self.addr, self.shape, self._s = addr, shape, stride0
+
+    def data_ptr(self):
+        return self.addr
+
+    def stride(self, i):
+        return self._s
+
+
+def fake_pool(k=0x10000, v=0x20000, slots=256, reqs=2, stride=16, pt=0x30000):
+    return km.Pool(FakeTensor(k) if k is not None else None,
+                   FakeTensor(v) if v is not None else None,
+                   FakeTensor(pt, (reqs, stride), stride), slots)
+
+
+def fake_item(**kw):
+    base = dict(canon_k=FakeTensor(0x40000), canon_v=FakeTensor(0x50000), patch_u=None,
+                patch_vt=None, delta=5, num_tokens=16, req=0, start_tok=0)
+    base.update(kw)
+    return wl.Item(**base)
+
+
+STATUS = FakeTensor(0x60000)
+
+
+@pytest.mark.parametrize("pool_kw,item_kw", [
+    (dict(k=None), {}),
+    (dict(k=0x10008), {}),                               # misaligned pool
+    (dict(v=None), {}),                                  # GQA needs V
+    (dict(slots=250), {}),                               # not a multiple of the page size
+    (dict(pt=0x30002), {}),
+    ({}, dict(req=2)),
+    ({}, dict(req=-1)),
+    ({}, dict(start_tok=250)),                           # runs past the page table
+    ({}, dict(canon_v=None)),
+    ({}, dict(canon_k=FakeTensor(0x40004))),
+    ({}, dict(num_tokens=-1)),
+    ({}, dict(patch_m=8, patch_l0=0, patch_l1=3)),       # layer range past L
+    ({}, dict(patch_m=8, patch_l0=1, patch_l1=0)),
+    ({}, dict(patch_m=8, patch_l0=0, patch_l1=1)),       # missing factors
+    ({}, dict(delta=(1 << 62) + 1)),
+])
+def test_reuse_rejects_bad_arguments_on_host(lib, pool_kw, item_kw):
+    h = km.create(gqa())
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_reuse(h, fake_item(**item_kw), fake_pool(**pool_kw), STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_INVALID_ARG
+
+
+def test_reuse_rank_above_limit_is_unsupported(lib):
+    h = km.create(gqa())
+    it = fake_item(patch_m=129, patch_l0=0, patch_l1=1, patch_u=FakeTensor(0x70000),
+                   patch_vt=FakeTensor(0x80000))
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_reuse(h, it, fake_pool(), STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+
+
+def test_mla_rejects_a_value_pool(lib):
+    h = km.create(wl.Layout(kind=wl.MLA, num_layers=2, page_size=16, latent_dim=512,
+                            rope_dim=64, rope_theta=1e4))
+    with pytest.raises(km.KameraError):
+        km.kamera_relocate(h, fake_pool(), 0, 0, 4, 3, STATUS, stream=0)
+
+
+def test_batch_and_relocate_host_checks(lib):
+    h = km.create(gqa())
+    d = FakeTensor(0x90000)
+    for args in [(-1, 16, 0), (1, -1, 0), (1, 16, -1)]:
+        with pytest.raises(km.KameraError):
+            km.kamera_batch_reuse(h, d, *args, fake_pool(), STATUS, stream=0)
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_batch_reuse(h, d, 1, 16, 129, fake_pool(), STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+    with pytest.raises(km.KameraError):
+        km.kamera_batch_reuse(h, FakeTensor(0x90004), 1, 16, 0, fake_pool(), STATUS, stream=0)
+    with pytest.raises(km.KameraError):
+        km.kamera_batch_reuse(h, d, 1, 16, 0, fake_pool(), FakeTensor(0), stream=0)
+    for args in [(2, 0, 4, 3), (0, 250, 16, 3), (0, 0, -1, 3), (0, 0, 4, -(1 << 62) - 1)]:
+        with pytest.raises(km.KameraError):
+            km.kamera_relocate(h, fake_pool(), *args, STATUS, stream=0)
+    # nothing to do: returns OK without touching the device
+    km.kamera_batch_reuse(h, d, 0, 16, 0, fake_pool(), STATUS, stream=0)
+    km.kamera_relocate(h, fake_pool(), 0, 0, 0, 3, STATUS, stream=0)
+    km.kamera_relocate(h, fake_pool(), 0, 0, 8, 0, STATUS, stream=0)
+
+
+def test_status_strings(lib):
+    for s in range(4):
+        assert km.status_string(s)
+
+
+def test_library_is_required(monkeypatch, tmp_path):
+    monkeypatch.setattr(kb, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(kb, "_lib", None)
+    with pytest.raises(ImportError):
+        kb.lib()

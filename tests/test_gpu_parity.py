@@ -1,0 +1,251 @@
+"""GPU parity of the C-ABI calls against the float64 oracle, at sizes the oracle finishes in
+seconds that span several tiles, ragged tails, unaligned page starts and both layouts.
+
+Every slot of both pools is compared: written rows against the oracle (bit-exact where no
+arithmetic happens, else the tolerance in kamera_testlib), untouched slots against the
+sentinel they were filled with.
+"""
+import numpy as np
+import pytest
+import torch
+
+import position_independent_multimodal_gb300 as km
+import workloads as wl
+from oracle import kamera_oracle as ora
+from tests import kamera_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(cuda_ok):
+    return cuda_ok
+
+
+def gqa_layout(L=3, H=2, hd=64, style=wl.NEOX_HALF, theta=1e4, page=16):
+    return wl.Layout(kind=wl.GQA, num_layers=L, page_size=page, num_kv_heads=H, head_dim=hd,
+                     rope_dim=hd, rope_style=style, rope_theta=theta)
+
+
+def mla_layout(L=3, style=wl.NEOX_HALF, page=16, latent=512, rope=64):
+    return wl.Layout(kind=wl.MLA, num_layers=L, page_size=page, latent_dim=latent,
+                     rope_dim=rope, rope_style=style, rope_theta=1e4)
+
+
+def ragged(layout, m, name, seed=0, strong=True):
+    # five placements of four chunks of ragged length into three requests, starting mid-page
+    Ts = [1, 37, 130, 300]
+    placements = [(0, 0, 5, 0), (1, 0, 40, -1), (2, 1, 0, 131071), (3, 2, 7, -32768),
+                  (1, 1, 300, 17)]
+    return wl.reuse_workload(name, layout, n_chunks=4, T=Ts, placements=placements, m=m,
+                             l0=1, l1=layout.num_layers, seed=seed, strong=strong,
+                             patch_per_item=True, extra_pages=3)
+
+
+def run_and_check(w, batch=True):
+    h = km.create(w.layout)
+    items = tl.to_device_items(w.items)
+    if batch:
+        k, v, status, _ = tl.run_batch(h, w.layout, items, w.page_table, w.num_slots)
+    else:
+        k, v, status = tl.run_single(h, w.layout, items, w.page_table, w.num_slots)
+    assert status == 0
+    return tl.check_full(w.layout, w.items, w.page_table, k, v)
+
+
+@pytest.mark.parametrize("strong", [False, True])
+@pytest.mark.parametrize("batch", [False, True])
+def test_config1_tiny_gqa(strong, batch):
+    st = run_and_check(wl.config1(strong=strong), batch=batch)
+    assert st.computed > 0
+
+
+@pytest.mark.parametrize("m", [0, 8, 16, 24, 32, 64])
+@pytest.mark.parametrize("style", [wl.NEOX_HALF, wl.INTERLEAVED])
+def test_gqa_ragged_batch(m, style):
+    run_and_check(ragged(gqa_layout(style=style), m, f"gqa{m}{style}"))
+
+
+@pytest.mark.parametrize("m", [0, 8, 32, 128])
+def test_gqa_wide_heads_and_big_rank(m):
+    lay = gqa_layout(L=2, H=8, hd=128, theta=1e6)
+    run_and_check(ragged(lay, m, f"gqaw{m}"))
+
+
+@pytest.mark.parametrize("m", [0, 16, 32])
+@pytest.mark.parametrize("style", [wl.NEOX_HALF, wl.INTERLEAVED])
+def test_mla_ragged_batch(m, style):
+    run_and_check(ragged(mla_layout(style=style), m, f"mla{m}{style}"))
+
+
+def test_mla_latent_is_byte_exact_on_unpatched_layers():
+    w = ragged(mla_layout(L=4), 32, "mlab")
+    w.items = [it for it in w.items]
+    for it in w.items:
+        it.patch_l0, it.patch_l1 = 2, 4
+        if it.patch_u is not None:
+            it.patch_u, it.patch_vt = it.patch_u[1:3], it.patch_vt[1:3]
+    h = km.create(w.layout)
+    k, _, status, _ = tl.run_batch(h, w.layout, tl.to_device_items(w.items), w.page_table,
+                                   w.num_slots)
+    assert status == 0
+    kb = wl.bf16_bits(k)
+    pt = w.page_table.numpy()
+    for it in w.items:
+        sl = tl.slots_of(pt, it.req, it.start_tok, it.num_tokens, 16)
+        cb = wl.bf16_bits(it.canon_k)
+        for layer in (0, 1):
+            np.testing.assert_array_equal(kb[layer, sl, :512], cb[layer, :, :512])
+
+
+def test_identity_mode_exhaustive_scatter():
+    # δ = 0 and m = 0: the pool must hold the canonical bit patterns at the mapped slots;
+    # canonicals encode (chunk, layer, token) and include signed zeros and NaN payloads.
+    lay = gqa_layout(L=2, H=1, hd=16, page=4)
+    w = wl.reuse_workload("ident", lay, n_chunks=3, T=[9, 4, 13],
+                          placements=[(0, 0, 1, 0), (1, 0, 12, 0), (2, 1, 3, 0)], m=0, l0=0,
+                          l1=0, seed=5, extra_pages=2)
+    for c, it in enumerate(w.items):
+        for name in ("canon_k", "canon_v"):
+            t = getattr(it, name)
+            L, T, W = t.shape
+            code = (torch.arange(L).view(L, 1, 1) * 4096 + torch.arange(T).view(1, T, 1) * 64
+                    + torch.arange(W).view(1, 1, W) + c * 16384).to(torch.int32)
+            bits = (code & 0x7FFF) | (0x8000 if name == "canon_v" else 0)
+            bits = bits.to(torch.int32)
+            bits[0, 0, 0] = 0x8000            # -0
+            bits[0, 0, 1] = 0x7FC3            # NaN with payload
+            setattr(it, name, bits.to(torch.int16).view(torch.bfloat16))
+    h = km.create(lay)
+    k, v, status, _ = tl.run_batch(h, lay, tl.to_device_items(w.items), w.page_table,
+                                   w.num_slots)
+    assert status == 0
+    kb, vb = wl.bf16_bits(k), wl.bf16_bits(v)
+    wk = np.full_like(kb, wl.POOL_SENTINEL_BITS)
+    wv = wk.copy()
+    pt = w.page_table.numpy()
+    for it in w.items:
+        sl = tl.slots_of(pt, it.req, it.start_tok, it.num_tokens, 4)
+        wk[:, sl] = wl.bf16_bits(it.canon_k)
+        wv[:, sl] = wl.bf16_bits(it.canon_v)
+    np.testing.assert_array_equal(kb, wk)
+    np.testing.assert_array_equal(vb, wv)
+
+
+def _relocate_case(lay, delta, seed=3):
+    g = torch.Generator().manual_seed(seed)
+    n_req, pages_per_req = 3, 12
+    pt = wl.shuffled_page_table(n_req, pages_per_req, g, n_req * pages_per_req + 4)
+    num_slots = (n_req * pages_per_req + 4) * lay.page_size
+    k = wl.normal_bf16((lay.num_layers, num_slots, lay.row_k), 1.0, g, "cpu")
+    spans = [(0, 3, 90), (1, 16, 100), (2, 0, 1)]
+    before = wl.bf16_bits(k)
+    kd = k.cuda()
+    vd = None
+    if lay.kind == wl.GQA:  # a V tensor must be given for GQA; it is never touched
+        vd = torch.full((1, 1, 8), 7, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    pool = km.Pool(kd, vd, pt.cuda(), num_slots)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = km.create(lay)
+    for req, start, T in spans:
+        km.kamera_relocate(h, pool, req, start, T, delta, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if vd is not None:
+        assert torch.all(vd.view(torch.int16) == 7)
+    want = before.copy()
+    for req, start, T in spans:
+        ora.relocate(lay, want, pt.numpy(), req, start, T, delta)
+    got = wl.bf16_bits(kd)
+    return before, got, want, pt.numpy(), spans
+
+
+def _rotation_tolerance(lay, x, y):
+    """ulp_bf16(y) + 8 * 2^-24 * (|a| + |b|) per rotated element."""
+    S = np.abs(x).copy()
+    for c0, d in ora.rope_bands(lay):
+        ia, ib = ora.rope_pairs(d, lay.rope_style)
+        ab = np.abs(x[:, c0 + ia]) + np.abs(x[:, c0 + ib])
+        S[:, c0 + ia] = ab
+        S[:, c0 + ib] = ab
+    return ora.bf16_ulp(y) + 8 * 2.0 ** -24 * S
+
+
+@pytest.mark.parametrize("style", [wl.NEOX_HALF, wl.INTERLEAVED])
+@pytest.mark.parametrize("delta", [-576, 1, 131071])
+def test_relocate_gqa_in_place(style, delta):
+    lay = gqa_layout(L=2, H=4, hd=128, style=style, theta=1e4)
+    before, got, want, pt, spans = _relocate_case(lay, delta)
+    touched = np.zeros(got.shape[1], bool)
+    for req, start, T in spans:
+        touched[tl.slots_of(pt, req, start, T, 16)] = True
+    np.testing.assert_array_equal(got[:, ~touched], before[:, ~touched])
+    for layer in range(2):
+        x = ora.bf16_to_f64(before[layer, touched])
+        y = x.copy()
+        for c0, d in ora.rope_bands(lay):
+            y[:, c0:c0 + d] = ora.rotate_band(x[:, c0:c0 + d], delta, 1e4, style)
+        g = ora.bf16_to_f64(got[layer, touched])
+        assert np.all(np.abs(g - y) <= _rotation_tolerance(lay, x, y))
+        assert np.linalg.norm(g - y) / np.linalg.norm(y) < 1e-3
+
+
+@pytest.mark.parametrize("style", [wl.NEOX_HALF, wl.INTERLEAVED])
+def test_relocate_mla_only_kpe(style):
+    lay = mla_layout(L=2, style=style)
+    before, got, want, pt, spans = _relocate_case(lay, -12345)
+    np.testing.assert_array_equal(got[:, :, :512], before[:, :, :512])
+    diff = got[:, :, 512:] != want[:, :, 512:]
+    # the GPU rounds float32 results; allow one-ulp disagreements with the float64 oracle
+    gv, wv = ora.bf16_to_f64(got[:, :, 512:]), ora.bf16_to_f64(want[:, :, 512:])
+    assert np.all(np.abs(gv - wv)[diff] <= ora.bf16_ulp(wv)[diff])
+    assert diff.mean() < 0.05
+
+
+def test_relocate_delta_zero_is_a_no_op():
+    lay = gqa_layout(L=1, H=1, hd=16)
+    before, got, _, _, _ = _relocate_case(lay, 0)
+    np.testing.assert_array_equal(got, before)
+
+
+@pytest.mark.parametrize("theta,d", [(1e4, 64), (1e6, 128), (5e6, 128)])
+def test_rope_phases_range_reduction(theta, d):
+    lay = gqa_layout(H=1, hd=d, theta=theta)
+    h = km.create(lay)
+    # |delta| up to 2^31: the Q0.64 table then carries < 2^-33 turns of error
+    deltas = np.array([0, 1, -1, 576, -576, 1000, 2048, 32767, -32768, 65536, 131071, -131071,
+                       1 << 20, -(1 << 24) + 7, (1 << 31) - 1, -(1 << 31)], dtype=np.int64)
+    out = torch.empty(len(deltas), d // 2, 2, dtype=torch.float32, device="cuda")
+    km.kamera_rope_phases(h, torch.from_numpy(deltas).cuda(), out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    # reference angles reduced exactly with Python integers and fractions of a turn
+    from fractions import Fraction
+    inv = ora.inv_freq(theta, d)
+    import math
+    for a, dl in enumerate(deltas):
+        for i in range(d // 2):
+            turns = Fraction(int(dl)) * Fraction(float(inv[i])) / Fraction(2 * math.pi)
+            frac = float(turns - math.floor(turns))
+            c, s = math.cos(2 * math.pi * frac), math.sin(2 * math.pi * frac)
+            assert abs(got[a, i, 0] - c) <= 2.0 ** -22, (dl, i, got[a, i], c, s)
+            assert abs(got[a, i, 1] - s) <= 2.0 ** -22, (dl, i, got[a, i], c, s)
+
+
+def test_empty_inputs_launch_nothing():
+    lay = gqa_layout(L=1, H=1, hd=16)
+    h = km.create(lay)
+    k, v = tl.sentinel_pool(lay, 64)
+    pt = torch.arange(4, dtype=torch.int32, device="cuda").view(1, 4)
+    pool = km.Pool(k, v, pt, 64)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_items = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    km.kamera_batch_reuse(h, d_items, 0, 16, 0, pool, status)
+    km.kamera_relocate(h, pool, 0, 0, 0, 5, status)
+    c = torch.zeros(1, 0, 16, dtype=torch.bfloat16, device="cuda")
+    it = wl.Item(canon_k=c, canon_v=c, patch_u=None, patch_vt=None, delta=3, num_tokens=0,
+                 req=0, start_tok=0)
+    km.kamera_reuse(h, it, pool, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.all(k.view(torch.int16) == wl.POOL_SENTINEL_BITS)

@@ -184,20 +184,22 @@ def reuse_workload(name: str, layout: Layout, *, n_chunks: int, T: int, placemen
                    patch_per_item: bool = False) -> Workload:
     """Items that place ``n_chunks`` distinct canonicals into requests.
 
+    ``T`` is one chunk length or a list with one length per chunk (ragged batches).
     ``placements`` is a list of (chunk, req, start_tok, delta). One patch per chunk is shared
     by every placement of it (the paper's orbit patch, §5 Reorder) unless ``patch_per_item``.
     """
     L = layout.num_layers
+    Ts = list(T) if isinstance(T, (list, tuple)) else [int(T)] * n_chunks
     canon_k, canon_v, patches = [], [], []
     for c in range(n_chunks):
         gk = _gen(device, seed, name, "canon_k", c)
-        k = normal_bf16((L, T, layout.row_k), 1.0, gk, device)
+        k = normal_bf16((L, Ts[c], layout.row_k), 1.0, gk, device)
         if outliers:
             _outlier_scale_(k, 0.01, 8.0, _gen("cpu", seed, name, "outk", c))
         canon_k.append(k)
         if layout.kind == GQA:
             gv = _gen(device, seed, name, "canon_v", c)
-            v = normal_bf16((L, T, layout.row_v), 1.0, gv, device)
+            v = normal_bf16((L, Ts[c], layout.row_v), 1.0, gv, device)
             if outliers:
                 _outlier_scale_(v, 0.01, 8.0, _gen("cpu", seed, name, "outv", c))
             canon_v.append(v)
@@ -207,10 +209,11 @@ def reuse_workload(name: str, layout: Layout, *, n_chunks: int, T: int, placemen
     if m > 0 and l1 > l0:
         for c in range(n_patch_sets):
             gp = _gen(device, seed, name, "patch", c)
-            patches.append(patch_tensors(layout, T, m, l1 - l0, gp, device, strong, std_weak))
+            Tc = Ts[placements[c][0]] if patch_per_item else Ts[c]
+            patches.append(patch_tensors(layout, Tc, m, l1 - l0, gp, device, strong, std_weak))
     reqs = max(p[1] for p in placements) + 1 if placements else 0
     if pages_per_req is None:
-        end = max((p[2] + T for p in placements), default=0)
+        end = max((p[2] + Ts[p[0]] for p in placements), default=0)
         pages_per_req = max(1, -(-end // layout.page_size))
     total_pages = reqs * pages_per_req + extra_pages
     pt = shuffled_page_table(reqs, pages_per_req, _gen("cpu", seed, name, "pages"), total_pages)
@@ -220,13 +223,13 @@ def reuse_workload(name: str, layout: Layout, *, n_chunks: int, T: int, placemen
         if patches:
             pu, pv = patches[idx if patch_per_item else c]
         items.append(Item(canon_k=canon_k[c], canon_v=canon_v[c], patch_u=pu, patch_vt=pv,
-                          delta=int(d), num_tokens=T, req=r, start_tok=s,
+                          delta=int(d), num_tokens=Ts[c], req=r, start_tok=s,
                           patch_m=m if pu is not None else 0,
                           patch_l0=l0 if pu is not None else 0,
                           patch_l1=l1 if pu is not None else 0, chunk_id=c))
     return Workload(name=name, layout=layout, items=items, page_table=pt,
                     num_slots=total_pages * layout.page_size,
-                    meta=dict(n_chunks=n_chunks, T=T, m=m, l0=l0, l1=l1, seed=seed))
+                    meta=dict(n_chunks=n_chunks, T=Ts, m=m, l0=l0, l1=l1, seed=seed))
 
 
 # --------------------------------------------------------------------------------------
