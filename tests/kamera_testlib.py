@@ -11,7 +11,7 @@ y is the oracle's exact float64 value, S the oracle's error scale (|a|+|b| on ro
 (rotation: a few roundings plus float32 cos/sin error; rank-m accumulation: at most m+1
 roundings, doubled for truncating accumulators) and only matters under cancellation. Columns
 no arithmetic touches must be bit-exact, and every (item, layer, channel) must also meet a
-relative Frobenius error <= 1e-3 against y.
+relative Frobenius error <= 1e-3 against the oracle's bf16 result.
 """
 from __future__ import annotations
 
@@ -138,8 +138,11 @@ def check_rows(layout, oitem, layer: int, ch: int, tokens, got_bits: np.ndarray)
     st.computed = int(comp.sum()) * got_bits.shape[0]
     st.not_rne_equal = int((got_bits[:, comp] != want_bits[:, comp]).sum())
     st.max_ulps = float(np.max(err / ora.bf16_ulp(y)))
-    ny = np.linalg.norm(y)
-    rel = np.linalg.norm(g - y) / ny if ny > 0 else np.linalg.norm(g - y)
+    # relative Frobenius error against the oracle's own bf16 result: rounding to bf16 alone
+    # moves a layer by ~1.6e-3 (RMS) from the exact values, so the bound compares outputs
+    r = ora.bf16_to_f64(want_bits[:, comp])
+    nr = np.linalg.norm(r)
+    rel = np.linalg.norm(g - r) / nr if nr > 0 else np.linalg.norm(g - r)
     st.worst_rel_frob = float(rel)
     assert rel <= REL_FROB, f"layer {layer} ch {ch}: relative Frobenius error {rel:.3e}"
     return st
