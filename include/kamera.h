@@ -49,6 +49,8 @@ typedef enum kamera_status {
                                        page table; that token's row was not written          */
 #define KAMERA_DEVICE_BAD_ITEM 0x2u /* kamera_batch_reuse: an item failed the checks that
                                        kamera_reuse makes on the host; none of it was written */
+#define KAMERA_DEVICE_TIMEOUT 0x4u  /* a tensor-core tile did not complete within 2 s; its
+                                       rows were not written (never expected)               */
 
 /* Attention families (§3 "One mechanism for MLA, GQA, and MHA"). MHA is GQA with one KV head
  * per query head. */

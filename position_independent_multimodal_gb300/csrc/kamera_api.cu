@@ -11,11 +11,8 @@ struct kamera_handle {
   kamera_layout desc;
   kamera::DevLayout lay;
   kamera::FreqQ64 freq;
+  int engine;  // engine of patched tiles (KAMERA_PATCH_ENGINE=fma selects the CUDA-core one)
 };
-
-namespace kamera {
-int reuse_stream_tile();
-}
 
 namespace {
 
@@ -47,6 +44,10 @@ kamera_status fill_layout(const kamera_layout &d, DevLayout *out) {
     l.row_k = l.row_v = l.H * l.hd;
     l.w0 = l.w1 = l.row_k;
     l.n_ch = 2;
+    // tiles of whole heads, about 128 columns wide
+    l.tw = l.hd >= 128 ? l.hd : l.hd * (128 / l.hd);
+    if (l.tw > l.row_k) l.tw = l.row_k;
+    l.ntile = (l.row_k + l.tw - 1) / l.tw;
   } else if (d.kind == KAMERA_MLA) {
     if (d.latent_dim < 1 || d.rope_dim < 1) return KAMERA_ERR_INVALID_ARG;
     if (!is_mult16(d.latent_dim) || !is_mult16(d.rope_dim) ||
@@ -62,6 +63,8 @@ kamera_status fill_layout(const kamera_layout &d, DevLayout *out) {
     l.w0 = d.latent_dim;
     l.w1 = d.rope_dim;
     l.n_ch = 1;
+    l.tw = d.latent_dim < 128 ? d.latent_dim : 128;
+    l.ntile = (d.latent_dim + l.tw - 1) / l.tw + 1;
   } else {
     return KAMERA_ERR_INVALID_ARG;
   }
@@ -130,6 +133,8 @@ kamera_status kamera_create(const kamera_layout *layout, kamera_handle **out) {
   h->desc = *layout;
   h->lay = l;
   fill_freq(*layout, l, &h->freq);
+  const char *eng = std::getenv("KAMERA_PATCH_ENGINE");
+  h->engine = (eng && std::strcmp(eng, "fma") == 0) ? kamera::kEngineFma : kamera::kEngineTensor;
   *out = h;
   return KAMERA_OK;
 }
@@ -188,12 +193,12 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.n_items = 1;
   a.max_tokens = item->num_tokens;
   a.max_m = item->patch_m;
+  a.engine = h->engine;
+  a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
-  const int tile = kamera::reuse_stream_tile();
-  const int tiles = (item->num_tokens + tile - 1) / tile;
-  return from_cuda(
-      kamera::launch_reuse_stream(a, tiles, 1, reinterpret_cast<cudaStream_t>(stream)));
+  const int tiles = (item->num_tokens + kamera::kTileRows - 1) / kamera::kTileRows;
+  return from_cuda(kamera::launch_reuse(a, tiles, 1, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_items,
@@ -215,13 +220,14 @@ kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_it
   a.n_items = num_items;
   a.max_tokens = max_tokens;
   a.max_m = max_patch_m;
+  a.engine = h->engine;
+  a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
-  const int tile = kamera::reuse_stream_tile();
-  const int tiles = (max_tokens + tile - 1) / tile;
-  if (tiles > 0x7FFFFFFF / 1) return KAMERA_ERR_UNSUPPORTED;
-  return from_cuda(
-      kamera::launch_reuse_stream(a, tiles, num_items, reinterpret_cast<cudaStream_t>(stream)));
+  const long long tiles = ((long long)max_tokens + kamera::kTileRows - 1) / kamera::kTileRows;
+  if (tiles * h->lay.ntile > 0x7FFFFFFFll) return KAMERA_ERR_UNSUPPORTED;
+  return from_cuda(kamera::launch_reuse(a, (int)tiles, num_items,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,

@@ -23,7 +23,64 @@ struct DevLayout {
   int w0, w1;        // patch group widths
   int npairs;        // rope pairs per band (rope_d / 2)
   int n_ch;          // 2 for GQA (K, V), 1 for MLA
+  // column tiles of the fused kernel: GQA rows split into tiles of `tw` columns holding whole
+  // heads; MLA rows into latent tiles of `tw` plus one tile for the k_pe band
+  int tw;            // tile width (<= 256, multiple of 16)
+  int ntile;         // tiles per row (same for both GQA channels)
 };
+
+// Engines for patched tiles.
+constexpr int kEngineTensor = 0;  // tcgen05 MMA into TMEM (rank a multiple of 8)
+constexpr int kEngineFma = 1;     // float32 FMAs on CUDA cores (any rank)
+
+// Rows per tile of the fused kernel: the MMA's M and the TMEM lanes.
+constexpr int kTileRows = 128;
+
+// Byte offsets of the fused kernel's dynamic shared memory.
+struct SmemPlan {
+  int canon;   // [128][pitch] bf16 canonical tile, 16-byte chunks XOR-swizzled by row
+  int pitch;   // row pitch in bytes (multiple of 128)
+  int a_op;    // A operand (U tile): K-major core matrices, [Kp/8][16][128 B]
+  int b_op;    // B operand (V_m^T tile): K-major core matrices, [Kp/8][tw/8][128 B]
+  int cs;      // float2 cos/sin table [npairs]
+  int slots;   // long long [128]
+  int misc;    // TMEM address (4 B) and the MMA mbarrier (8 B, 8-aligned)
+  int total;
+};
+
+// A column tile: [col0, col0 + ncols) of a channel's row.
+struct Tile {
+  int col0, ncols;
+  int group, gcol0;  // patch group and the tile's first column inside it
+  int band;          // width of the rope bands it holds (0: nothing rotates in this tile)
+};
+
+__host__ __device__ inline Tile tile_of(const DevLayout &l, int ch, int ti, bool rotate) {
+  Tile t;
+  if (l.kind == KAMERA_GQA) {
+    t.col0 = ti * l.tw;
+    t.ncols = (l.row_k - t.col0) < l.tw ? (l.row_k - t.col0) : l.tw;
+    t.group = ch;
+    t.gcol0 = t.col0;
+    t.band = (ch == 0 && rotate) ? l.hd : 0;
+  } else {
+    const int nlat = (l.latent + l.tw - 1) / l.tw;
+    if (ti < nlat) {
+      t.col0 = ti * l.tw;
+      t.ncols = (l.latent - t.col0) < l.tw ? (l.latent - t.col0) : l.tw;
+      t.group = 0;
+      t.gcol0 = t.col0;
+      t.band = 0;
+    } else {
+      t.col0 = l.latent;
+      t.ncols = l.rope_d;
+      t.group = 1;
+      t.gcol0 = 0;
+      t.band = rotate ? l.rope_d : 0;
+    }
+  }
+  return t;
+}
 
 // Per-pair rotation speed in turns per token, as an unsigned Q0.64 fixed-point fraction:
 // q_i = round(inv_freq_i / (2 pi) * 2^64). The angle of offset delta is delta * q_i mod 2^64,
@@ -48,6 +105,8 @@ struct ReuseArgs {
   int n_items;
   int max_tokens;
   int max_m;
+  int engine;                // kEngineTensor or kEngineFma for patched tiles
+  SmemPlan smem;
   unsigned *status;
   FreqQ64 freq;
 };
@@ -252,9 +311,10 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
   }
 }
 
-// Kernel launchers (kamera_stream.cu).
-cudaError_t launch_reuse_stream(const ReuseArgs &a, int tiles, int n_items, cudaStream_t s);
-cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);
+// Kernel launchers.
+SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
+cudaError_t launch_reuse(const ReuseArgs &a, int token_tiles, int n_items, cudaStream_t s);
+cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,
                                float *out, cudaStream_t s);
 

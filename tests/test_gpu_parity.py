@@ -60,10 +60,19 @@ def test_config1_tiny_gqa(strong, batch):
     assert st.computed > 0
 
 
-@pytest.mark.parametrize("m", [0, 8, 16, 24, 32, 64])
+@pytest.mark.parametrize("m", [0, 3, 8, 12, 16, 24, 32, 64])
 @pytest.mark.parametrize("style", [wl.NEOX_HALF, wl.INTERLEAVED])
 def test_gqa_ragged_batch(m, style):
+    # ranks 3 and 12 take the CUDA-core path, multiples of 8 the tensor-core path
     run_and_check(ragged(gqa_layout(style=style), m, f"gqa{m}{style}"))
+
+
+@pytest.mark.parametrize("kind", ["gqa", "mla"])
+def test_fma_engine_matches_oracle(kind, monkeypatch):
+    # the CUDA-core engine for every patched tile (the ablation of the tensor-core path)
+    monkeypatch.setenv("KAMERA_PATCH_ENGINE", "fma")
+    lay = gqa_layout(L=2, H=4, hd=128) if kind == "gqa" else mla_layout(L=2)
+    run_and_check(ragged(lay, 32, f"fma{kind}"))
 
 
 @pytest.mark.parametrize("m", [0, 8, 32, 128])
