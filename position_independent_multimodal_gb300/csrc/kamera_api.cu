@@ -197,8 +197,7 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
-  const int tiles = (item->num_tokens + kamera::kTileRows - 1) / kamera::kTileRows;
-  return from_cuda(kamera::launch_reuse(a, tiles, 1, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(kamera::launch_reuse(a, 1, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_items,
@@ -224,10 +223,9 @@ kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_it
   a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
-  const long long tiles = ((long long)max_tokens + kamera::kTileRows - 1) / kamera::kTileRows;
-  if (tiles * h->lay.ntile > 0x7FFFFFFFll) return KAMERA_ERR_UNSUPPORTED;
-  return from_cuda(kamera::launch_reuse(a, (int)tiles, num_items,
-                                        reinterpret_cast<cudaStream_t>(stream)));
+  if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
+    return KAMERA_ERR_UNSUPPORTED;
+  return from_cuda(kamera::launch_reuse(a, num_items, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,

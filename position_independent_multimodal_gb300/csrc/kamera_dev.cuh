@@ -38,14 +38,17 @@ constexpr int kTileRows = 128;
 
 // Byte offsets of the fused kernel's dynamic shared memory.
 struct SmemPlan {
-  int canon;   // [128][pitch] bf16 canonical tile, 16-byte chunks XOR-swizzled by row
-  int pitch;   // row pitch in bytes (multiple of 128)
-  int a_op;    // A operand (U tile): K-major core matrices, [Kp/8][16][128 B]
-  int b_op;    // B operand (V_m^T tile): K-major core matrices, [Kp/8][tw/8][128 B]
-  int cs;      // float2 cos/sin table [npairs]
-  int slots;   // long long [128]
-  int misc;    // TMEM address (4 B) and the MMA mbarrier (8 B, 8-aligned)
+  int b_op, b_stage;     // two B operands (V_m^T rows): MN-major core matrices [Kp/8][tw/8][128 B]
+  int a_op, a_stage;     // two A operands (U rows): K-major core matrices [Kp/8][16][128 B]
+  int canon, stage;      // two stages of [128][pitch] bf16 canonical rows
+  int pitch;             // row pitch in bytes (tile width * 2 + 16: rows land on distinct banks)
+  int cs, cs_stage;      // two float2 cos/sin tables [npairs]
+  int pages, pages_stage;  // two stages of page ids of the tile's tokens
+  int desc;              // two stage descriptors
+  int slots;             // long long [128]: slot of each row of the tile being stored
+  int misc;              // TMEM address (4 B) and the MMA mbarrier (8 B, 8-aligned)
   int total;
+  int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
 };
 
 // A column tile: [col0, col0 + ncols) of a channel's row.
@@ -313,7 +316,7 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
 
 // Kernel launchers.
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
-cudaError_t launch_reuse(const ReuseArgs &a, int token_tiles, int n_items, cudaStream_t s);
+cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,
                                float *out, cudaStream_t s);

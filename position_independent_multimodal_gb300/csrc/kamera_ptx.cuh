@@ -30,6 +30,14 @@ __device__ __forceinline__ void cp_async_commit() {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
+// all but the most recently committed group have landed
+__device__ __forceinline__ void cp_async_wait_group1() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+// 4-byte copy through L1 (page-table entries)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 
 // generic-proxy shared-memory writes made visible to the async proxy (tensor core reads)
 __device__ __forceinline__ void fence_proxy_async_smem() {
