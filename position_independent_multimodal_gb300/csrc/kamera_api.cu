@@ -197,7 +197,12 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
-  return from_cuda(kamera::launch_reuse(a, 1, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+  // unpatched layers stream through registers; patched layers take the tensor-core pipeline
+  cudaError_t e = kamera::launch_reuse_copy(a, strm);
+  if (e == cudaSuccess && item->patch_m > 0 && item->patch_l1 > item->patch_l0)
+    e = kamera::launch_reuse(a, 1, strm);
+  return from_cuda(e);
 }
 
 kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_items,
@@ -225,7 +230,11 @@ kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_it
   a.freq = h->freq;
   if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
     return KAMERA_ERR_UNSUPPORTED;
-  return from_cuda(kamera::launch_reuse(a, num_items, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+  // unpatched layers stream through registers; patched layers take the tensor-core pipeline
+  cudaError_t e = kamera::launch_reuse_copy(a, strm);
+  if (e == cudaSuccess && max_patch_m > 0) e = kamera::launch_reuse(a, num_items, strm);
+  return from_cuda(e);
 }
 
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,

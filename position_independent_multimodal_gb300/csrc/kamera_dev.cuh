@@ -46,7 +46,7 @@ struct SmemPlan {
   int pages, pages_stage;  // two stages of page ids of the tile's tokens
   int desc;              // two stage descriptors
   int slots;             // long long [128]: slot of each row of the tile being stored
-  int misc;              // TMEM address (4 B) and the MMA mbarrier (8 B, 8-aligned)
+  int misc;              // TMEM address (4 B), the MMA mbarrier and the two stage mbarriers
   int total;
   int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
 };
@@ -318,6 +318,7 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
+cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,
                                float *out, cudaStream_t s);
 
