@@ -38,8 +38,8 @@ constexpr int kTileRows = 128;
 
 // Byte offsets of the fused kernel's dynamic shared memory.
 struct SmemPlan {
-  int b_op, b_stage;     // two B operands (V_m^T rows): MN-major core matrices [Kp/8][tw/8][128 B]
-  int a_op, a_stage;     // two A operands (U rows): K-major core matrices [Kp/8][16][128 B]
+  int b_op, b_stage;     // B operand (V_m^T rows): MN-major core matrices [Kp/8][tw/8][128 B]
+  int a_op, a_stage;     // one or two A operands (U rows): K-major core matrices [Kp/8][16][128 B]
   int canon, stage;      // two stages of [128][pitch] bf16 canonical rows
   int pitch;             // row pitch in bytes (tile width * 2 + 16: rows land on distinct banks)
   int cs, cs_stage;      // two float2 cos/sin tables [npairs]
@@ -49,6 +49,8 @@ struct SmemPlan {
   int misc;              // TMEM address (4 B), the MMA mbarrier and the two stage mbarriers
   int total;
   int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
+  int acc_cols;          // TMEM columns of one accumulator
+  int u_bufs;            // U buffers (2: staged two tiles ahead; 1: after each MMA)
 };
 
 // A column tile: [col0, col0 + ncols) of a channel's row.

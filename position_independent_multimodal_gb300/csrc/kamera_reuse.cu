@@ -53,6 +53,36 @@ __device__ __forceinline__ uint32_t ldg_u16(const __nv_bfloat16 *p) {
 }
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// Two float32 lanes in one 64-bit register, for the packed f32x2 arithmetic of sm_100+.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// bf16 pair (low, high half of a 32-bit word) -> two float32 lanes
+__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(f32x2 v) {
+  float lo, hi;
+  f2_split(v, lo, hi);
+  return pack2_rn(lo, hi);
+}
+
 // e -> (e / n, e % n) with a shift when n is a power of two
 struct DivMod {
   int n, sh;  // sh >= 0: n == 1 << sh
@@ -129,11 +159,14 @@ __device__ __forceinline__ void patch16(const PatchSrc &ps, int ca, int cb, floa
 }
 
 // Rotate + patch one row of the tile in place, one rounding (this thread's half of the units).
-// NeoX bands: groups of 8 pairs (columns i..i+7 with partners i+band/2..); interleaved bands
+// NeoX bands: groups of 8 pairs (columns i..i+7 with partners i+band/2..) in packed f32x2
+// arithmetic: a' = b*(-sin) + (a*cos + p_a), b' = a*sin + (b*cos + p_b). Interleaved bands
 // and unrotated tiles: 8-column chunks. Half h takes units u with u % 2 == h; tcgen05.ld is
-// warp-collective, so all lanes of a warp walk the same units.
+// warp-collective, so all lanes of a warp walk the same units. `rot` holds cos[npairs],
+// sin[npairs] and -sin[npairs] of the item's offset.
 __device__ __forceinline__ void epilogue_row(uint32_t crow, const Tile &tile, int style,
-                                             int half, const PatchSrc &ps, const float2 *cs) {
+                                             int half, const PatchSrc &ps, const float *rot,
+                                             int npairs) {
   const int NC = tile.ncols, band = tile.band;
   if (band != 0 && style == KAMERA_ROPE_NEOX_HALF) {
     const int hb = band >> 1;
@@ -143,34 +176,56 @@ __device__ __forceinline__ void epilogue_row(uint32_t crow, const Tile &tile, in
       int head, i;
       hbd.split(g * 8, &head, &i);
       const int ca = head * band + i, cb = ca + hb;
-      float xa[8], xb[8], pa[8], pb[8];
-      unpack8(lds16(crow + ca * 2), xa);
-      unpack8(lds16(crow + cb * 2), xb);
+      float pa[8], pb[8];
       patch16(ps, ca, cb, pa, pb);
+      const uint4 ra = lds16(crow + ca * 2), rb = lds16(crow + cb * 2);
+      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+      const float4 *cv = reinterpret_cast<const float4 *>(rot + i);
+      const float4 *sv = reinterpret_cast<const float4 *>(rot + npairs + i);
+      const float4 *nv = reinterpret_cast<const float4 *>(rot + 2 * npairs + i);
+      uint32_t oa[4], ob[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        rot_pair(xa[e], xb[e], cs[i + e]);
-        xa[e] += pa[e];
-        xb[e] += pb[e];
+      for (int q = 0; q < 2; ++q) {
+        const float4 c4 = cv[q], s4 = sv[q], n4 = nv[q];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int j = 2 * q + h2;  // word j holds elements 2j, 2j+1
+          const f32x2 c = h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
+          const f32x2 sn = h2 ? f2(s4.z, s4.w) : f2(s4.x, s4.y);
+          const f32x2 ns = h2 ? f2(n4.z, n4.w) : f2(n4.x, n4.y);
+          const f32x2 a = bf2_to_f2(wa[j]), b = bf2_to_f2(wb[j]);
+          const f32x2 na = fma2(b, ns, fma2(a, c, f2(pa[2 * j], pa[2 * j + 1])));
+          const f32x2 nb = fma2(a, sn, fma2(b, c, f2(pb[2 * j], pb[2 * j + 1])));
+          oa[j] = f2_to_bf2(na);
+          ob[j] = f2_to_bf2(nb);
+        }
       }
-      sts16(crow + ca * 2, pack8_rn(xa));
-      sts16(crow + cb * 2, pack8_rn(xb));
+      sts16(crow + ca * 2, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+      sts16(crow + cb * 2, make_uint4(ob[0], ob[1], ob[2], ob[3]));
     }
   } else {
     const int nchunks = NC >> 3;
     for (int ck = half; ck < nchunks; ck += 2) {
       const int col = ck * 8;
-      float x[8], p[8];
-      unpack8(lds16(crow + col * 2), x);
+      float p[8];
       patch8(ps, col, p);
+      const uint4 rw = lds16(crow + col * 2);
+      const uint32_t w[4] = {rw.x, rw.y, rw.z, rw.w};
+      uint32_t o[4];
       if (band != 0) {  // interleaved pairs (2i, 2i+1)
         const int f0 = (col % band) >> 1;
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) rot_pair(x[e], x[e + 1], cs[f0 + (e >> 1)]);
-      }
+        for (int j = 0; j < 4; ++j) {
+          float x0 = __uint_as_float(w[j] << 16), x1 = __uint_as_float(w[j] & 0xFFFF0000u);
+          rot_pair(x0, x1, make_float2(rot[f0 + j], rot[npairs + f0 + j]));
+          o[j] = pack2_rn(x0 + p[2 * j], x1 + p[2 * j + 1]);
+        }
+      } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] += p[e];
-      sts16(crow + col * 2, pack8_rn(x));
+        for (int j = 0; j < 4; ++j)
+          o[j] = f2_to_bf2(add2(bf2_to_f2(w[j]), f2(p[2 * j], p[2 * j + 1])));
+      }
+      sts16(crow + col * 2, make_uint4(o[0], o[1], o[2], o[3]));
     }
   }
 }
@@ -197,6 +252,7 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   const int ncore = tile.ncols >> 3;
   const int row = ch == 0 ? lay.row_k : lay.row_v;
   const bool tensor = a.engine == kEngineTensor && (m & 7) == 0 && aligned16(it.patch_u);
+  const bool u2 = P.u_bufs == 2;  // U of tile t+2 staged with its rows (else one buffer)
   const int li = layer - it.patch_l0;
   const __nv_bfloat16 *canon = static_cast<const __nv_bfloat16 *>(ch == 0 ? it.canon_k
                                                                            : it.canon_v) +
@@ -211,9 +267,8 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
                         (long long)layer * a.pool.num_slots * row + tile.col0;
   const int ntt = (T + kTileRows - 1) / kTileRows;
   const uint32_t s0 = ptx::smem_addr(smem);
-  const uint32_t a_op = s0 + P.a_op, b_op = s0 + P.b_op, c_op = s0 + P.canon;
-  const uint32_t pg_op = s0 + P.pages;
-  const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;
+  const uint32_t b_op = s0 + P.b_op, c_op = s0 + P.canon, pg_op = s0 + P.pages;
+  const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
   const DivMod cpr(ncore);
   const DivMod psd(lay.page_size);
   const int rs = (kThr % ncore == 0) ? kThr / ncore : 0;  // rows per pass of the fixed mapping
@@ -222,7 +277,8 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   const int r = ((warp & 3) << 5) + (tid & 31);  // epilogue row (TMEM lane)
   const int half = warp >> 2;
   __nv_bfloat16 **rowptr = reinterpret_cast<__nv_bfloat16 **>(smem + P.slots);
-  float2 *cs = reinterpret_cast<float2 *>(smem + P.cs);
+  float *rot = reinterpret_cast<float *>(smem + P.cs);  // cos[np] | sin[np] | -sin[np]
+  auto a_buf = [&](int t) { return s0 + P.a_op + (u2 ? (t & 1) * P.a_stage : 0); };
 
   // canonical rows and page ids of tile t into stage s
   auto issue_canon = [&](int t, int s) {
@@ -255,6 +311,7 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
     const int t0 = t * kTileRows;
     const int rows = min(kTileRows, T - t0);
     const __nv_bfloat16 *Ut = U + (long long)t0 * m;
+    const uint32_t a_op = a_buf(t);
     if (tensor) {
       const DivMod kcs(Kp >> 3);
       for (int e = tid; e < kTileRows * kcs.n; e += kThr) {
@@ -273,17 +330,42 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
       }
     }
   };
+  uint32_t tmem = 0;
+  const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, tile.ncols) | (1u << 16);  // B MN-major
+  // MMA of tile t into accumulator t & 1 (one thread); arrives on barrier t & 1
+  auto issue_mma = [&](int t) {
+    ptx::tc_fence_after();
+    // In the no-swizzle MN-major layout the descriptor's leading offset is the K-direction
+    // step between core matrices and the stride offset the MN-direction step (K-major A:
+    // LBO along K, SBO along M).
+    const uint32_t lbo_a = 16 * 128, sbo_a = 128;
+    const uint32_t k_step_b = ncore * 128, mn_step_b = 128;
+    const uint32_t a_op = a_buf(t);
+    const uint32_t d = tmem + (t & 1) * P.acc_cols;
+    for (int ks = 0; ks < Kp / 16; ++ks) {
+      const uint64_t ad = ptx::smem_desc(a_op + ks * 2 * lbo_a, lbo_a, sbo_a);
+      const uint64_t bd = ptx::smem_desc(b_op + ks * 2 * k_step_b, k_step_b, mn_step_b);
+      ptx::mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit(s_bar + 8 * (t & 1));
+  };
 
   if (warp == 0) {
     ptx::tmem_alloc(s_tmem, P.tmem_cols);
     ptx::tmem_relinquish();
   }
   if (tid == 0) {
-    ptx::mbar_init(s_bar, 1);  // MMA completion
+    ptx::mbar_init(s_bar, 1);
+    ptx::mbar_init(s_bar + 8, 1);
     ptx::fence_mbar_init();
   }
   if (tile.band)  // cos/sin of this item's offset, once per CTA
-    for (int i = tid; i < lay.npairs; i += kThr) cs[i] = rope_phase(a.freq.q[i], it.delta);
+    for (int i = tid; i < lay.npairs; i += kThr) {
+      const float2 c = rope_phase(a.freq.q[i], it.delta);
+      rot[i] = c.x;
+      rot[lay.npairs + i] = c.y;
+      rot[2 * lay.npairs + i] = -c.y;
+    }
   // B operand, once per CTA: a 16-byte run of a V_m^T row is one core-matrix row
   for (int e = tid; e < Kp * ncore; e += kThr) {
     int k, j;
@@ -296,42 +378,28 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   issue_canon(0, 0);
   issue_u(0);
   ptx::cp_async_commit();
-  if (ntt > 1) issue_canon(1, 1);
+  if (ntt > 1) {
+    issue_canon(1, 1);
+    if (u2) issue_u(1);
+  }
   ptx::cp_async_commit();
+  ptx::cp_async_wait_group1();  // tile 0 (and B)
+  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
-  __syncthreads();  // TMEM address and barrier initialisation visible
+  __syncthreads();  // TMEM address, barriers, tile 0 visible
   ptx::tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + P.misc);
-  const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, tile.ncols) | (1u << 16);  // B MN-major
-
-  uint32_t mma_phase = 0;
+  tmem = *reinterpret_cast<volatile uint32_t *>(smem + P.misc);
   bool timed_out = false;
+  if (tensor && tid == 0) issue_mma(0);
+
   for (int t = 0; t < ntt; ++t) {
     const int s = t & 1;
     const int t0 = t * kTileRows;
     const int rows = min(kTileRows, T - t0);
-    ptx::cp_async_wait_group1();  // tile t's rows, pages and U (and B, cos/sin at t = 0)
-    ptx::fence_proxy_async_smem();
-    __syncthreads();
     const bool use_tc = tensor && !timed_out;
-    if (use_tc) {
-      if (tid == 0) {
-        ptx::tc_fence_after();
-        // In the no-swizzle MN-major layout the descriptor's leading offset is the
-        // K-direction step between core matrices and the stride offset the MN-direction
-        // step (K-major A: LBO along K, SBO along M).
-        const uint32_t lbo_a = 16 * 128, sbo_a = 128;
-        const uint32_t k_step_b = ncore * 128, mn_step_b = 128;
-        for (int ks = 0; ks < Kp / 16; ++ks) {
-          const uint64_t ad = ptx::smem_desc(a_op + ks * 2 * lbo_a, lbo_a, sbo_a);
-          const uint64_t bd = ptx::smem_desc(b_op + ks * 2 * k_step_b, k_step_b, mn_step_b);
-          ptx::mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(s_bar);
-      }
-      // warp 0 waits for the MMA; the other warps sleep at the barrier
+    if (use_tc) {  // warp 0 waits for MMA(t); the other warps sleep at the barrier
       if (warp == 0) {
-        const bool ok = ptx::mbar_wait(s_bar, mma_phase, kWaitLimitNs);
+        const bool ok = ptx::mbar_wait(s_bar + 8 * s, (t >> 1) & 1, kWaitLimitNs);
         if (tid == 0) *reinterpret_cast<volatile int *>(smem + P.misc + 4) = ok ? 0 : 1;
       }
       ptx::tc_fence_before();
@@ -341,24 +409,22 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
         timed_out = true;
         if (tid == 0) atomicOr(a.status, KAMERA_DEVICE_TIMEOUT);
       }
-      mma_phase ^= 1;
+      // one U buffer: MMA(t) has read it, so U of tile t+1 may land now
+      if (!u2 && t + 1 < ntt) issue_u(t + 1);
+      ptx::cp_async_commit();
     }
-    // the A operand is free once the MMA has read it: U of the next tile lands meanwhile
-    if (tensor && t + 1 < ntt) issue_u(t + 1);
-    ptx::cp_async_commit();
-
-    const bool write = !timed_out;
+    const bool write = !(tensor && timed_out);
     const uint32_t c_row = c_op + s * P.stage + r * P.pitch;
     if (write && (r < rows || use_tc)) {
       PatchSrc ps;
       ps.tensor = use_tc;
-      ps.trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      ps.a_base = a_op;
+      ps.trow = tmem + s * P.acc_cols + ((uint32_t)((warp & 3) * 32) << 16);
+      ps.a_base = a_buf(t);
       ps.b_base = b_op;
       ps.r = r;
       ps.m = m;
       ps.ncore = ncore;
-      epilogue_row(c_row, tile, lay.style, half, ps, cs);
+      epilogue_row(c_row, tile, lay.style, half, ps, rot, lay.npairs);
     }
     if (half == 0 && r < rows) {  // the row's owner finds its slot
       int pg, in_page;
@@ -376,12 +442,17 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
         atomicOr(a.status, KAMERA_DEVICE_SLOT_OOB);
       rowptr[r] = dst;
     }
-    if (use_tc) ptx::tc_fence_before();
-    __syncthreads();  // rows complete
-    if (!tensor && t + 1 < ntt) {  // CUDA-core path: the A operand was read by the epilogue
+    // the CUDA-core path with one U buffer reads U(t) in the epilogue: U(t+1) after it
+    if (!u2 && !tensor && t + 1 < ntt) {
+      __syncthreads();
       issue_u(t + 1);
       ptx::cp_async_commit();
     }
+    ptx::cp_async_wait_all();  // tile t+1's rows, pages and U
+    ptx::fence_proxy_async_smem();
+    if (use_tc) ptx::tc_fence_before();
+    __syncthreads();  // rows of tile t complete, tile t+1 staged
+    if (tensor && !timed_out && t + 1 < ntt && tid == 0) issue_mma(t + 1);
     if (write) {  // fixed 16-byte chunk per thread, coalesced along each row
       const uint32_t st0 = c_op + s * P.stage;
       if (rs) {
@@ -400,7 +471,10 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
       }
     }
     __syncthreads();  // stage s is free
-    if (t + 2 < ntt) issue_canon(t + 2, s);
+    if (t + 2 < ntt) {
+      issue_canon(t + 2, s);
+      if (u2) issue_u(t + 2);
+    }
     ptx::cp_async_commit();
   }
   ptx::cp_async_wait_all();
@@ -422,24 +496,29 @@ SmemPlan reuse_smem_plan(const DevLayout &l, int max_m) {
   p.stage = align128(kTileRows * p.pitch);
   p.a_stage = align128(kTileRows * kp * 2);
   p.b_stage = align128(widest * kp * 2);
-  p.cs_stage = align128(l.npairs * 8);
+  p.cs_stage = align128(l.npairs * 12);
   p.pages_stage = align128((kTileRows / l.page_size + 2) * 4);
+  const int fixed = p.b_stage + 2 * p.stage + p.cs_stage + 2 * p.pages_stage +
+                    align128(kTileRows * 8) + 128;
+  // two U buffers when two CTAs still fit on an SM (227 KB of shared memory, 1 KB reserved
+  // per CTA), else one
+  p.u_bufs = (fixed + 2 * p.a_stage + 1024) * 2 <= 227 * 1024 ? 2 : 1;
   // B first: every descriptor offset stays inside the allocation
   int off = 0;
   p.b_op = off;
   off += p.b_stage;
   p.a_op = off;
-  off += p.a_stage;
+  off += p.u_bufs * p.a_stage;
   p.canon = off;
   off += 2 * p.stage;
   p.cs = off;
   off += p.cs_stage;
   p.pages = off;
   off += 2 * p.pages_stage;
-  p.desc = off;  // unused
+  p.desc = off;   // unused
   p.slots = off;  // row pointers of the tile being stored
   off = align128(off + kTileRows * 8);
-  p.misc = off;  // TMEM address, timeout flag, MMA barrier
+  p.misc = off;   // TMEM address, timeout flag, two MMA barriers
   off = align128(off + 32);
   p.total = off;
   int cols = 0;
@@ -447,7 +526,8 @@ SmemPlan reuse_smem_plan(const DevLayout &l, int max_m) {
     cols = 32;
     while (cols < widest) cols <<= 1;
   }
-  p.tmem_cols = cols;
+  p.acc_cols = cols;       // one accumulator
+  p.tmem_cols = 2 * cols;  // two: MMA of the next tile runs under this tile's stores
   return p;
 }
 

@@ -70,11 +70,11 @@ __global__ void __launch_bounds__(kThreads) relocate_kernel(const __grid_constan
   }
 }
 
-constexpr int kCopyRows = 64;
+constexpr int kCopyRows = 128;
 
 // Unpatched layers of reuse items: the canonical rows of (item, layer, channel) stream through
 // registers to their slots, rope columns rotated on the way (R(delta) with no patch term),
-// everything else copied byte for byte. One CTA per 64 rows of an (item, layer, channel);
+// everything else copied byte for byte. One CTA per 128 rows of an (item, layer, channel);
 // the grid runs items fastest after the row blocks, so placements that share a canonical read
 // it from L2. Patched layers are left to the tensor-core kernel.
 template <bool kFixedUnit>
@@ -84,7 +84,7 @@ __device__ __forceinline__ void copy_rows(const DevLayout &lay, int ch, bool rot
                                           const float2 *cs) {
   const int tid = threadIdx.x;
   const int upr = row >> 4;
-  constexpr int B = 4;
+  constexpr int B = 2;  // two units (four 16-byte vectors) in flight per thread
   if (kFixedUnit) {
     // upr divides the block: every thread keeps one column unit and walks rows
     const int u = tid % upr, r0 = tid / upr, rstep = kThreads / upr;
