@@ -40,6 +40,8 @@ def parse():
                     help="target CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the brief timings of the MLA, survival and recall-sweep workloads")
     return ap.parse_args()
 
 
@@ -47,29 +49,42 @@ def parse():
 # workload accounting
 # ----------------------------------------------------------------------------------------
 
-def accounting(w):
-    """Algorithmic bytes of one step of a reuse workload (bf16 = 2 bytes)."""
+def accounting(w, items=None):
+    """Algorithmic bytes of one step of a reuse workload (bf16 = 2 bytes), in total and per
+    kernel: the streaming kernel takes the unpatched layers, the tensor-core kernel the patched
+    ones. Canonical bytes count each distinct canonical once (placements that share it read
+    it from L2); patch bytes count each distinct factor once."""
+    items = w.items if items is None else items
     lay = w.layout
     row = lay.row_k + lay.row_v
-    written = sum(lay.num_layers * it.num_tokens * row * 2 for it in w.items)
-    seen, canon = set(), 0
-    for it in w.items:
-        key = it.canon_k.data_ptr()
-        if key not in seen:
-            seen.add(key)
-            canon += lay.num_layers * it.num_tokens * row * 2
-    seen, patch = set(), 0
-    for it in w.items:
-        if it.patch_u is None:
-            continue
-        key = it.patch_u.data_ptr()
-        if key not in seen:
-            seen.add(key)
-            patch += (it.patch_u.numel() + it.patch_vt.numel()) * 2
-    naive_canon = written
-    meta = 64 * len(w.items) + w.page_table.numel() * 4
-    return dict(written=written, canon_distinct=canon, canon_naive=naive_canon, patch=patch,
-                meta=meta, algorithmic=written + canon + patch + meta)
+
+    def patched(it, layer):
+        return it.patch_m > 0 and it.patch_l0 <= layer < it.patch_l1
+
+    out = {"copy": dict(written=0, canon=0), "tensor": dict(written=0, canon=0, patch=0)}
+    seen_c, seen_p = set(), set()
+    for it in items:
+        for layer in range(lay.num_layers):
+            kind = "tensor" if patched(it, layer) else "copy"
+            nbytes = it.num_tokens * row * 2
+            out[kind]["written"] += nbytes
+            key = (it.canon_k.data_ptr(), layer)
+            if key not in seen_c:
+                seen_c.add(key)
+                out[kind]["canon"] += nbytes
+        if it.patch_u is not None and it.patch_u.data_ptr() not in seen_p:
+            seen_p.add(it.patch_u.data_ptr())
+            out["tensor"]["patch"] += (it.patch_u.numel() + it.patch_vt.numel()) * 2
+    meta = 64 * len(items) + w.page_table.numel() * 4
+    for k in out:
+        out[k]["algorithmic"] = sum(out[k].values()) + meta
+    written = out["copy"]["written"] + out["tensor"]["written"]
+    canon = out["copy"]["canon"] + out["tensor"]["canon"]
+    return dict(written=written, canon_distinct=canon, canon_naive=written,
+                patch=out["tensor"]["patch"], meta=meta,
+                algorithmic=written + canon + out["tensor"]["patch"] + meta,
+                per_kernel={"reuse_copy_kernel": out["copy"]["algorithmic"],
+                            "reuse_kernel": out["tensor"]["algorithmic"]})
 
 
 def measured_peak():
@@ -304,9 +319,19 @@ def kamera_arm(args, rank, world, local_rank):
     n_items = len(w.items)
     max_m = max(it.patch_m for it in w.items)
     stream = torch.cuda.current_stream()
+    # three events per timed step: before, between and after the call's two kernels
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for trio in marks:
+        for e in trio:
+            e.record(stream)  # creates the event handles
+    torch.cuda.synchronize()
 
-    def step():
-        km.kamera_batch_reuse(h, d_items, n_items, 1024, max_m, pool, status, stream)
+    def step(trio=None):
+        if trio is None:
+            km.kamera_batch_reuse(h, d_items, n_items, 1024, max_m, pool, status, stream)
+        else:
+            km.kamera_batch_reuse_timed(h, d_items, n_items, 1024, max_m, pool, status, trio,
+                                        stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -324,13 +349,15 @@ def kamera_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(marks[i])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
+    kern_ms = {"reuse_copy_kernel": statistics.fmean(t[0].elapsed_time(t[1]) for t in marks),
+               "reuse_kernel": statistics.fmean(t[1].elapsed_time(t[2]) for t in marks)}
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -341,10 +368,14 @@ def kamera_arm(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(args, w, h, dev, stream)
+    del k, v, pool, w
+    torch.cuda.empty_cache()
+    others = None
+    if rank == 0 and world == 1 and not args.no_other_workloads:
+        others = other_workloads(dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        del w
         cpu = cpu_baseline(args.cpu_seconds)
 
     if rank != 0:
@@ -352,6 +383,13 @@ def kamera_arm(args, rank, world, local_rank):
     peak, src = measured_peak()
     s = ms / 1e3
     achieved = acc["algorithmic"] / s / 1e9
+    dom = max(kern_ms, key=kern_ms.get)
+    kernels = {}
+    for name, kms in kern_ms.items():
+        kb = acc["per_kernel"][name]
+        kernels[name] = {"ms": kms, "algorithmic_bytes": kb,
+                         "achieved_gbs": kb / (kms / 1e3) / 1e9 if kms > 0 else None,
+                         "frac": kb / (kms / 1e3) / 1e9 / peak if kms > 0 else None}
     line = {
         "metric": METRIC,
         "value": acc["written"] * world / s / 1e9,
@@ -364,20 +402,115 @@ def kamera_arm(args, rank, world, local_rank):
         "us_per_chunk": ms * 1e3 / n_items,
         "gb_s_moved": achieved * world,
         "frac_hbm_peak": achieved / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
-                     else "fallback 6.8 TB/s",
-                     "kernel": "reuse_stream_kernel",
-                     "algorithmic_bytes_per_launch": acc["algorithmic"]},
-        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": None,
+                     "kernel": dom, "algorithmic_bytes_per_launch": acc["per_kernel"][dom],
+                     "launch_ms": kern_ms[dom],
+                     "peak_source": (f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                                     else "fallback 6.8 TB/s")},
+        "kernels": kernels,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
     if e2e:
         line["e2e"] = e2e
+    if others:
+        line["other_workloads"] = others
     if cpu:
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
+
+
+def time_calls(fn, steps, warmup=1):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def other_workloads(dev):
+    """Brief timings of the MLA recall, sliding-window survival and recall-sweep workloads
+    (each a parity-tested configuration of its own); reported beside the main line."""
+    import torch
+    import position_independent_multimodal_gb300 as km
+    import workloads as wl
+
+    peak, _ = measured_peak()
+    out = {}
+
+    def reuse_calls(w, launches):
+        lay = w.layout
+        h = km.create(lay)
+        k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+        v = (torch.empty(lay.num_layers, w.num_slots, lay.row_v, dtype=torch.bfloat16,
+                         device=dev) if lay.kind == wl.GQA else None)
+        pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        packed = [(km.pack_items(items).to(dev), len(items),
+                   max(it.num_tokens for it in items), max(it.patch_m for it in items))
+                  for items in launches]
+
+        def call():
+            for d, n, mt, mm in packed:
+                km.kamera_batch_reuse(h, d, n, mt, mm, pool, st)
+        ms = time_calls(call, 5)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        return ms
+
+    w = wl.config3(device=dev)
+    acc = accounting(w)
+    ms = reuse_calls(w, [w.items])
+    out["mla_recall_64_chunks"] = {
+        "workload": "MLA (DeepSeek-V2-Lite-shaped) 27 layers, c_KV 512 + k_pe 64, 64 chunks "
+                    "T=1024, delta in [-32768, 32768], m=32 on layers 13-26",
+        "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
+        "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
+        "chunks_per_s": len(w.items) / ms * 1e3}
+    del w
+    torch.cuda.empty_cache()
+
+    w = wl.config4(device=dev)
+    h = km.create(w.layout)
+    vd = torch.zeros(1, 1, 8, dtype=torch.bfloat16, device=dev)
+    pool = km.Pool(w.k_pool, vd, w.page_table.to(dev), w.num_slots)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def reloc():
+        for sp in w.spans:
+            km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, st)
+    ms = time_calls(reloc, 3)
+    moved = sum(sp.num_tokens for sp in w.spans) * w.layout.num_layers * w.layout.row_k * 2 * 2
+    out["mha_sliding_window_448_survivors"] = {
+        "workload": "MHA 32 layers x 32 heads x 128, 64 sequences x 7 survivor chunks of 576 "
+                    "tokens re-rotated in place by delta=-576 (K pool 77 GB)",
+        "ms_per_step": ms, "gb_s_written": moved / 2 / ms / 1e6,
+        "frac_hbm_peak": moved / ms / 1e6 / peak,
+        "chunks_per_s": 448 / ms * 1e3}
+    del w, pool
+    torch.cuda.empty_cache()
+
+    w = wl.config5(device=dev)
+    launches = [wl.config5_launch_items(w, g) for g in range(8)]
+    ms = reuse_calls(w, launches)
+    written = sum(accounting(w, items)["written"] for items in launches)
+    alg = sum(accounting(w, items)["algorithmic"] for items in launches)
+    out["gqa_recall_sweep_1024_items"] = {
+        "workload": "GQA 64 layers (8 launches of 8-layer slices), H_kv=8 x 128, 256 requests x "
+                    "4 recalls T=1024, delta in [0, 131072), m=64 on layers 32-63",
+        "ms_per_step": ms, "gb_s_written": written / ms / 1e6,
+        "frac_hbm_peak": alg / ms / 1e6 / peak, "chunks_per_s": 1024 / ms * 1e3}
+    del w, launches
+    torch.cuda.empty_cache()
+    return out
 
 
 def end_to_end(args, w, h, dev, stream):

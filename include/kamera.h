@@ -176,6 +176,18 @@ kamera_status kamera_batch_reuse(const kamera_handle *handle, const kamera_item 
                                  kamera_stream_t stream);
 
 /*
+ * kamera_batch_reuse with timing marks. The call runs two kernels on the stream: one for the
+ * layers without a patch (rotation and copies), then one for the patched layers (tensor-core
+ * patch). events[0..2] are CUDA events (cudaEvent_t) recorded before the first kernel,
+ * between the two, and after the second; any entry may be NULL. The work done is identical
+ * to kamera_batch_reuse.
+ */
+kamera_status kamera_batch_reuse_timed(const kamera_handle *handle, const kamera_item *d_items,
+                                       int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
+                                       const kamera_pool *pool, uint32_t *d_status,
+                                       kamera_stream_t stream, void *const events[3]);
+
+/*
  * The RoPE phases the kernels use: for each of num_deltas offsets d_deltas[n] (device int64)
  * and each rope pair i of the layout, (cos, sin) of delta * inv_freq_i with inv_freq_i =
  * theta^(-2i/d), written as float32 pairs to d_out[n][rope_dim/2][2] (device). The angle is

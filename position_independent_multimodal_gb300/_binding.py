@@ -80,8 +80,11 @@ def lib() -> ctypes.CDLL:
         L.kamera_batch_reuse.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(kamera_pool), vp,
                                          vp]
         L.kamera_rope_phases.argtypes = [vp, vp, i32, vp, vp]
+        L.kamera_batch_reuse_timed.argtypes = [vp, vp, i32, i32, i32,
+                                               ctypes.POINTER(kamera_pool), vp, vp,
+                                               ctypes.POINTER(vp)]
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
-                  "kamera_batch_reuse", "kamera_rope_phases"):
+                  "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -196,3 +199,16 @@ def kamera_rope_phases(handle: Handle, d_deltas: torch.Tensor, d_out: torch.Tens
     """(cos, sin) per (delta, pair) into ``d_out`` float32 [n][rope_dim/2][2]."""
     _check(lib().kamera_rope_phases(handle.ptr, _ptr(d_deltas), int(d_deltas.numel()),
                                     _ptr(d_out), _stream(stream)), "kamera_rope_phases")
+
+
+def kamera_batch_reuse_timed(handle: Handle, d_items: torch.Tensor, num_items: int,
+                             max_tokens: int, max_patch_m: int, pool: Pool, status: torch.Tensor,
+                             events, stream=None) -> None:
+    """kamera_batch_reuse recording three torch.cuda.Event objects (or None) before, between
+    and after its two kernels."""
+    arr = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in events])
+    p = pool.c()
+    _check(lib().kamera_batch_reuse_timed(handle.ptr, _ptr(d_items), int(num_items),
+                                          int(max_tokens), int(max_patch_m), ctypes.byref(p),
+                                          _ptr(status), _stream(stream), arr),
+           "kamera_batch_reuse_timed")

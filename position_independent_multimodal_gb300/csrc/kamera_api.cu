@@ -205,10 +205,11 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   return from_cuda(e);
 }
 
-kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_items,
-                                 int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
-                                 const kamera_pool *pool, uint32_t *d_status,
-                                 kamera_stream_t stream) {
+namespace {
+
+kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, int32_t num_items,
+                          int32_t max_tokens, int32_t max_patch_m, const kamera_pool *pool,
+                          uint32_t *d_status, kamera_stream_t stream, void *const *events) {
   if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
   if (num_items < 0 || max_tokens < 0 || max_patch_m < 0) return KAMERA_ERR_INVALID_ARG;
   if (max_patch_m > kamera::kMaxRank) return KAMERA_ERR_UNSUPPORTED;
@@ -231,10 +232,35 @@ kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_it
   if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
     return KAMERA_ERR_UNSUPPORTED;
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) -> cudaError_t {
+    if (!events || !events[i]) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), strm);
+  };
   // unpatched layers stream through registers; patched layers take the tensor-core pipeline
-  cudaError_t e = kamera::launch_reuse_copy(a, strm);
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, strm);
+  if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess && max_patch_m > 0) e = kamera::launch_reuse(a, num_items, strm);
+  if (e == cudaSuccess) e = mark(2);
   return from_cuda(e);
+}
+
+}  // namespace
+
+kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_items,
+                                 int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
+                                 const kamera_pool *pool, uint32_t *d_status,
+                                 kamera_stream_t stream) {
+  return batch_reuse(h, d_items, num_items, max_tokens, max_patch_m, pool, d_status, stream,
+                     nullptr);
+}
+
+kamera_status kamera_batch_reuse_timed(const kamera_handle *h, const kamera_item *d_items,
+                                       int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
+                                       const kamera_pool *pool, uint32_t *d_status,
+                                       kamera_stream_t stream, void *const events[3]) {
+  return batch_reuse(h, d_items, num_items, max_tokens, max_patch_m, pool, d_status, stream,
+                     events);
 }
 
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,

@@ -230,26 +230,88 @@ __device__ __forceinline__ void epilogue_row(uint32_t crow, const Tile &tile, in
   }
 }
 
-__global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ ReuseArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+// Epilogue of one row for a compile-time tile shape: NC columns, NeoX bands of width BAND
+// (0: nothing rotates), accumulator in TMEM. Half h takes the contiguous half of the units:
+// NeoX pairs [h*NC/4, (h+1)*NC/4) with their partners, or 8-column chunks
+// [h*NC/16, (h+1)*NC/16); every offset is a constant of the unrolled loop.
+template <int NC, int BAND>
+__device__ __forceinline__ void epilogue_fixed(uint32_t crow, int half, uint32_t trow,
+                                               const float *rot, int npairs) {
+  if constexpr (BAND > 0) {
+    constexpr int HB = BAND / 2, PAIRS_HALF = NC / 4, GROUPS = PAIRS_HALF / 8;
+#pragma unroll
+    for (int q = 0; q < GROUPS; ++q) {
+      const int p = half * PAIRS_HALF + q * 8;  // first pair of the group
+      const int head = p / HB, i = p % HB;
+      const int ca = head * BAND + i, cb = ca + HB;
+      uint32_t acc[16];
+      ptx::tmem_ld8(trow + ca, acc);
+      ptx::tmem_ld8(trow + cb, acc + 8);
+      const uint4 ra = lds16(crow + ca * 2), rb = lds16(crow + cb * 2);
+      const float4 *cv = reinterpret_cast<const float4 *>(rot + i);
+      const float4 *sv = reinterpret_cast<const float4 *>(rot + npairs + i);
+      const float4 *nv = reinterpret_cast<const float4 *>(rot + 2 * npairs + i);
+      ptx::tmem_ld_wait(acc);
+      ptx::tmem_ld_wait(acc + 8);
+      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+      uint32_t oa[4], ob[4];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float4 c4 = cv[h2], s4 = sv[h2], n4 = nv[h2];
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          const int j = 2 * h2 + g2;  // word j holds elements 2j, 2j+1
+          const f32x2 c = g2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
+          const f32x2 sn = g2 ? f2(s4.z, s4.w) : f2(s4.x, s4.y);
+          const f32x2 ns = g2 ? f2(n4.z, n4.w) : f2(n4.x, n4.y);
+          const f32x2 a = bf2_to_f2(wa[j]), b = bf2_to_f2(wb[j]);
+          const f32x2 pa = f2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+          const f32x2 pb =
+              f2(__uint_as_float(acc[8 + 2 * j]), __uint_as_float(acc[8 + 2 * j + 1]));
+          oa[j] = f2_to_bf2(fma2(b, ns, fma2(a, c, pa)));
+          ob[j] = f2_to_bf2(fma2(a, sn, fma2(b, c, pb)));
+        }
+      }
+      sts16(crow + ca * 2, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+      sts16(crow + cb * 2, make_uint4(ob[0], ob[1], ob[2], ob[3]));
+    }
+  } else {
+    constexpr int CH_HALF = NC / 16;  // 8-column chunks per half
+#pragma unroll
+    for (int q = 0; q < CH_HALF; q += 2) {
+      const int col = (half * CH_HALF + q) * 8;
+      uint32_t acc[16];
+      ptx::tmem_ld8(trow + col, acc);
+      ptx::tmem_ld8(trow + col + 8, acc + 8);
+      const uint4 r0 = lds16(crow + col * 2), r1 = lds16(crow + col * 2 + 16);
+      ptx::tmem_ld_wait(acc);
+      ptx::tmem_ld_wait(acc + 8);
+      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        o[j] = f2_to_bf2(add2(bf2_to_f2(w[j]),
+                              f2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]))));
+      sts16(crow + col * 2, make_uint4(o[0], o[1], o[2], o[3]));
+      sts16(crow + col * 2 + 16, make_uint4(o[4], o[5], o[6], o[7]));
+    }
+  }
+}
+
+// Everything one CTA does for its task. NC > 0 fixes the tile width and BAND the NeoX band
+// width at compile time (the tensor-core epilogue is then fully unrolled); NC == 0 is the
+// general path for any tile, band, pairing and engine.
+template <int NC, int BAND>
+__device__ __forceinline__ void run_task(const ReuseArgs &a, unsigned char *smem,
+                                         const kamera_item &it, int layer, int ch,
+                                         const Tile &tile) {
+  constexpr bool kFixed = NC > 0;
   const SmemPlan &P = a.smem;
   const DevLayout &lay = a.lay;
   const int tid = threadIdx.x, warp = tid >> 5;
-  // this CTA's task: column tile, item, (layer, channel)
-  const int ct = blockIdx.x, item = blockIdx.y;
-  const int layer = blockIdx.z / lay.n_ch;
-  const int ch = blockIdx.z - layer * lay.n_ch;
-  const kamera_item it = a.items ? a.items[item] : a.single;
-  if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
-    if (ct == 0 && blockIdx.z == 0 && tid == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);
-    return;
-  }
-  if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;  // the copy kernel's work
-
   const int T = it.num_tokens, m = it.patch_m, Kp = (m + 15) & ~15;
-  const bool rotate = ch == 0 && it.delta != 0;
-  const Tile tile = tile_of(lay, ch, ct, rotate);
-  const int ncore = tile.ncols >> 3;
+  const int ncols = kFixed ? NC : tile.ncols;
+  const int ncore = ncols >> 3;
   const int row = ch == 0 ? lay.row_k : lay.row_v;
   const bool tensor = a.engine == kEngineTensor && (m & 7) == 0 && aligned16(it.patch_u);
   const bool u2 = P.u_bufs == 2;  // U of tile t+2 staged with its rows (else one buffer)
@@ -271,7 +333,8 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
   const DivMod cpr(ncore);
   const DivMod psd(lay.page_size);
-  const int rs = (kThr % ncore == 0) ? kThr / ncore : 0;  // rows per pass of the fixed mapping
+  // fixed 16-byte chunk per thread for row copies: rows my_r0, my_r0 + rs, ...
+  const int rs = (kThr % ncore == 0) ? kThr / ncore : 0;
   int my_r0 = 0, my_ck = 0;
   if (rs) cpr.split(tid, &my_r0, &my_ck);
   const int r = ((warp & 3) << 5) + (tid & 31);  // epilogue row (TMEM lane)
@@ -331,7 +394,7 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
     }
   };
   uint32_t tmem = 0;
-  const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, tile.ncols) | (1u << 16);  // B MN-major
+  const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, ncols) | (1u << 16);  // B MN-major
   // MMA of tile t into accumulator t & 1 (one thread); arrives on barrier t & 1
   auto issue_mma = [&](int t) {
     ptx::tc_fence_after();
@@ -391,6 +454,7 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   tmem = *reinterpret_cast<volatile uint32_t *>(smem + P.misc);
   bool timed_out = false;
   if (tensor && tid == 0) issue_mma(0);
+  const uint32_t trow0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
   for (int t = 0; t < ntt; ++t) {
     const int s = t & 1;
@@ -416,15 +480,24 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
     const bool write = !(tensor && timed_out);
     const uint32_t c_row = c_op + s * P.stage + r * P.pitch;
     if (write && (r < rows || use_tc)) {
-      PatchSrc ps;
-      ps.tensor = use_tc;
-      ps.trow = tmem + s * P.acc_cols + ((uint32_t)((warp & 3) * 32) << 16);
-      ps.a_base = a_buf(t);
-      ps.b_base = b_op;
-      ps.r = r;
-      ps.m = m;
-      ps.ncore = ncore;
-      epilogue_row(c_row, tile, lay.style, half, ps, rot, lay.npairs);
+      bool done = false;
+      if constexpr (kFixed) {
+        if (use_tc) {
+          epilogue_fixed<NC, BAND>(c_row, half, trow0 + s * P.acc_cols, rot, lay.npairs);
+          done = true;
+        }
+      }
+      if (!done) {
+        PatchSrc ps;
+        ps.tensor = use_tc;
+        ps.trow = trow0 + s * P.acc_cols;
+        ps.a_base = a_buf(t);
+        ps.b_base = b_op;
+        ps.r = r;
+        ps.m = m;
+        ps.ncore = ncore;
+        epilogue_row(c_row, tile, lay.style, half, ps, rot, lay.npairs);
+      }
     }
     if (half == 0 && r < rows) {  // the row's owner finds its slot
       int pg, in_page;
@@ -481,6 +554,38 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
+}
+
+__global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ ReuseArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const DevLayout &lay = a.lay;
+  // this CTA's task: column tile, item, (layer, channel)
+  const int ct = blockIdx.x, item = blockIdx.y;
+  const int layer = blockIdx.z / lay.n_ch;
+  const int ch = blockIdx.z - layer * lay.n_ch;
+  const kamera_item it = a.items ? a.items[item] : a.single;
+  if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
+    if (ct == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);
+    return;
+  }
+  if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;  // the copy kernel's work
+  const bool rotate = ch == 0 && it.delta != 0;
+  const Tile tile = tile_of(lay, ch, ct, rotate);
+  const bool neox = lay.style == KAMERA_ROPE_NEOX_HALF;
+  // compile-time shapes of the reference layouts; everything else takes the general path
+  if (tile.ncols == 128 && tile.band == 0) {
+    run_task<128, 0>(a, smem, it, layer, ch, tile);
+  } else if (tile.ncols == 128 && tile.band == 128 && neox) {
+    run_task<128, 128>(a, smem, it, layer, ch, tile);
+  } else if (tile.ncols == 128 && tile.band == 64 && neox) {
+    run_task<128, 64>(a, smem, it, layer, ch, tile);
+  } else if (tile.ncols == 64 && tile.band == 64 && neox) {
+    run_task<64, 64>(a, smem, it, layer, ch, tile);
+  } else if (tile.ncols == 64 && tile.band == 0) {
+    run_task<64, 0>(a, smem, it, layer, ch, tile);
+  } else {
+    run_task<0, 0>(a, smem, it, layer, ch, tile);
+  }
 }
 
 int align128(int x) { return (x + 127) & ~127; }

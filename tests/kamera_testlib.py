@@ -148,6 +148,33 @@ def check_rows(layout, oitem, layer: int, ch: int, tokens, got_bits: np.ndarray)
     return st
 
 
+def mini_item(layout, it: wl.Item, layer: int, toks: np.ndarray):
+    """An oracle item holding only ``toks`` rows of one layer (host bits), so a sample of a
+    full-size item is checked without copying the whole item to the host."""
+    idx = torch.as_tensor(np.asarray(toks), device=it.canon_k.device)
+    ck = {layer: wl.bf16_bits(it.canon_k[layer].index_select(0, idx))}
+    cv = None if it.canon_v is None else {layer: wl.bf16_bits(it.canon_v[layer].index_select(0, idx))}
+    pu = pv = None
+    if it.patch_m > 0 and it.patch_l0 <= layer < it.patch_l1:
+        li = layer - it.patch_l0
+        pu = {li: [wl.bf16_bits(it.patch_u[li, g].index_select(0, idx)) for g in range(2)]}
+        pv = {li: wl.bf16_bits(it.patch_vt[li])}
+    return ora.as_item(canon_k=ck, canon_v=cv, patch_u=pu, patch_vt=pv, delta=it.delta,
+                       num_tokens=len(toks), req=it.req, start_tok=0, patch_m=it.patch_m,
+                       patch_l0=it.patch_l0, patch_l1=it.patch_l1)
+
+
+def check_sampled(layout, it: wl.Item, layer: int, ch: int, toks, pool: torch.Tensor,
+                  page_table: np.ndarray) -> Stats:
+    """Check the rows of sampled tokens of one (item, layer, channel) in a device pool."""
+    toks = np.asarray(sorted(set(int(t) for t in toks)))
+    logical = it.start_tok + toks
+    sl = (page_table[it.req, logical // layout.page_size].astype(np.int64) * layout.page_size
+          + logical % layout.page_size)
+    got = wl.bf16_bits(pool[layer].index_select(0, torch.as_tensor(sl, device=pool.device)))
+    return check_rows(layout, mini_item(layout, it, layer, toks), layer, ch, None, got)
+
+
 def slots_of(page_table: np.ndarray, req: int, start: int, T: int, page: int) -> np.ndarray:
     toks = start + np.arange(T)
     return page_table[req, toks // page].astype(np.int64) * page + toks % page

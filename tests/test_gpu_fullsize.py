@@ -1,0 +1,155 @@
+"""Parity at the full sizes of the five reference workloads, through the same C-ABI calls the
+benchmark times. Sampled rows are compared with the float64 oracle one by one (the oracle
+cannot redo a whole workload in seconds); whole-pool properties are checked on the device:
+every slot of every request written, untouched rows unchanged, and the byte-copy columns
+(V and the MLA latent on unpatched layers) equal to the canonical bytes."""
+import numpy as np
+import pytest
+import torch
+
+import position_independent_multimodal_gb300 as km
+import workloads as wl
+from oracle import kamera_oracle as ora
+from tests import kamera_testlib as tl
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(cuda_ok):
+    yield
+    torch.cuda.empty_cache()
+
+
+def run_batch(w, items):
+    lay = w.layout
+    k, v = tl.sentinel_pool(lay, w.num_slots)
+    h = km.create(lay)
+    pt = w.page_table.cuda()
+    d_items = km.pack_items(items).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    max_t = max(it.num_tokens for it in items)
+    max_m = max(it.patch_m for it in items)
+    km.kamera_batch_reuse(h, d_items, len(items), max_t, max_m, km.Pool(k, v, pt, w.num_slots),
+                          status)
+    torch.cuda.synchronize()
+    return k, v, int(status.item())
+
+
+def unwritten_rows(pool):
+    return int((pool.view(torch.int16) == wl.POOL_SENTINEL_BITS).all(dim=-1).sum().item())
+
+
+def item_slots(w, it):
+    toks = it.start_tok + np.arange(it.num_tokens)
+    pt = w.page_table.numpy()
+    ps = w.layout.page_size
+    return torch.as_tensor(pt[it.req, toks // ps].astype(np.int64) * ps + toks % ps, device="cuda")
+
+
+def sample_tokens(rng, T, n=40):
+    return np.unique(np.concatenate([[0, T - 1, 127, 128], rng.integers(0, T, n)]))
+
+
+def check_units(w, items, k, v, n_units, seed, layers=None):
+    rng = np.random.default_rng(seed)
+    lay = w.layout
+    pt = w.page_table.numpy()
+    n_ch = 2 if lay.kind == wl.GQA else 1
+    layer_pool = layers if layers is not None else range(lay.num_layers)
+    st = tl.Stats()
+    for _ in range(n_units):
+        it = items[int(rng.integers(len(items)))]
+        layer = int(rng.choice(list(layer_pool)))
+        ch = int(rng.integers(n_ch))
+        pool = k if ch == 0 else v
+        st.add(tl.check_sampled(lay, it, layer, ch, sample_tokens(rng, it.num_tokens), pool, pt))
+    return st
+
+
+def test_config2_gqa_reorder_full():
+    w = wl.config2(device="cuda")
+    k, v, status = run_batch(w, w.items)
+    assert status == 0
+    assert unwritten_rows(k) == 0 and unwritten_rows(v) == 0
+    st = check_units(w, w.items, k, v, 40, seed=2)
+    assert st.computed > 0
+    # unpatched layers: V is a byte copy of the canonical values
+    for it in w.items[:6]:
+        sl = item_slots(w, it)
+        for layer in (0, 7, 13):
+            assert torch.equal(v[layer].index_select(0, sl), it.canon_v[layer])
+    del k, v, w
+    torch.cuda.empty_cache()
+
+
+def test_config3_mla_recall_full():
+    w = wl.config3(device="cuda")
+    k, _, status = run_batch(w, w.items)
+    assert status == 0
+    assert unwritten_rows(k) == 0
+    check_units(w, w.items, k, None, 40, seed=3)
+    # the latent c_KV is copied byte for byte on unpatched layers (0-12)
+    for it in w.items[::8]:
+        sl = item_slots(w, it)
+        for layer in range(0, 13, 4):
+            assert torch.equal(k[layer].index_select(0, sl)[:, :512], it.canon_k[layer][:, :512])
+    del k, w
+    torch.cuda.empty_cache()
+
+
+def test_config4_sliding_window_survivors_full():
+    w = wl.config4(device="cuda")
+    lay = w.layout
+    pt = w.page_table.numpy()
+    rng = np.random.default_rng(4)
+    ps = lay.page_size
+    # sampled rows before the slide: survivor tokens and evicted-chunk tokens
+    probes = []
+    for _ in range(24):
+        req = int(rng.integers(len(w.spans)))
+        tok = int(rng.integers(0, w.meta["chunk"] * w.meta["window"]))
+        layer = int(rng.integers(lay.num_layers))
+        slot = int(pt[req, tok // ps]) * ps + tok % ps
+        probes.append((req, tok, layer, slot, wl.bf16_bits(w.k_pool[layer, slot])))
+    h = km.create(lay)
+    vd = torch.zeros(1, 1, 8, dtype=torch.bfloat16, device="cuda")  # GQA needs a V; untouched
+    pool = km.Pool(w.k_pool, vd, w.page_table.cuda(), w.num_slots)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for sp in w.spans:
+        km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for req, tok, layer, slot, before in probes:
+        got = wl.bf16_bits(w.k_pool[layer, slot])
+        if tok < w.meta["chunk"]:  # the evicted chunk's rows are not touched
+            np.testing.assert_array_equal(got, before)
+            continue
+        x = ora.bf16_to_f64(before)[None]
+        y = x.copy()
+        for c0, d in ora.rope_bands(lay):
+            y[:, c0:c0 + d] = ora.rotate_band(x[:, c0:c0 + d], -w.meta["chunk"], lay.rope_theta,
+                                              lay.rope_style)
+        g = ora.bf16_to_f64(got)[None]
+        S = np.abs(x).copy()
+        for c0, d in ora.rope_bands(lay):
+            ia, ib = ora.rope_pairs(d, lay.rope_style)
+            S[:, c0 + ia] = S[:, c0 + ib] = np.abs(x[:, c0 + ia]) + np.abs(x[:, c0 + ib])
+        assert np.all(np.abs(g - y) <= ora.bf16_ulp(y) + 8 * 2.0 ** -24 * S)
+    del w, pool
+    torch.cuda.empty_cache()
+
+
+def test_config5_recall_sweep_full():
+    w = wl.config5(device="cuda")
+    Ls = w.meta["layer_slices"]
+    for launch in range(w.meta["full_layout"].num_layers // Ls):
+        items = wl.config5_launch_items(w, launch)
+        k, v, status = run_batch(w, items)
+        assert status == 0
+        assert unwritten_rows(k) == 0 and unwritten_rows(v) == 0
+        if launch in (0, 3, 4, 7):  # unpatched and patched slices
+            check_units(w, items, k, v, 10, seed=50 + launch)
+        del k, v
+    del w
+    torch.cuda.empty_cache()
