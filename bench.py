@@ -296,6 +296,30 @@ def config_desc(acc=None):
 
 
 # ----------------------------------------------------------------------------------------
+# sharding across ranks: every rank reuses its own seeded copy of the workload (no data-path
+# collective); the job time is the slowest rank's
+# ----------------------------------------------------------------------------------------
+
+def rank_seed(rank: int) -> int:
+    return rank
+
+
+def job_time_ms(ms: float, world: int, device=None) -> float:
+    """Max over ranks of the per-step time (every rank ran the same number of steps)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(written_per_rank: int, world: int, job_ms: float) -> float:
+    """GB/s written by all ranks together over the slowest rank's step time."""
+    return written_per_rank * world / (job_ms / 1e3) / 1e9
+
+
+# ----------------------------------------------------------------------------------------
 # the CUDA arm
 # ----------------------------------------------------------------------------------------
 
@@ -306,7 +330,7 @@ def kamera_arm(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = wl.config2(seed=rank, device=dev)
+    w = wl.config2(seed=rank_seed(rank), device=dev)
     lay = w.layout
     acc = accounting(w)
     h = km.create(lay)
@@ -358,10 +382,7 @@ def kamera_arm(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1) / args.steps
     kern_ms = {"reuse_copy_kernel": statistics.fmean(t[0].elapsed_time(t[1]) for t in marks),
                "reuse_kernel": statistics.fmean(t[1].elapsed_time(t[2]) for t in marks)}
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = job_time_ms(ms, world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
 
@@ -392,7 +413,7 @@ def kamera_arm(args, rank, world, local_rank):
                          "frac": kb / (kms / 1e3) / 1e9 / peak if kms > 0 else None}
     line = {
         "metric": METRIC,
-        "value": acc["written"] * world / s / 1e9,
+        "value": whole_job_gbs(acc["written"], world, ms),
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -19,7 +19,7 @@ Reuse, Eq. 1 in §1 and §3; App. A "Forming and applying the patch"):
   * The result is written into a paged KV pool at the chunk's new slots (§6 "Recompute-free
     on a live engine": SGLang's paged KV pool).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * inv_freq_i = θ^(-2i/d), i < d/2, d = rotary dim (head_dim for GQA/MHA, the 64-dim k_pe band
     for MLA); the angle δ·inv_freq_i is formed in float64 and cos/sin taken in float64.
   * NeoX-half pairing pairs dim i with i + d/2 inside a rope band; interleaved pairs 2i, 2i+1.
