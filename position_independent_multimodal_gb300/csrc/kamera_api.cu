@@ -118,6 +118,16 @@ kamera_status check_pool(const DevLayout &l, const kamera_pool *p, DevPool *out)
 
 kamera_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA; }
 
+// The persistent warp-specialised kernel takes every layer of the layouts it serves (with the
+// tensor engine); other layouts run the streaming kernel plus the general patched pipeline.
+kamera::SmemPlan reuse_plan(const kamera_handle *h, int max_m) {
+  if (h->engine == kamera::kEngineTensor && kamera::fast_layout(h->lay))
+    return kamera::reuse_ws_plan(h->lay, max_m);
+  return kamera::reuse_smem_plan(h->lay, max_m);
+}
+
+
+
 }  // namespace
 
 extern "C" {
@@ -194,10 +204,11 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.max_tokens = item->num_tokens;
   a.max_m = item->patch_m;
   a.engine = h->engine;
-  a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
+  a.smem = reuse_plan(h, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+  if (a.smem.fast) return from_cuda(kamera::launch_reuse_ws(a, strm));
   // unpatched layers stream through registers; patched layers take the tensor-core pipeline
   cudaError_t e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess && item->patch_m > 0 && item->patch_l1 > item->patch_l0)
@@ -226,7 +237,7 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
   a.max_tokens = max_tokens;
   a.max_m = max_patch_m;
   a.engine = h->engine;
-  a.smem = kamera::reuse_smem_plan(h->lay, a.max_m);
+  a.smem = reuse_plan(h, a.max_m);
   a.status = d_status;
   a.freq = h->freq;
   if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
@@ -236,8 +247,14 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
     if (!events || !events[i]) return cudaSuccess;
     return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), strm);
   };
-  // unpatched layers stream through registers; patched layers take the tensor-core pipeline
   cudaError_t e = mark(0);
+  if (a.smem.fast) {  // one persistent kernel: marks 1 and 2 both follow it
+    if (e == cudaSuccess) e = kamera::launch_reuse_ws(a, strm);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = mark(2);
+    return from_cuda(e);
+  }
+  // unpatched layers stream through registers; patched layers take the tensor-core pipeline
   if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess && max_patch_m > 0) e = kamera::launch_reuse(a, num_items, strm);

@@ -51,6 +51,8 @@ struct SmemPlan {
   int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
   int acc_cols;          // TMEM columns of one accumulator
   int u_bufs;            // U buffers (2: staged two tiles ahead; 1: after each MMA)
+  int fast;              // 1: plan of reuse_ws_kernel (swizzled stages, identity operand at desc)
+  int nstages;           // reuse_ws_kernel: pipeline stages
 };
 
 // A column tile: [col0, col0 + ncols) of a channel's row.
@@ -319,6 +321,9 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
 // Kernel launchers.
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
+bool fast_layout(const DevLayout &l);                               // kamera_reuse_ws.cu
+SmemPlan reuse_ws_plan(const DevLayout &l, int max_m);
+cudaError_t launch_reuse_ws(const ReuseArgs &a, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,

@@ -17,6 +17,7 @@
 // staged operands. Unpatched layers never reach this kernel (see reuse_copy_kernel).
 #include "kamera_dev.cuh"
 #include "kamera_ptx.cuh"
+#include "kamera_smem.cuh"
 
 namespace kamera {
 
@@ -24,101 +25,6 @@ namespace {
 
 constexpr int kThr = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any MMA of one tile
-
-__device__ __forceinline__ uint4 lds16(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-__device__ __forceinline__ void sts16(uint32_t a, const uint4 &v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)v) : "memory");
-}
-__device__ __forceinline__ void stg16(void *p, const uint4 &v) {
-  *reinterpret_cast<uint4 *>(p) = v;
-}
-__device__ __forceinline__ uint32_t ldg_u16(const __nv_bfloat16 *p) {
-  return __ldg(reinterpret_cast<const unsigned short *>(p));
-}
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
-
-// Two float32 lanes in one 64-bit register, for the packed f32x2 arithmetic of sm_100+.
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 f2(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-// bf16 pair (low, high half of a 32-bit word) -> two float32 lanes
-__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
-  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-__device__ __forceinline__ uint32_t f2_to_bf2(f32x2 v) {
-  float lo, hi;
-  f2_split(v, lo, hi);
-  return pack2_rn(lo, hi);
-}
-
-// e -> (e / n, e % n) with a shift when n is a power of two
-struct DivMod {
-  int n, sh;  // sh >= 0: n == 1 << sh
-  __device__ __forceinline__ explicit DivMod(int n_) : n(n_), sh(-1) {
-    if ((n_ & (n_ - 1)) == 0) {
-      sh = 0;
-      while ((1 << sh) < n_) ++sh;
-    }
-  }
-  __device__ __forceinline__ void split(int e, int *q, int *r) const {
-    if (sh >= 0) {
-      *q = e >> sh;
-      *r = e & (n - 1);
-    } else {
-      *q = e / n;
-      *r = e - *q * n;
-    }
-  }
-};
-
-// Patch value of 8 consecutive tile columns [n0, n0+8) of row r from the staged operands
-// (the CUDA-core contraction). A: element (r, k) at ((k/8)*16 + r/8)*128 + (r%8)*16 +
-// (k%8)*2; B (MN-major): element (n, k) at ((k/8)*ncore + n/8)*128 + (k%8)*16 + (n%8)*2.
-__device__ __forceinline__ void fma_patch8(uint32_t a_base, uint32_t b_base, int r, int n0, int m,
-                                           int ncore, float *p) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) p[e] = 0.f;
-  for (int k = 0; k < m; ++k) {
-    const float u = bf16_bits_to_float(
-        lds_u16(a_base + (((k >> 3) * 16 + (r >> 3)) << 7) + ((r & 7) << 4) + ((k & 7) << 1)));
-    float v[8];
-    unpack8(lds16(b_base + (((k >> 3) * ncore + (n0 >> 3)) << 7) + ((k & 7) << 4)), v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) p[e] = fmaf(u, v[e], p[e]);
-  }
-}
 
 struct PatchSrc {
   bool tensor;
@@ -571,16 +477,10 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;  // the copy kernel's work
   const bool rotate = ch == 0 && it.delta != 0;
   const Tile tile = tile_of(lay, ch, ct, rotate);
-  const bool neox = lay.style == KAMERA_ROPE_NEOX_HALF;
   // compile-time shapes of the reference layouts; everything else takes the general path
+  // (NeoX tiles of 64 or 128 columns with the tensor engine run in reuse_fast_kernel)
   if (tile.ncols == 128 && tile.band == 0) {
     run_task<128, 0>(a, smem, it, layer, ch, tile);
-  } else if (tile.ncols == 128 && tile.band == 128 && neox) {
-    run_task<128, 128>(a, smem, it, layer, ch, tile);
-  } else if (tile.ncols == 128 && tile.band == 64 && neox) {
-    run_task<128, 64>(a, smem, it, layer, ch, tile);
-  } else if (tile.ncols == 64 && tile.band == 64 && neox) {
-    run_task<64, 64>(a, smem, it, layer, ch, tile);
   } else if (tile.ncols == 64 && tile.band == 0) {
     run_task<64, 0>(a, smem, it, layer, ch, tile);
   } else {
@@ -593,7 +493,7 @@ int align128(int x) { return (x + 127) & ~127; }
 }  // namespace
 
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m) {
-  SmemPlan p;
+  SmemPlan p{};
   int widest = l.tw;
   if (l.kind == KAMERA_MLA && l.rope_d > widest) widest = l.rope_d;
   const int kp = max_m > 0 ? ((max_m + 15) & ~15) : 0;
