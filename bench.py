@@ -84,7 +84,7 @@ def accounting(w, items=None):
                 patch=out["tensor"]["patch"], meta=meta,
                 algorithmic=written + canon + out["tensor"]["patch"] + meta,
                 per_kernel={"reuse_copy_kernel": out["copy"]["algorithmic"],
-                            "reuse_fast_kernel": out["tensor"]["algorithmic"]})
+                            "reuse_tile_kernel": out["tensor"]["algorithmic"]})
 
 
 def measured_peak():
@@ -381,7 +381,7 @@ def kamera_arm(args, rank, world, local_rank):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
     kern_ms = {"reuse_copy_kernel": statistics.fmean(t[0].elapsed_time(t[1]) for t in marks),
-               "reuse_fast_kernel": statistics.fmean(t[1].elapsed_time(t[2]) for t in marks)}
+               "reuse_tile_kernel": statistics.fmean(t[1].elapsed_time(t[2]) for t in marks)}
     ms = job_time_ms(ms, world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed region")

@@ -118,11 +118,12 @@ kamera_status check_pool(const DevLayout &l, const kamera_pool *p, DevPool *out)
 
 kamera_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA; }
 
-// The persistent warp-specialised kernel takes every layer of the layouts it serves (with the
-// tensor engine); other layouts run the streaming kernel plus the general patched pipeline.
+// Unpatched layers always stream through the copy kernel. Patched layers take the per-tile
+// tensor-core kernel on the layouts it serves (with the tensor engine), else the general
+// patched pipeline.
 kamera::SmemPlan reuse_plan(const kamera_handle *h, int max_m) {
   if (h->engine == kamera::kEngineTensor && kamera::fast_layout(h->lay))
-    return kamera::reuse_ws_plan(h->lay, max_m);
+    return kamera::reuse_tile_plan(h->lay, max_m);
   return kamera::reuse_smem_plan(h->lay, max_m);
 }
 
@@ -208,11 +209,10 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.status = d_status;
   a.freq = h->freq;
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-  if (a.smem.fast) return from_cuda(kamera::launch_reuse_ws(a, strm));
   // unpatched layers stream through registers; patched layers take the tensor-core pipeline
   cudaError_t e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess && item->patch_m > 0 && item->patch_l1 > item->patch_l0)
-    e = kamera::launch_reuse(a, 1, strm);
+    e = a.smem.fast ? kamera::launch_reuse_tile(a, 1, strm) : kamera::launch_reuse(a, 1, strm);
   return from_cuda(e);
 }
 
@@ -247,17 +247,13 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
     if (!events || !events[i]) return cudaSuccess;
     return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), strm);
   };
-  cudaError_t e = mark(0);
-  if (a.smem.fast) {  // one persistent kernel: marks 1 and 2 both follow it
-    if (e == cudaSuccess) e = kamera::launch_reuse_ws(a, strm);
-    if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess) e = mark(2);
-    return from_cuda(e);
-  }
   // unpatched layers stream through registers; patched layers take the tensor-core pipeline
+  cudaError_t e = mark(0);
   if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess && max_patch_m > 0) e = kamera::launch_reuse(a, num_items, strm);
+  if (e == cudaSuccess && max_patch_m > 0)
+    e = a.smem.fast ? kamera::launch_reuse_tile(a, num_items, strm)
+                    : kamera::launch_reuse(a, num_items, strm);
   if (e == cudaSuccess) e = mark(2);
   return from_cuda(e);
 }

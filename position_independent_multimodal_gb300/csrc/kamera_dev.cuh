@@ -51,8 +51,7 @@ struct SmemPlan {
   int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
   int acc_cols;          // TMEM columns of one accumulator
   int u_bufs;            // U buffers (2: staged two tiles ahead; 1: after each MMA)
-  int fast;              // 1: plan of reuse_ws_kernel (swizzled stages, identity operand at desc)
-  int nstages;           // reuse_ws_kernel: pipeline stages
+  int fast;              // 1: plan of reuse_tile_kernel (swizzled tile, identity operand at desc)
 };
 
 // A column tile: [col0, col0 + ncols) of a channel's row.
@@ -204,6 +203,16 @@ struct ColUnit {
   int gca, gcb;  // columns inside the patch group
 };
 
+// Unit u of a region [c0, c0 + w) that does not rotate: two 8-column chunks from the same
+// 128-column group, half a group apart, so 8 consecutive units cover whole 128-byte lines
+// (the last group may be narrower).
+__device__ __forceinline__ void plain_unit(int c0, int w, int u, int *ca, int *cb) {
+  const int gbase = (u >> 3) * 128;
+  const int gw = (w - gbase) < 128 ? (w - gbase) : 128;
+  *ca = c0 + gbase + 8 * (u & 7);
+  *cb = *ca + (gw >> 1);
+}
+
 __device__ __forceinline__ int units_per_row(const DevLayout &l, int ch) {
   return (ch == 0 ? l.row_k : l.row_v) >> 4;
 }
@@ -212,8 +221,7 @@ __device__ __forceinline__ ColUnit col_unit(const DevLayout &l, int ch, int u, b
   ColUnit c;
   if (l.kind == KAMERA_GQA) {
     if (ch == 1 || !rotate) {
-      c.ca = u * 16;
-      c.cb = c.ca + 8;
+      plain_unit(0, ch == 0 ? l.row_k : l.row_v, u, &c.ca, &c.cb);
       c.rot = 0;
       c.fa = c.fb = 0;
     } else {
@@ -239,8 +247,7 @@ __device__ __forceinline__ ColUnit col_unit(const DevLayout &l, int ch, int u, b
   } else {
     const int lat_units = l.latent >> 4;
     if (u < lat_units) {
-      c.ca = u * 16;
-      c.cb = c.ca + 8;
+      plain_unit(0, l.latent, u, &c.ca, &c.cb);
       c.rot = 0;
       c.fa = c.fb = 0;
       c.group = 0;
@@ -249,8 +256,7 @@ __device__ __forceinline__ ColUnit col_unit(const DevLayout &l, int ch, int u, b
     } else {
       const int r = u - lat_units;
       if (!rotate) {
-        c.ca = l.latent + 16 * r;
-        c.cb = c.ca + 8;
+        plain_unit(l.latent, l.rope_d, r, &c.ca, &c.cb);
         c.rot = 0;
         c.fa = c.fb = 0;
       } else if (l.style == KAMERA_ROPE_NEOX_HALF) {
@@ -321,9 +327,9 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
 // Kernel launchers.
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
-bool fast_layout(const DevLayout &l);                               // kamera_reuse_ws.cu
-SmemPlan reuse_ws_plan(const DevLayout &l, int max_m);
-cudaError_t launch_reuse_ws(const ReuseArgs &a, cudaStream_t s);
+bool fast_layout(const DevLayout &l);                               // kamera_reuse_tile.cu
+SmemPlan reuse_tile_plan(const DevLayout &l, int max_m);
+cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,

@@ -1,0 +1,511 @@
+// Patched-layer kernel of the Kamera reuse operator for the common layouts (Eq. 1,
+// KV^(B|A) = R(delta) KV(B|empty) + U_m V_m^T written into the paged KV pool; App. A
+// "apply_reuse": a per-layer RoPE rotation plus a rank-m GEMM into the paged KV cache).
+//
+// Layouts served: NeoX-half pairing with column tiles of 64 or 128 columns holding whole heads
+// (GQA/MHA head_dim 64 or 128; MLA c_KV tiles of 64 or 128 and a k_pe band of 64 or 128),
+// tensor engine. Unpatched layers stream through reuse_copy_kernel; other layouts use
+// reuse_kernel.
+//
+// One CTA of 256 threads per task (item, patched layer, channel, column tile) walks the
+// chunk's tokens in tiles of 128 through two shared-memory stages; two CTAs share an SM. The
+// canonical rows of tile t+2 and their page ids are in flight (cp.async) while tile t is
+// finished, and U of tile t+1 lands during tile t's epilogue. Canonical tiles are staged in the
+// tensor core's 128-byte swizzled K-major layout (rows of 128 bytes per 64-column atom, 16-byte
+// chunk j of row r at chunk j ^ (r % 8)), so copies in and out move 4 rows x 128 bytes per
+// warp instruction and a thread that owns a row reads and writes its chunks without bank
+// conflicts. U rows (A operand) and V_m^T columns (B operand, staged once per task) are
+// no-swizzle core matrices. Per tile one thread issues tcgen05.mma into one of two TMEM
+// accumulators [128 lanes = tokens][tile columns]: the patch U V_m^T and, when the tile does
+// not rotate, the canonical tile itself as X I per 16-column block (I a 16 x 16 identity:
+// exact products, float32 accumulation); the MMA of tile t+1 runs while tile t is stored. In
+// the epilogue each token row belongs to two threads (TMEM lane quarter warp % 4, half warp / 4
+// of the columns): a folded tile only rounds the accumulator; a rotating tile rotates the
+// staged row on the CUDA cores (packed f32x2) and adds the patch; one rounding to bf16, written
+// back in place. Ranks that are not a multiple of 8 form the patch on the CUDA cores from the
+// staged operands.
+#include "kamera_dev.cuh"
+#include "kamera_ptx.cuh"
+#include "kamera_smem.cuh"
+
+namespace kamera {
+
+namespace {
+
+constexpr int kThrT = 256;
+constexpr uint64_t kWaitNsT = 2000000000ull;  // 2 s: far beyond one MMA
+constexpr int kAtomT = kTileRows * 128;       // one 64-column swizzle atom of a 128-row tile
+
+// Shared address of 16-byte chunk j (8 columns) of row r in a swizzled tile at x.
+__device__ __forceinline__ uint32_t swz(uint32_t x, int r, int j) {
+  return x + (j >> 3) * kAtomT + r * 128 + (((j & 7) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ int lds_i32t(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Canonical folded into the accumulator: round and write back. Half h owns the contiguous
+// chunks [h*NC/16, (h+1)*NC/16).
+template <int NC>
+__device__ __forceinline__ void epi_fold(uint32_t x, int r, int half, uint32_t trow) {
+  constexpr int CH = NC / 16;
+#pragma unroll
+  for (int q0 = 0; q0 < CH; q0 += 2) {
+    const int j0 = half * CH + q0;
+    uint32_t acc[16];
+    ptx::tmem_ld16(trow + j0 * 8, acc);
+    ptx::tmem_ld_wait(acc);
+    ptx::tmem_ld_wait(acc + 8);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        o[e] = pack2_rn(__uint_as_float(acc[8 * q + 2 * e]),
+                        __uint_as_float(acc[8 * q + 2 * e + 1]));
+      sts16(swz(x, r, j0 + q), make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+}
+
+// NeoX bands of width BAND, patch from TMEM: groups of 8 pairs (columns ca..ca+7, partners
+// cb = ca + BAND/2), a' = b*(-sin) + (a*cos + p_a), b' = a*sin + (b*cos + p_b) in packed f32x2
+// arithmetic, one rounding. Half h owns pairs [h*NC/4, (h+1)*NC/4). `rot` holds
+// cos[np] | sin[np] | -sin[np].
+template <int NC, int BAND>
+__device__ __forceinline__ void epi_rot(uint32_t x, int r, int half, uint32_t trow,
+                                        const float *rot, int np) {
+  constexpr int HB = BAND / 2, PAIRS_HALF = NC / 4, GROUPS = PAIRS_HALF / 8;
+#pragma unroll
+  for (int q = 0; q < GROUPS; ++q) {
+    const int p = half * PAIRS_HALF + q * 8;
+    const int head = p / HB, i = p % HB;
+    const int ca = head * BAND + i, cb = ca + HB;
+    uint32_t acc[16];
+    ptx::tmem_ld8(trow + ca, acc);
+    ptx::tmem_ld8(trow + cb, acc + 8);
+    const uint32_t aa = swz(x, r, ca >> 3), ab = swz(x, r, cb >> 3);
+    const uint4 ra = lds16(aa), rb = lds16(ab);
+    const float4 *cv = reinterpret_cast<const float4 *>(rot + i);
+    const float4 *sv = reinterpret_cast<const float4 *>(rot + np + i);
+    const float4 *nv = reinterpret_cast<const float4 *>(rot + 2 * np + i);
+    ptx::tmem_ld_wait(acc);
+    ptx::tmem_ld_wait(acc + 8);
+    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const float4 c4 = cv[h2], s4 = sv[h2], n4 = nv[h2];
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int j = 2 * h2 + g2;  // word j holds elements 2j, 2j+1
+        const f32x2 c = g2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
+        const f32x2 sn = g2 ? f2(s4.z, s4.w) : f2(s4.x, s4.y);
+        const f32x2 ns = g2 ? f2(n4.z, n4.w) : f2(n4.x, n4.y);
+        const f32x2 av = bf2_to_f2(wa[j]), bv = bf2_to_f2(wb[j]);
+        const f32x2 pa = f2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+        const f32x2 pb = f2(__uint_as_float(acc[8 + 2 * j]), __uint_as_float(acc[8 + 2 * j + 1]));
+        oa[j] = f2_to_bf2(fma2(bv, ns, fma2(av, c, pa)));
+        ob[j] = f2_to_bf2(fma2(av, sn, fma2(bv, c, pb)));
+      }
+    }
+    sts16(aa, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+    sts16(ab, make_uint4(ob[0], ob[1], ob[2], ob[3]));
+  }
+}
+
+// CUDA-core contraction (ranks that are not a multiple of 8): the patch of row r from the
+// staged operands, added to the staged row (rotated first when band > 0), one rounding. Each
+// half owns the chunks of epi_fold / epi_rot.
+__device__ __noinline__ void epi_fma(uint32_t x, int r, int half, int nc, int band,
+                                     uint32_t a_op, uint32_t b_op, int m, const float *rot,
+                                     int np) {
+  const int ncore = nc >> 3;
+  if (band > 0) {
+    const int hb = band >> 1, pairs_half = nc >> 2;
+    for (int g = 0; g < pairs_half / 8; ++g) {
+      const int p = half * pairs_half + g * 8;
+      const int head = p / hb, i = p % hb;
+      const int ca = head * band + i, cb = ca + hb;
+      float pa[8], pb[8], xa[8], xb[8];
+      fma_patch8(a_op, b_op, r, ca, m, ncore, pa);
+      fma_patch8(a_op, b_op, r, cb, m, ncore, pb);
+      const uint32_t aa = swz(x, r, ca >> 3), ab = swz(x, r, cb >> 3);
+      unpack8(lds16(aa), xa);
+      unpack8(lds16(ab), xb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        rot_pair(xa[e], xb[e], make_float2(rot[i + e], rot[np + i + e]));
+        xa[e] += pa[e];
+        xb[e] += pb[e];
+      }
+      sts16(aa, pack8_rn(xa));
+      sts16(ab, pack8_rn(xb));
+    }
+  } else {
+    const int per_half = ncore >> 1;
+    for (int j = half * per_half; j < (half + 1) * per_half; ++j) {
+      float p[8], xv[8];
+      fma_patch8(a_op, b_op, r, 8 * j, m, ncore, p);
+      const uint32_t ad = swz(x, r, j);
+      unpack8(lds16(ad), xv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xv[e] += p[e];
+      sts16(ad, pack8_rn(xv));
+    }
+  }
+}
+
+template <int NC, int BAND>
+__device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsigned char *sp,
+                                          const kamera_item &it, int layer, int ch,
+                                          const Tile &tile) {
+  constexpr int ATOMS = NC / 64;
+  constexpr int NCORE = NC / 8;
+  const SmemPlan &P = a.smem;
+  const DevLayout &lay = a.lay;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = it.num_tokens, m = it.patch_m, Kp = (m + 15) & ~15, m8 = m >> 3;
+  const int row = ch == 0 ? lay.row_k : lay.row_v;
+  const bool tensor = (m & 7) == 0 && aligned16(it.patch_u);
+  const bool fold = tensor && BAND == 0;
+  const bool u2 = P.u_bufs == 2;  // U of tile t+2 staged with its rows (else one buffer)
+  const int ps = lay.page_size;
+  const int ntt = (T + kTileRows - 1) / kTileRows;
+  const uint32_t x_op = s0 + P.canon, v_op = s0 + P.b_op;
+  const uint32_t id_op = s0 + P.desc, pg_op = s0 + P.pages;
+  const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
+  volatile int *flag = reinterpret_cast<volatile int *>(sp + P.misc + 4);
+  unsigned long long *rowptr = reinterpret_cast<unsigned long long *>(sp + P.slots);
+  float *rot = reinterpret_cast<float *>(sp + P.cs);
+  const int li = layer - it.patch_l0;
+  const __nv_bfloat16 *U = static_cast<const __nv_bfloat16 *>(it.patch_u) +
+                           (long long)(li * 2 + tile.group) * T * m;
+  const __nv_bfloat16 *canon = static_cast<const __nv_bfloat16 *>(ch == 0 ? it.canon_k
+                                                                           : it.canon_v) +
+                               (long long)layer * T * row + tile.col0;
+  auto u_buf = [&](int t) { return s0 + P.a_op + (u2 ? (t & 1) * P.a_stage : 0); };
+  const int lc = tid & 7, lr = tid >> 3;  // copies: chunk of an atom row, row of each pass
+  const uint32_t swc = (uint32_t)((lc ^ (lr & 7)) << 4);
+  const DivMod md(m8 > 0 ? m8 : 1);
+  const DivMod psd(ps);
+
+  // canonical rows of tile t into stage s (4 rows x 128 bytes per warp instruction) and the
+  // page ids of its tokens
+  auto issue_x = [&](int t, int s) {
+    const int t0 = t * kTileRows, rows = min(kTileRows, T - t0);
+    const __nv_bfloat16 *src = canon + (long long)(t0 + lr) * row + 8 * lc;
+    const uint32_t dst = x_op + s * P.stage + lr * 128 + swc;
+    const long long step = 32ll * row;
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      if (lr + 32 * pr < rows) {
+#pragma unroll
+        for (int at = 0; at < ATOMS; ++at)
+          ptx::cp_async16(dst + at * kAtomT + pr * 32 * 128, src + pr * step + at * 64, 16u);
+      }
+    }
+    int p_first, off0, npages, dummy;
+    psd.split(it.start_tok + t0, &p_first, &off0);
+    psd.split(off0 + rows - 1, &npages, &dummy);
+    const int32_t *ptab = a.pool.pt + (long long)it.req * a.pool.pt_stride + p_first;
+    for (int e = tid; e <= npages; e += kThrT)
+      ptx::cp_async4(pg_op + s * P.pages_stage + 4 * e, ptab + e);
+  };
+  // U rows of tile t as the A operand (K-major core matrices). Rows past the chunk stay stale
+  // (their accumulator rows are never stored); the rank padding was zeroed once.
+  auto issue_u = [&](int t) {
+    const int t0 = t * kTileRows, rows = min(kTileRows, T - t0);
+    const __nv_bfloat16 *Ut = U + (long long)t0 * m;
+    const uint32_t ub = u_buf(t);
+    if (tensor) {
+      for (int e = tid; e < rows * m8; e += kThrT) {
+        int rr, kc;
+        md.split(e, &rr, &kc);
+        ptx::cp_async16(ub + ((kc * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4),
+                        Ut + (long long)rr * m + kc * 8, 16u);
+      }
+    } else {
+      for (int e = tid; e < kTileRows * Kp; e += kThrT) {
+        const int rr = e / Kp, k = e - rr * Kp;
+        const uint32_t v = (rr < rows && k < m) ? ldg_u16(Ut + (long long)rr * m + k) : 0u;
+        sts_u16(ub + (((k >> 3) * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4) + ((k & 7) << 1), v);
+      }
+    }
+  };
+  uint32_t tmem = 0;
+  // MMA of tile t into accumulator t & 1 (one thread); arrives on barrier t & 1
+  auto issue_mma = [&](int t) {
+    ptx::tc_fence_after();
+    const uint32_t ub = u_buf(t), d = tmem + (t & 1) * P.acc_cols;
+    // no-swizzle layouts: K-major A with the K step (2048) as leading offset and the M step
+    // (128) as stride; MN-major B with the K step as leading offset and the N step as stride
+    const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, NC) | (1u << 16);
+    for (int ks = 0; ks < Kp / 16; ++ks)
+      ptx::mma_bf16(d, ptx::smem_desc(ub + ks * 2 * 2048, 2048, 128),
+                    ptx::smem_desc(v_op + ks * 2 * NCORE * 128, NCORE * 128, 128), idesc,
+                    ks > 0 ? 1u : 0u);
+    if (fold) {  // D[:, 16j..16j+15] += X[:, 16j..16j+15] * I
+      const uint32_t idesc16 = ptx::idesc_bf16_f32(kTileRows, 16) | (1u << 16);
+      const uint64_t bd = ptx::smem_desc(id_op, 256, 128);
+      const uint32_t xs = x_op + (t & 1) * P.stage;
+#pragma unroll
+      for (int j = 0; j < NC / 16; ++j)
+        ptx::mma_bf16(d + 16 * j, ptx::smem_desc_sw128(xs + (j >> 2) * kAtomT + (j & 3) * 32),
+                      bd, idesc16, 1u);
+    }
+    ptx::mma_commit(s_bar + 8 * (t & 1));
+  };
+
+  if (warp == 0) {
+    ptx::tmem_alloc(s_tmem, P.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    ptx::mbar_init(s_bar, 1);
+    ptx::mbar_init(s_bar + 8, 1);
+    ptx::fence_mbar_init();
+    *flag = 0;
+  }
+  if (BAND > 0)  // cos/sin of the item's offset, once per CTA
+    for (int i = tid; i < lay.npairs; i += kThrT) {
+      const float2 c = rope_phase(a.freq.q[i], it.delta);
+      rot[i] = c.x;
+      rot[lay.npairs + i] = c.y;
+      rot[2 * lay.npairs + i] = -c.y;
+    }
+  if (tensor && (Kp >> 3) > m8)  // rank padding of the U buffers: zero (meets zero V_m^T rows)
+    for (int e = tid; e < (u2 ? 2 : 1) * kTileRows; e += kThrT) {
+      const int b = e >> 7, rr = e & 127;
+      sts16(s0 + P.a_op + b * P.a_stage + ((m8 * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4),
+            make_uint4(0u, 0u, 0u, 0u));
+    }
+  if (fold) {  // 16 x 16 identity, MN-major core matrices (element (n, k))
+    const int n = tid & 15, k = tid >> 4;
+    sts_u16(id_op + ((k >> 3) * 2 + (n >> 3)) * 128 + (k & 7) * 16 + (n & 7) * 2,
+            n == k ? 0x3F80u : 0u);
+  }
+  {  // V_m^T of the tile, once: MN-major core matrices, ranks past m zero
+    const int wg = tile.group == 0 ? lay.w0 : lay.w1;
+    const __nv_bfloat16 *vt = static_cast<const __nv_bfloat16 *>(it.patch_vt) +
+                              (long long)li * m * (lay.w0 + lay.w1) +
+                              (tile.group == 0 ? 0 : (long long)m * lay.w0) + tile.gcol0;
+    for (int e = tid; e < Kp * NCORE; e += kThrT) {
+      const int k = e / NCORE, j = e % NCORE;
+      const bool ok = k < m;
+      ptx::cp_async16(v_op + ((k >> 3) * NCORE + j) * 128 + (k & 7) * 16,
+                      ok ? (const void *)(vt + (long long)k * wg + 8 * j) : (const void *)vt,
+                      ok ? 16u : 0u);
+    }
+  }
+  issue_x(0, 0);
+  issue_u(0);
+  ptx::cp_async_commit();
+  if (ntt > 1) {
+    issue_x(1, 1);
+    if (u2) issue_u(1);
+  }
+  ptx::cp_async_commit();
+  ptx::cp_async_wait_group1();  // tile 0 (and V_m^T)
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();  // TMEM address, barriers, identity, table, tile 0 visible
+  ptx::tc_fence_after();
+  tmem = *reinterpret_cast<volatile uint32_t *>(sp + P.misc);
+  bool timed_out = false;
+  if (tensor && tid == 0) issue_mma(0);
+  const int r = ((warp & 3) << 5) + lane;  // epilogue row (TMEM lane)
+  const int half = warp >> 2;
+  const uint32_t trow0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+  for (int t = 0; t < ntt; ++t) {
+    const int s = t & 1;
+    const int t0 = t * kTileRows, rows = min(kTileRows, T - t0);
+    const bool use_tc = tensor && !timed_out;
+    if (use_tc) {  // warp 0 waits for MMA(t); the other warps sleep at the barrier
+      if (warp == 0) {
+        const bool ok = ptx::mbar_wait(s_bar + 8 * s, (t >> 1) & 1, kWaitNsT);
+        if (lane == 0 && !ok) *flag = 1;
+      }
+      ptx::tc_fence_before();
+      __syncthreads();
+      ptx::tc_fence_after();
+      if (*flag) {
+        timed_out = true;
+        if (tid == 0) atomicOr(a.status, KAMERA_DEVICE_TIMEOUT);
+      }
+      // one U buffer: MMA(t) has read it, so U of tile t+1 may land now
+      if (!u2 && t + 1 < ntt) issue_u(t + 1);
+      ptx::cp_async_commit();
+    }
+    const bool write = !(tensor && timed_out);
+    const uint32_t xs = x_op + s * P.stage;
+    if (write) {
+      if (use_tc) {
+        if constexpr (BAND == 0)
+          epi_fold<NC>(xs, r, half, trow0 + s * P.acc_cols);
+        else
+          epi_rot<NC, BAND>(xs, r, half, trow0 + s * P.acc_cols, rot, lay.npairs);
+      } else if (!tensor && r < rows) {
+        epi_fma(xs, r, half, NC, BAND, u_buf(t), v_op, m, rot, lay.npairs);
+      }
+    }
+    if (half == 0 && r < rows) {  // the row's owner finds its slot
+      int pg, in_page, p_first, off0;
+      psd.split(it.start_tok + t0 + r, &pg, &in_page);
+      psd.split(it.start_tok + t0, &p_first, &off0);
+      const int page = lds_i32t(pg_op + s * P.pages_stage + 4 * (pg - p_first));
+      unsigned long long dst = 0;
+      if (page >= 0 && (long long)(page + 1) * ps <= a.pool.num_slots)
+        dst = static_cast<unsigned long long>(__cvta_generic_to_global(
+            (ch == 0 ? a.pool.k : a.pool.v) +
+            ((long long)layer * a.pool.num_slots + (long long)page * ps + in_page) * row +
+            tile.col0));
+      else
+        atomicOr(a.status, KAMERA_DEVICE_SLOT_OOB);
+      rowptr[r] = dst;
+    }
+    // the CUDA-core path with one U buffer reads U(t) in the epilogue: U(t+1) after it
+    if (!u2 && !tensor && t + 1 < ntt) {
+      __syncthreads();
+      issue_u(t + 1);
+      ptx::cp_async_commit();
+    }
+    ptx::cp_async_wait_all();  // tile t+1's rows, pages and U
+    ptx::fence_proxy_async_smem();
+    if (use_tc) ptx::tc_fence_before();
+    __syncthreads();  // rows of tile t complete, tile t+1 staged
+    if (tensor && !timed_out && t + 1 < ntt && tid == 0) issue_mma(t + 1);
+    if (write) {  // 4 rows x 128 bytes per warp instruction
+      const uint32_t src = xs + lr * 128 + swc;
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        const int rr = lr + 32 * pr;
+        if (rr < rows) {
+          const unsigned long long dst = rowptr[rr];
+          if (dst) {
+#pragma unroll
+            for (int at = 0; at < ATOMS; ++at)
+              stg16_global(reinterpret_cast<void *>(dst + 128ull * at + 16ull * lc),
+                           lds16(src + at * kAtomT + pr * 32 * 128));
+          }
+        }
+      }
+    }
+    __syncthreads();  // stage s is free
+    if (t + 2 < ntt) {
+      issue_x(t + 2, s);
+      if (u2) issue_u(t + 2);
+    }
+    ptx::cp_async_commit();
+  }
+  ptx::cp_async_wait_all();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
+}
+
+__global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_constant__ ReuseArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t s0 = (raw + 1023u) & ~1023u;  // the swizzle atoms need 1024-byte alignment
+  unsigned char *sp = smem_raw + (s0 - raw);
+  const DevLayout &lay = a.lay;
+  const int ct = blockIdx.x, item = blockIdx.y;
+  const int layer = blockIdx.z / lay.n_ch;
+  const int ch = blockIdx.z - layer * lay.n_ch;
+  const kamera_item it = a.items ? a.items[item] : a.single;
+  // rejected items are reported by the copy kernel; unpatched layers are its work too
+  if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) return;
+  if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;
+  const bool rotate = ch == 0 && it.delta != 0;
+  const Tile tile = tile_of(lay, ch, ct, rotate);
+  if (tile.ncols == 128) {
+    if (tile.band == 0)
+      task_loop<128, 0>(a, s0, sp, it, layer, ch, tile);
+    else if (tile.band == 128)
+      task_loop<128, 128>(a, s0, sp, it, layer, ch, tile);
+    else
+      task_loop<128, 64>(a, s0, sp, it, layer, ch, tile);
+  } else {
+    if (tile.band == 0)
+      task_loop<64, 0>(a, s0, sp, it, layer, ch, tile);
+    else
+      task_loop<64, 64>(a, s0, sp, it, layer, ch, tile);
+  }
+}
+
+int align128t(int x) { return (x + 127) & ~127; }
+
+}  // namespace
+
+bool fast_layout(const DevLayout &l) {
+  if (l.style != KAMERA_ROPE_NEOX_HALF) return false;
+  if (l.tw != 64 && l.tw != 128) return false;
+  if (l.kind == KAMERA_GQA) return (l.hd == 64 || l.hd == 128) && l.hd <= l.tw && l.row_k % l.tw == 0;
+  return l.latent % l.tw == 0 && (l.rope_d == 64 || l.rope_d == 128);
+}
+
+SmemPlan reuse_tile_plan(const DevLayout &l, int max_m) {
+  SmemPlan p{};
+  int widest = l.tw;
+  if (l.kind == KAMERA_MLA && l.rope_d > widest) widest = l.rope_d;
+  const int kp = max_m > 0 ? ((max_m + 15) & ~15) : 16;
+  p.fast = 1;
+  p.pitch = widest * 2;
+  p.stage = kTileRows * widest * 2;  // a multiple of 1024: the swizzle atoms stay aligned
+  p.a_stage = align128t(kTileRows * kp * 2);
+  p.b_stage = align128t(widest * kp * 2);
+  p.cs_stage = align128t(l.npairs * 12);
+  p.pages_stage = align128t((kTileRows / l.page_size + 2) * 4);
+  const int fixed = 2 * p.stage + p.b_stage + 512 + p.cs_stage + 2 * p.pages_stage +
+                    kTileRows * 8 + 128 + 1024;
+  // two U buffers when two CTAs still fit on an SM (227 KB of shared memory, 1 KB reserved
+  // per CTA), else one
+  p.u_bufs = (fixed + 2 * p.a_stage + 1024) * 2 <= 227 * 1024 ? 2 : 1;
+  int off = 0;
+  p.canon = off;  // two stages of swizzled tiles, first so they stay 1024-aligned
+  off += 2 * p.stage;
+  p.b_op = off;
+  off += p.b_stage;
+  p.a_op = off;
+  off += p.u_bufs * p.a_stage;
+  p.desc = off;  // the 16 x 16 identity operand
+  off += 512;
+  p.cs = off;
+  off += p.cs_stage;
+  p.pages = off;
+  off += 2 * p.pages_stage;
+  p.slots = off;  // global addresses of the rows of the tile being stored
+  off += kTileRows * 8;
+  p.misc = off;   // TMEM address, timeout flag, two MMA barriers
+  off += 128;
+  p.total = off + 1024;  // slack to align the base to 1024 bytes
+  int cols = 32;
+  while (cols < widest) cols <<= 1;
+  p.acc_cols = cols;
+  p.tmem_cols = 2 * cols;
+  return p;
+}
+
+cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s) {
+  static int configured_smem[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (a.smem.total > configured_smem[dev] && a.smem.total > 48 * 1024) {
+    e = cudaFuncSetAttribute(reuse_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             a.smem.total);
+    if (e != cudaSuccess) return e;
+    configured_smem[dev] = a.smem.total;
+  }
+  dim3 grid(a.lay.ntile, n_items, a.lay.L * a.lay.n_ch);
+  reuse_tile_kernel<<<grid, kThrT, a.smem.total, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kamera
