@@ -87,6 +87,30 @@ def accounting(w, items=None):
                             "reuse_tile_kernel": out["tensor"]["algorithmic"]})
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when there is
+    no record or the kernel's sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    try:
+        rec = {}
+        for line in open(path):
+            line = line.strip()
+            if line and not line.startswith("#") and "=" in line:
+                k, v = line.split("=", 1)
+                rec[k.strip()] = v.strip()
+        csrc = os.path.join(ROOT, "position_independent_multimodal_gb300", "csrc")
+        h = hashlib.sha256()
+        for f in ("kamera_reuse_tile.cu", "kamera_dev.cuh", "kamera_ptx.cuh", "kamera_smem.cuh"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+        if rec.get("kernel") != kernel or rec.get("source_sha256") != h.hexdigest():
+            return None
+        return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -424,7 +448,8 @@ def kamera_arm(args, rank, world, local_rank):
         "gb_s_moved": achieved * world,
         "frac_hbm_peak": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
-                     "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": None,
+                     "unit": "GB/s", "frac": kernels[dom]["frac"],
+                     "traffic": recorded_traffic(dom),
                      "kernel": dom, "algorithmic_bytes_per_launch": acc["per_kernel"][dom],
                      "launch_ms": kern_ms[dom],
                      "peak_source": (f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
