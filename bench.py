@@ -367,8 +367,9 @@ def kamera_arm(args, rank, world, local_rank):
     n_items = len(w.items)
     max_m = max(it.patch_m for it in w.items)
     stream = torch.cuda.current_stream()
-    # three events per timed step: before, between and after the call's two kernels
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # three events per split step: before, between and after the call's two kernels
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+             for _ in range(min(args.steps, 1000))]
     for trio in marks:
         for e in trio:
             e.record(stream)  # creates the event handles
@@ -395,13 +396,20 @@ def kamera_arm(args, rank, world, local_rank):
     clocks.start()
     barrier()
     torch.cuda.synchronize()
+    # the step as a user runs it: the two kernels side by side (copy kernel on the library's
+    # side stream, joined back before the next step)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        step(marks[i])
+        step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
+    # per-kernel split for the roofline: the same call with event marks between its kernels,
+    # which runs them one after the other on the stream
+    for i in range(len(marks)):
+        step(marks[i])
+    torch.cuda.synchronize()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
     kern_ms = {"reuse_copy_kernel": statistics.fmean(t[0].elapsed_time(t[1]) for t in marks),
@@ -456,6 +464,9 @@ def kamera_arm(args, rank, world, local_rank):
                                      else "fallback 6.8 TB/s")},
         "kernels": kernels,
         "gpu_launches": 2 * args.steps,
+        "kernel_split": (f"per-kernel times from {len(marks)} further steps with event marks "
+                         f"between the two kernels (run one after the other); the headline "
+                         f"step runs them side by side"),
         "clocks": clk,
     }
     if e2e:

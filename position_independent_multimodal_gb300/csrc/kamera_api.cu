@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "kamera_dev.cuh"
@@ -118,6 +119,57 @@ kamera_status check_pool(const DevLayout &l, const kamera_pool *p, DevPool *out)
 
 kamera_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA; }
 
+// A side stream per device on which the copy kernel runs next to the patched-layer kernel (the
+// two write disjoint layers). The caller's stream forks into it and joins it again through two
+// events, so work issued on the caller's stream afterwards waits for both kernels. Created on
+// the first call that needs it on that device; a failure to create it only serialises the two
+// kernels on the caller's stream.
+struct SideStream {
+  std::mutex mu;
+  bool tried = false;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[64];
+
+SideStream *side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream &ss = g_side[dev];
+  std::lock_guard<std::mutex> lock(ss.mu);
+  if (!ss.tried) {
+    ss.tried = true;
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      ss.stream = nullptr;
+    }
+  }
+  return ss.stream ? &ss : nullptr;
+}
+
+// Patched layers on the caller's stream, unpatched layers on the side stream at the same time
+// (layouts served by the tile kernel); otherwise the two kernels in order on the caller's
+// stream.
+cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, cudaStream_t s) {
+  SideStream *ss = (a.smem.fast && patched) ? side_stream() : nullptr;
+  if (!ss) {
+    cudaError_t e = kamera::launch_reuse_copy(a, s);
+    if (e == cudaSuccess && patched)
+      e = a.smem.fast ? kamera::launch_reuse_tile(a, n_items, s)
+                      : kamera::launch_reuse(a, n_items, s);
+    return e;
+  }
+  std::lock_guard<std::mutex> lock(ss->mu);  // one fork/join at a time per device
+  cudaError_t e = cudaEventRecord(ss->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
+  if (e == cudaSuccess) e = kamera::launch_reuse_tile(a, n_items, s);
+  if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, ss->stream);
+  if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ss->join, 0);
+  return e;
+}
+
 // Unpatched layers always stream through the copy kernel. Patched layers take the per-tile
 // tensor-core kernel on the layouts it serves (with the tensor engine), else the general
 // patched pipeline.
@@ -210,10 +262,8 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.freq = h->freq;
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
   // unpatched layers stream through registers; patched layers take the tensor-core pipeline
-  cudaError_t e = kamera::launch_reuse_copy(a, strm);
-  if (e == cudaSuccess && item->patch_m > 0 && item->patch_l1 > item->patch_l0)
-    e = a.smem.fast ? kamera::launch_reuse_tile(a, 1, strm) : kamera::launch_reuse(a, 1, strm);
-  return from_cuda(e);
+  return from_cuda(
+      launch_both(a, 1, item->patch_m > 0 && item->patch_l1 > item->patch_l0, strm));
 }
 
 namespace {
@@ -247,7 +297,8 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
     if (!events || !events[i]) return cudaSuccess;
     return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), strm);
   };
-  // unpatched layers stream through registers; patched layers take the tensor-core pipeline
+  if (!events) return from_cuda(launch_both(a, num_items, max_patch_m > 0, strm));
+  // timed: the two kernels in order on the caller's stream, marks around each
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess) e = mark(1);
