@@ -14,8 +14,12 @@
  * "apply_reuse": a per-layer RoPE rotation plus a GEMM into the paged KV cache).
  *
  * Conventions shared by every call:
- *   - All tensors are device memory owned by the caller. The library allocates nothing, keeps
- *     no pointer after a call returns and never modifies the canonical or patch stores.
+ *   - All tensors are device memory owned by the caller. The library allocates no device
+ *     memory, keeps no pointer after a call returns and never modifies the canonical or patch
+ *     stores. The first reuse call on a device that runs both of its kernels creates one
+ *     non-blocking stream and two events for that device, kept until the process exits: the
+ *     kernel for unpatched layers runs there beside the one for patched layers, forked from and
+ *     joined back into the caller's stream, so stream order is as if both ran on it.
  *   - bf16 everywhere for data; float32 arithmetic inside, one round-to-nearest-even to bf16.
  *   - Calls are asynchronous on the given stream (NULL = the legacy default stream).
  *   - Host-checkable errors return synchronously and launch nothing.
