@@ -523,6 +523,39 @@ def other_workloads(dev):
             raise RuntimeError(f"device status {int(st.item())}")
         return ms
 
+    # reversible switch: the patch re-added in place on the cached rows of the 18 reorder
+    # placements (their patched layers), alternately added and removed
+    w = wl.config2(device=dev)
+    lay = w.layout
+    h = km.create(lay)
+    k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_items = km.pack_items(w.items).to(dev)
+    km.kamera_batch_reuse(h, d_items, len(w.items), 1024, 32, pool, st)
+    flips = [1]
+
+    def readd():
+        sign = flips[0]
+        flips[0] = -sign
+        km.kamera_batch_patch_inplace(h, d_items, len(w.items), 1024, 32, pool, sign, st)
+    ms = time_calls(readd, 20, warmup=4)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    rows = sum(it.num_tokens * (it.patch_l1 - it.patch_l0) for it in w.items)
+    moved = rows * (lay.row_k + lay.row_v) * 2 * 2 + \
+        sum((it.patch_u.numel() + it.patch_vt.numel()) * 2 for it in w.items[:3])
+    out["patch_readd_in_place_18_placements"] = {
+        "workload": "GQA reorder pool (28 layers, H_kv=4 x 128): rank-32 patch re-added in place "
+                    "on layers 14-27 of all 18 placements (one batched call), alternately +1 "
+                    "and -1",
+        "ms_per_step": ms, "gb_s_moved": moved / ms / 1e6,
+        "frac_hbm_peak": moved / ms / 1e6 / peak}
+    del w, k, v, pool
+    torch.cuda.empty_cache()
+
     w = wl.config3(device=dev)
     acc = accounting(w)
     ms = reuse_calls(w, [w.items])

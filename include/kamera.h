@@ -192,6 +192,41 @@ kamera_status kamera_batch_reuse_timed(const kamera_handle *handle, const kamera
                                        kamera_stream_t stream, void *const events[3]);
 
 /*
+ * Conditioning switched back on in place (App. E "Context management as reversible state
+ * edits": reverting to the context-clean view is a copy of the stored canonical, which
+ * kamera_reuse with patch_m = 0 performs; re-applying conditioning is a single rank-m add).
+ * For every layer in [patch_l0, patch_l1) and both patch groups (GQA: K and V; MLA: c_KV and
+ * k_pe), the cached rows of logical tokens [start_tok, start_tok + num_tokens) of request req
+ * become bf16(row + sign * U V_m^T), with one rounding. Nothing rotates: the rows are already
+ * in their place. sign = -1 subtracts the same patch.
+ * patch_u, patch_vt: the chunk's factors in the kamera_item layout ([l1-l0][2][T][m] and
+ * [l1-l0][m*W0 + m*W1], bf16, device), with T = num_tokens.
+ * Returns UNSUPPORTED for layouts whose column tiles are not 64 or 128 columns wide (GQA rows
+ * not a multiple of the tile width, head_dim 256; MLA k_pe other than 64 or 128). Rows whose
+ * page falls outside the pool are skipped with KAMERA_DEVICE_SLOT_OOB. patch_m == 0,
+ * patch_l0 == patch_l1 or num_tokens == 0 launches nothing.
+ */
+kamera_status kamera_patch_inplace(const kamera_handle *handle, const kamera_pool *pool,
+                                   int32_t req, int32_t start_tok, int32_t num_tokens,
+                                   const void *patch_u, const void *patch_vt, int32_t patch_m,
+                                   int32_t patch_l0, int32_t patch_l1, int32_t sign,
+                                   uint32_t *d_status, kamera_stream_t stream);
+
+/*
+ * kamera_patch_inplace for many chunks in one launch. d_items is a device array of
+ * kamera_item; only num_tokens, req, start_tok, patch_u, patch_vt, patch_m, patch_l0 and
+ * patch_l1 are read (the canonical pointers and delta are ignored). Each item is checked on
+ * the device against the rules of kamera_patch_inplace plus num_tokens <= max_tokens and
+ * patch_m <= max_patch_m; a failing item sets KAMERA_DEVICE_BAD_ITEM and is skipped. Items
+ * must not cover the same rows.
+ */
+kamera_status kamera_batch_patch_inplace(const kamera_handle *handle, const kamera_item *d_items,
+                                         int32_t num_items, int32_t max_tokens,
+                                         int32_t max_patch_m, const kamera_pool *pool,
+                                         int32_t sign, uint32_t *d_status,
+                                         kamera_stream_t stream);
+
+/*
  * The RoPE phases the kernels use: for each of num_deltas offsets d_deltas[n] (device int64)
  * and each rope pair i of the layout, (cos, sin) of delta * inv_freq_i with inv_freq_i =
  * theta^(-2i/d), written as float32 pairs to d_out[n][rope_dim/2][2] (device). The angle is

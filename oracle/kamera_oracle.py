@@ -294,6 +294,35 @@ def relocate(layout, k_pool, page_table, req: int, start_tok: int, num_tokens: i
                 k_pool[layer, s, c0:c0 + d] = f64_to_bf16(rot)
 
 
+def patch_inplace(layout, k_pool, v_pool, page_table, req: int, start_tok: int,
+                  num_tokens: int, patch_u, patch_vt, m: int, l0: int, l1: int,
+                  sign: int = 1) -> None:
+    """Conditioning switched back on in place: the rank-m patch added to the cached rows of a
+    chunk (App. E "Context management as reversible state edits": re-applying conditioning
+    is a single rank-m add; the clean view it starts from is the stored canonical). For each
+    layer in [l0, l1) and each patch group, the rows of logical tokens
+    [start_tok, start_tok + num_tokens) of request ``req`` become row + sign · U·Vt, computed
+    in float64 and rounded once to bf16. ``sign = -1`` subtracts the same patch. Nothing
+    rotates; columns outside the groups do not exist (the groups tile the row)."""
+    if m <= 0 or l1 <= l0 or num_tokens <= 0:
+        return
+    page = layout.page_size
+    slots = [slot_of(page_table, req, start_tok + t, page) for t in range(num_tokens)]
+    n_ch = 2 if layout.kind == GQA else 1
+    for layer in range(l0, l1):
+        li = layer - l0
+        for ch in range(n_ch):
+            pool = k_pool if ch == 0 else v_pool
+            rows = bf16_to_f64(np.stack([pool[layer, s, :] for s in slots]))
+            for c0, w, g in channel_groups(layout, ch):
+                u = factor_f64(patch_u[li][g])
+                vt = factor_f64(vt_of_group(layout, patch_vt[li], m, g))
+                rows[:, c0:c0 + w] = rows[:, c0:c0 + w] + sign * (u @ vt)
+            bits = f64_to_bf16(rows)
+            for t, s in enumerate(slots):
+                pool[layer, s, :] = bits[t]
+
+
 # ----------------------------------------------------------------------------------------
 # compile side, for the pins only (App. A ``form_patch``)
 # ----------------------------------------------------------------------------------------

@@ -8,6 +8,8 @@ from ._binding import (  # noqa: F401
     ITEM_BYTES, KAMERA_DEVICE_BAD_ITEM, KAMERA_DEVICE_SLOT_OOB, KAMERA_ERR_CUDA,
     KAMERA_ERR_INVALID_ARG, KAMERA_ERR_UNSUPPORTED, KAMERA_GQA, KAMERA_MLA, KAMERA_OK,
     KAMERA_ROPE_INTERLEAVED, KAMERA_ROPE_NEOX_HALF, LIB_PATH, Handle, KameraError, Pool,
-    create, kamera_batch_reuse, kamera_batch_reuse_timed, kamera_relocate, kamera_reuse, kamera_rope_phases, lib, make_item, make_layout,
+    create, kamera_batch_patch_inplace, kamera_batch_reuse, kamera_batch_reuse_timed,
+    kamera_patch_inplace, kamera_relocate,
+    kamera_reuse, kamera_rope_phases, lib, make_item, make_layout,
     pack_items, status_string,
 )

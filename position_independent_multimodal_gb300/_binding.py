@@ -83,8 +83,13 @@ def lib() -> ctypes.CDLL:
         L.kamera_batch_reuse_timed.argtypes = [vp, vp, i32, i32, i32,
                                                ctypes.POINTER(kamera_pool), vp, vp,
                                                ctypes.POINTER(vp)]
+        L.kamera_patch_inplace.argtypes = [vp, ctypes.POINTER(kamera_pool), i32, i32, i32, vp,
+                                           vp, i32, i32, i32, i32, vp, vp]
+        L.kamera_batch_patch_inplace.argtypes = [vp, vp, i32, i32, i32,
+                                                 ctypes.POINTER(kamera_pool), i32, vp, vp]
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
-                  "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed"):
+                  "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed",
+                  "kamera_patch_inplace", "kamera_batch_patch_inplace"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -192,6 +197,27 @@ def kamera_batch_reuse(handle: Handle, d_items: torch.Tensor, num_items: int, ma
     _check(lib().kamera_batch_reuse(handle.ptr, _ptr(d_items), int(num_items), int(max_tokens),
                                     int(max_patch_m), ctypes.byref(p), _ptr(status),
                                     _stream(stream)), "kamera_batch_reuse")
+
+
+def kamera_patch_inplace(handle: Handle, pool: Pool, req: int, start_tok: int, num_tokens: int,
+                         patch_u: torch.Tensor, patch_vt: torch.Tensor, patch_m: int,
+                         patch_l0: int, patch_l1: int, sign: int, status: torch.Tensor,
+                         stream=None) -> None:
+    p = pool.c()
+    _check(lib().kamera_patch_inplace(handle.ptr, ctypes.byref(p), int(req), int(start_tok),
+                                      int(num_tokens), _ptr(patch_u), _ptr(patch_vt),
+                                      int(patch_m), int(patch_l0), int(patch_l1), int(sign),
+                                      _ptr(status), _stream(stream)), "kamera_patch_inplace")
+
+
+def kamera_batch_patch_inplace(handle: Handle, d_items: torch.Tensor, num_items: int,
+                               max_tokens: int, max_patch_m: int, pool: Pool, sign: int,
+                               status: torch.Tensor, stream=None) -> None:
+    p = pool.c()
+    _check(lib().kamera_batch_patch_inplace(handle.ptr, _ptr(d_items), int(num_items),
+                                            int(max_tokens), int(max_patch_m), ctypes.byref(p),
+                                            int(sign), _ptr(status), _stream(stream)),
+           "kamera_batch_patch_inplace")
 
 
 def kamera_rope_phases(handle: Handle, d_deltas: torch.Tensor, d_out: torch.Tensor,

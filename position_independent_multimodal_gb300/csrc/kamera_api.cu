@@ -327,6 +327,80 @@ kamera_status kamera_batch_reuse_timed(const kamera_handle *h, const kamera_item
                      events);
 }
 
+kamera_status kamera_patch_inplace(const kamera_handle *h, const kamera_pool *pool, int32_t req,
+                                   int32_t start_tok, int32_t num_tokens, const void *patch_u,
+                                   const void *patch_vt, int32_t patch_m, int32_t patch_l0,
+                                   int32_t patch_l1, int32_t sign, uint32_t *d_status,
+                                   kamera_stream_t stream) {
+  if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
+  kamera::ReuseArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  if (sign != 1 && sign != -1) return KAMERA_ERR_INVALID_ARG;
+  kamera_item it;
+  std::memset(&it, 0, sizeof(it));
+  it.patch_u = patch_u;
+  it.patch_vt = patch_vt;
+  it.num_tokens = num_tokens;
+  it.req = req;
+  it.start_tok = start_tok;
+  it.patch_m = patch_m;
+  it.patch_l0 = patch_l0;
+  it.patch_l1 = patch_l1;
+  const int chk = kamera::inplace_item_check(it, h->lay, a.pool, 1 << 30, kamera::kMaxRank);
+  if (chk != 0) return static_cast<kamera_status>(chk);
+  if (patch_m == 0 || patch_l0 == patch_l1 || num_tokens == 0) return KAMERA_OK;
+  if (!kamera::inplace_layout(h->lay)) return KAMERA_ERR_UNSUPPORTED;
+  a.single = it;
+  a.items = nullptr;
+  a.n_items = 1;
+  a.max_tokens = num_tokens;
+  a.max_m = patch_m;
+  a.engine = kamera::kEngineTensor;
+  a.smem = kamera::reuse_tile_plan(h->lay, patch_m);
+  a.inplace = 1;
+  a.sign = sign;
+  a.status = d_status;
+  a.freq = h->freq;
+  return from_cuda(kamera::launch_reuse_tile(a, 1, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kamera_status kamera_batch_patch_inplace(const kamera_handle *h, const kamera_item *d_items,
+                                         int32_t num_items, int32_t max_tokens,
+                                         int32_t max_patch_m, const kamera_pool *pool,
+                                         int32_t sign, uint32_t *d_status,
+                                         kamera_stream_t stream) {
+  if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
+  if (num_items < 0 || max_tokens < 0 || max_patch_m < 0) return KAMERA_ERR_INVALID_ARG;
+  if (max_patch_m > kamera::kMaxRank) return KAMERA_ERR_UNSUPPORTED;
+  if (sign != 1 && sign != -1) return KAMERA_ERR_INVALID_ARG;
+  kamera::ReuseArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  if (num_items == 0 || max_tokens == 0 || max_patch_m == 0) return KAMERA_OK;
+  if (!d_items || (reinterpret_cast<uintptr_t>(d_items) & 7u)) return KAMERA_ERR_INVALID_ARG;
+  if (num_items > 65535) return KAMERA_ERR_UNSUPPORTED;
+  if (!kamera::inplace_layout(h->lay)) return KAMERA_ERR_UNSUPPORTED;
+  if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
+    return KAMERA_ERR_UNSUPPORTED;
+  a.items = d_items;
+  a.n_items = num_items;
+  a.max_tokens = max_tokens;
+  a.max_m = max_patch_m;
+  a.engine = kamera::kEngineTensor;
+  a.smem = kamera::reuse_tile_plan(h->lay, max_patch_m);
+  a.inplace = 1;
+  a.sign = sign;
+  a.status = d_status;
+  a.freq = h->freq;
+  return from_cuda(
+      kamera::launch_reuse_tile(a, num_items, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,
                                  int32_t num_deltas, float *d_out, kamera_stream_t stream) {
   if (!h || num_deltas < 0) return KAMERA_ERR_INVALID_ARG;

@@ -112,6 +112,8 @@ struct ReuseArgs {
   int max_tokens;
   int max_m;
   int engine;                // kEngineTensor or kEngineFma for patched tiles
+  int inplace;               // 1: patch re-add on cached rows (read from and written to the pool)
+  int sign;                  // inplace: +1 adds U V_m^T, -1 subtracts it
   SmemPlan smem;
   unsigned *status;
   FreqQ64 freq;
@@ -157,6 +159,27 @@ __host__ __device__ inline int item_check(const kamera_item &it, const DevLayout
         return KAMERA_ERR_INVALID_ARG;
     }
   }
+  return 0;
+}
+
+// The rules of an item of an in-place patch re-add: the canonical pointers and the offset are
+// not read; tokens, request, rank, layers and factors as for reuse.
+__host__ __device__ inline int inplace_item_check(const kamera_item &it, const DevLayout &lay,
+                                                  const DevPool &pool, int max_tokens,
+                                                  int max_m) {
+  if (it.num_tokens < 0 || it.num_tokens > max_tokens) return KAMERA_ERR_INVALID_ARG;
+  if (it.patch_m < 0 || it.patch_m > kMaxRank) return KAMERA_ERR_UNSUPPORTED;
+  if (it.patch_m > max_m) return KAMERA_ERR_INVALID_ARG;
+  if (it.num_tokens == 0 || it.patch_m == 0) return 0;
+  if (it.req < 0 || it.req >= pool.num_reqs || it.start_tok < 0) return KAMERA_ERR_INVALID_ARG;
+  if ((long long)it.start_tok + it.num_tokens > (long long)pool.pt_stride * lay.page_size)
+    return KAMERA_ERR_INVALID_ARG;
+  if (it.patch_l0 < 0 || it.patch_l1 < it.patch_l0 || it.patch_l1 > lay.L)
+    return KAMERA_ERR_INVALID_ARG;
+  if (it.patch_l1 > it.patch_l0 &&
+      (!it.patch_u || !it.patch_vt || !aligned16(it.patch_vt) ||
+       (reinterpret_cast<uintptr_t>(it.patch_u) & 1u)))
+    return KAMERA_ERR_INVALID_ARG;
   return 0;
 }
 
@@ -328,6 +351,7 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
 bool fast_layout(const DevLayout &l);                               // kamera_reuse_tile.cu
+bool inplace_layout(const DevLayout &l);
 SmemPlan reuse_tile_plan(const DevLayout &l, int max_m);
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu

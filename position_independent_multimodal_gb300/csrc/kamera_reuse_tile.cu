@@ -159,7 +159,7 @@ __device__ __noinline__ void epi_fma(uint32_t x, int r, int half, int nc, int ba
   }
 }
 
-template <int NC, int BAND>
+template <int NC, int BAND, bool INPLACE>
 __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsigned char *sp,
                                           const kamera_item &it, int layer, int ch,
                                           const Tile &tile) {
@@ -184,9 +184,11 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
   const int li = layer - it.patch_l0;
   const __nv_bfloat16 *U = static_cast<const __nv_bfloat16 *>(it.patch_u) +
                            (long long)(li * 2 + tile.group) * T * m;
-  const __nv_bfloat16 *canon = static_cast<const __nv_bfloat16 *>(ch == 0 ? it.canon_k
-                                                                           : it.canon_v) +
-                               (long long)layer * T * row + tile.col0;
+  const __nv_bfloat16 *canon = INPLACE ? nullptr
+                                         : static_cast<const __nv_bfloat16 *>(
+                                               ch == 0 ? it.canon_k : it.canon_v) +
+                                               (long long)layer * T * row + tile.col0;
+  const __nv_bfloat16 *pool_ch = ch == 0 ? a.pool.k : a.pool.v;
   auto u_buf = [&](int t) { return s0 + P.a_op + (u2 ? (t & 1) * P.a_stage : 0); };
   const int lc = tid & 7, lr = tid >> 3;  // copies: chunk of an atom row, row of each pass
   const uint32_t swc = (uint32_t)((lc ^ (lr & 7)) << 4);
@@ -197,15 +199,36 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
   // page ids of its tokens
   auto issue_x = [&](int t, int s) {
     const int t0 = t * kTileRows, rows = min(kTileRows, T - t0);
-    const __nv_bfloat16 *src = canon + (long long)(t0 + lr) * row + 8 * lc;
     const uint32_t dst = x_op + s * P.stage + lr * 128 + swc;
-    const long long step = 32ll * row;
+    if constexpr (!INPLACE) {
+      const __nv_bfloat16 *src = canon + (long long)(t0 + lr) * row + 8 * lc;
+      const long long step = 32ll * row;
 #pragma unroll
-    for (int pr = 0; pr < 4; ++pr) {
-      if (lr + 32 * pr < rows) {
+      for (int pr = 0; pr < 4; ++pr) {
+        if (lr + 32 * pr < rows) {
 #pragma unroll
-        for (int at = 0; at < ATOMS; ++at)
-          ptx::cp_async16(dst + at * kAtomT + pr * 32 * 128, src + pr * step + at * 64, 16u);
+          for (int at = 0; at < ATOMS; ++at)
+            ptx::cp_async16(dst + at * kAtomT + pr * 32 * 128, src + pr * step + at * 64, 16u);
+        }
+      }
+    } else {  // the cached rows themselves, gathered through the page table
+      const int32_t *ptab = a.pool.pt + (long long)it.req * a.pool.pt_stride;
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        const int rr = lr + 32 * pr;
+        if (rr < rows) {
+          int pg, in_page;
+          psd.split(it.start_tok + t0 + rr, &pg, &in_page);
+          const int page = __ldg(ptab + pg);
+          if (page >= 0 && (long long)(page + 1) * ps <= a.pool.num_slots) {
+            const __nv_bfloat16 *src =
+                pool_ch + ((long long)layer * a.pool.num_slots + (long long)page * ps + in_page) *
+                              row + tile.col0 + 8 * lc;
+#pragma unroll
+            for (int at = 0; at < ATOMS; ++at)
+              ptx::cp_async16(dst + at * kAtomT + pr * 32 * 128, src + at * 64, 16u);
+          }
+        }
       }
     }
     int p_first, off0, npages, dummy;
@@ -310,6 +333,13 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
   }
   ptx::cp_async_commit();
   ptx::cp_async_wait_group1();  // tile 0 (and V_m^T)
+  if (INPLACE && a.sign < 0)  // subtraction: negate V_m^T exactly (bf16 sign bits)
+    for (int e = tid; e < Kp * NCORE * 4; e += kThrT) {
+      const uint32_t ad = v_op + 4 * e;
+      uint32_t w;
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(ad));
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(ad), "r"(w ^ 0x80008000u) : "memory");
+    }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();  // TMEM address, barriers, identity, table, tile 0 visible
@@ -425,17 +455,41 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_const
   const Tile tile = tile_of(lay, ch, ct, rotate);
   if (tile.ncols == 128) {
     if (tile.band == 0)
-      task_loop<128, 0>(a, s0, sp, it, layer, ch, tile);
+      task_loop<128, 0, false>(a, s0, sp, it, layer, ch, tile);
     else if (tile.band == 128)
-      task_loop<128, 128>(a, s0, sp, it, layer, ch, tile);
+      task_loop<128, 128, false>(a, s0, sp, it, layer, ch, tile);
     else
-      task_loop<128, 64>(a, s0, sp, it, layer, ch, tile);
+      task_loop<128, 64, false>(a, s0, sp, it, layer, ch, tile);
   } else {
     if (tile.band == 0)
-      task_loop<64, 0>(a, s0, sp, it, layer, ch, tile);
+      task_loop<64, 0, false>(a, s0, sp, it, layer, ch, tile);
     else
-      task_loop<64, 64>(a, s0, sp, it, layer, ch, tile);
+      task_loop<64, 64, false>(a, s0, sp, it, layer, ch, tile);
   }
+}
+
+// The patch re-added in place on cached rows: every tile unrotated, rows gathered from and
+// written back to the pool.
+__global__ void __launch_bounds__(kThrT, 2) patch_inplace_kernel(const __grid_constant__ ReuseArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t s0 = (raw + 1023u) & ~1023u;
+  unsigned char *sp = smem_raw + (s0 - raw);
+  const DevLayout &lay = a.lay;
+  const int ct = blockIdx.x, item = blockIdx.y;
+  const int layer = blockIdx.z / lay.n_ch;
+  const int ch = blockIdx.z - layer * lay.n_ch;
+  const kamera_item it = a.items ? a.items[item] : a.single;
+  if (a.items && inplace_item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
+    if (ct == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);
+    return;
+  }
+  if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;
+  const Tile tile = tile_of(lay, ch, ct, false);
+  if (tile.ncols == 128)
+    task_loop<128, 0, true>(a, s0, sp, it, layer, ch, tile);
+  else
+    task_loop<64, 0, true>(a, s0, sp, it, layer, ch, tile);
 }
 
 int align128t(int x) { return (x + 127) & ~127; }
@@ -446,6 +500,14 @@ bool fast_layout(const DevLayout &l) {
   if (l.style != KAMERA_ROPE_NEOX_HALF) return false;
   if (l.tw != 64 && l.tw != 128) return false;
   if (l.kind == KAMERA_GQA) return (l.hd == 64 || l.hd == 128) && l.hd <= l.tw && l.row_k % l.tw == 0;
+  return l.latent % l.tw == 0 && (l.rope_d == 64 || l.rope_d == 128);
+}
+
+// The in-place patch add never rotates, so any pairing and head width will do as long as
+// every column tile is 64 or 128 columns wide.
+bool inplace_layout(const DevLayout &l) {
+  if (l.tw != 64 && l.tw != 128) return false;
+  if (l.kind == KAMERA_GQA) return l.row_k % l.tw == 0;
   return l.latent % l.tw == 0 && (l.rope_d == 64 || l.rope_d == 128);
 }
 
@@ -492,19 +554,20 @@ SmemPlan reuse_tile_plan(const DevLayout &l, int max_m) {
 }
 
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s) {
-  static int configured_smem[64] = {0};
+  static int configured_smem[2][64] = {{0}};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (a.smem.total > configured_smem[dev] && a.smem.total > 48 * 1024) {
-    e = cudaFuncSetAttribute(reuse_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             a.smem.total);
+  const int which = a.inplace ? 1 : 0;
+  void (*kernel)(const ReuseArgs) = which ? patch_inplace_kernel : reuse_tile_kernel;
+  if (a.smem.total > configured_smem[which][dev] && a.smem.total > 48 * 1024) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, a.smem.total);
     if (e != cudaSuccess) return e;
-    configured_smem[dev] = a.smem.total;
+    configured_smem[which][dev] = a.smem.total;
   }
   dim3 grid(a.lay.ntile, n_items, a.lay.L * a.lay.n_ch);
-  reuse_tile_kernel<<<grid, kThrT, a.smem.total, s>>>(a);
+  kernel<<<grid, kThrT, a.smem.total, s>>>(a);
   return cudaGetLastError();
 }
 

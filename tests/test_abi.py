@@ -170,6 +170,54 @@ def test_batch_and_relocate_host_checks(lib):
     km.kamera_relocate(h, fake_pool(), 0, 0, 8, 0, STATUS, stream=0)
 
 
+def test_patch_inplace_host_checks(lib):
+    h = km.create(gqa())
+    u, vt = FakeTensor(0x70000), FakeTensor(0x80000)
+    bad = [
+        dict(req=2), dict(start_tok=-1), dict(num_tokens=-1), dict(start_tok=250),
+        dict(sign=0), dict(sign=2), dict(l0=1, l1=0), dict(l1=3), dict(u=None),
+        dict(vt=FakeTensor(0x80008)), dict(u=FakeTensor(0x70001)),
+    ]
+    for kw in bad:
+        a = dict(req=0, start_tok=0, num_tokens=16, u=u, vt=vt, m=8, l0=0, l1=1, sign=1)
+        a.update(kw)
+        with pytest.raises(km.KameraError) as e:
+            km.kamera_patch_inplace(h, fake_pool(), a["req"], a["start_tok"], a["num_tokens"],
+                                    a["u"], a["vt"], a["m"], a["l0"], a["l1"], a["sign"],
+                                    STATUS, stream=0)
+        assert e.value.status == km.KAMERA_ERR_INVALID_ARG, kw
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_patch_inplace(h, fake_pool(), 0, 0, 16, u, vt, 129, 0, 1, 1, STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+    # nothing to do: returns OK without touching the device
+    for m, l0, l1, T in [(0, 0, 1, 16), (8, 1, 1, 16), (8, 0, 1, 0)]:
+        km.kamera_patch_inplace(h, fake_pool(), 0, 0, T, u, vt, m, l0, l1, -1, STATUS, stream=0)
+    # tiles that are not 64 or 128 columns wide are not served
+    wide = km.create(wl.Layout(kind=wl.GQA, num_layers=2, page_size=16, num_kv_heads=2,
+                               head_dim=256, rope_dim=256, rope_theta=1e4))
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_patch_inplace(wide, fake_pool(), 0, 0, 16, u, vt, 8, 0, 1, 1, STATUS,
+                                stream=0)
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+
+
+def test_batch_patch_inplace_host_checks(lib):
+    h = km.create(gqa())
+    d = FakeTensor(0x90000)
+    for args in [(-1, 16, 8, 1), (1, -1, 8, 1), (1, 16, -1, 1), (1, 16, 8, 0)]:
+        with pytest.raises(km.KameraError):
+            km.kamera_batch_patch_inplace(h, d, args[0], args[1], args[2], fake_pool(), args[3],
+                                          STATUS, stream=0)
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_batch_patch_inplace(h, d, 1, 16, 129, fake_pool(), 1, STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+    with pytest.raises(km.KameraError):
+        km.kamera_batch_patch_inplace(h, FakeTensor(0x90004), 1, 16, 8, fake_pool(), 1, STATUS,
+                                      stream=0)
+    km.kamera_batch_patch_inplace(h, d, 0, 16, 8, fake_pool(), 1, STATUS, stream=0)
+    km.kamera_batch_patch_inplace(h, d, 3, 16, 0, fake_pool(), -1, STATUS, stream=0)
+
+
 def test_status_strings(lib):
     for s in range(4):
         assert km.status_string(s)

@@ -5,6 +5,8 @@ Every slot of both pools is compared: written rows against the oracle (bit-exact
 arithmetic happens, else the tolerance in kamera_testlib), untouched slots against the
 sentinel they were filled with.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -259,3 +261,157 @@ def test_empty_inputs_launch_nothing():
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert torch.all(k.view(torch.int16) == wl.POOL_SENTINEL_BITS)
+
+
+# ------------------------------------------------------------------------------------------
+# reversible switch: patch re-added (and removed) in place on cached rows
+# ------------------------------------------------------------------------------------------
+
+def _inplace_expected(lay, before_k, before_v, pt, it, sign):
+    """Oracle result of one in-place add on a host copy of the pools, plus the float64 values
+    and error scale of the touched rows (for the tolerance)."""
+    k, v = before_k.copy(), None if before_v is None else before_v.copy()
+    u = wl.bf16_bits(it.patch_u)
+    vt = wl.bf16_bits(it.patch_vt)
+    ora.patch_inplace(lay, k, v, pt, it.req, it.start_tok, it.num_tokens, u, vt, it.patch_m,
+                      it.patch_l0, it.patch_l1, sign)
+    slots = tl.slots_of(pt, it.req, it.start_tok, it.num_tokens, lay.page_size)
+    vals, mags = {}, {}
+    for layer in range(it.patch_l0, it.patch_l1):
+        li = layer - it.patch_l0
+        for ch in range(2 if lay.kind == wl.GQA else 1):
+            pool = before_k if ch == 0 else before_v
+            x = ora.bf16_to_f64(pool[layer, slots])
+            y, s = x.copy(), np.abs(x)
+            for c0, w, g in ora.channel_groups(lay, ch):
+                uu = ora.factor_f64(u[li][g])
+                vv = ora.factor_f64(ora.vt_of_group(lay, vt[li], it.patch_m, g))
+                y[:, c0:c0 + w] += sign * (uu @ vv)
+                s[:, c0:c0 + w] += np.abs(uu) @ np.abs(vv)
+            vals[(layer, ch)], mags[(layer, ch)] = y, s
+    return k, v, slots, vals, mags
+
+
+def _check_inplace(lay, it, got_k, got_v, want_k, want_v, slots, vals, mags):
+    m = it.patch_m
+    for (layer, ch), y in vals.items():
+        got = ora.bf16_to_f64((got_k if ch == 0 else got_v)[layer, slots])
+        tol = ora.bf16_ulp(y) + (2 * m + 8) * 2.0 ** -24 * mags[(layer, ch)]
+        assert np.all(np.abs(got - y) <= tol), (layer, ch)
+    # everything else: the bytes the oracle leaves (untouched rows and layers)
+    mask = np.ones(want_k.shape[:2], dtype=bool)
+    for layer in range(it.patch_l0, it.patch_l1):
+        mask[layer, slots] = False
+    np.testing.assert_array_equal(got_k[mask], want_k[mask])
+    if want_v is not None:
+        np.testing.assert_array_equal(got_v[mask], want_v[mask])
+
+
+@pytest.mark.parametrize("kind,m", [("gqa", 8), ("gqa", 12), ("gqa", 32), ("gqai", 16),
+                                    ("mla", 32), ("mla", 24)])
+def test_patch_inplace_add_then_remove(kind, m):
+    lay = {"gqa": gqa_layout(), "gqai": gqa_layout(style=wl.INTERLEAVED),
+           "mla": mla_layout()}[kind]
+    w = ragged(lay, m, f"inplace{kind}{m}")
+    h = km.create(lay)
+    items = tl.to_device_items(w.items)
+    clean = [dataclasses.replace(it, patch_m=0, patch_l0=0, patch_l1=0, patch_u=None,
+                                 patch_vt=None) for it in items]
+    k, v, status, (_, pt_dev) = tl.run_batch(h, lay, clean, w.page_table, w.num_slots)
+    assert status == 0
+    pt = w.page_table.numpy()
+    pool = km.Pool(k, v, pt_dev, w.num_slots)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for it in items:
+        if it.num_tokens < 2:
+            continue
+        for sign in (1, -1):
+            before_k = wl.bf16_bits(k)
+            before_v = None if v is None else wl.bf16_bits(v)
+            km.kamera_patch_inplace(h, pool, it.req, it.start_tok, it.num_tokens, it.patch_u,
+                                    it.patch_vt, it.patch_m, it.patch_l0, it.patch_l1, sign, st)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+            want = _inplace_expected(lay, before_k, before_v, pt, it, sign)
+            _check_inplace(lay, it, wl.bf16_bits(k), None if v is None else wl.bf16_bits(v),
+                           *want)
+
+
+def test_patch_inplace_on_clean_view_matches_reuse_with_patch():
+    # δ = 0: the clean view is an exact copy, so re-adding the patch must give the bytes the
+    # patched reuse writes (both round x + U V_m^T once, on the same kernel path)
+    lay = gqa_layout(L=3, H=2, hd=128)
+    w = wl.reuse_workload("sw0", lay, n_chunks=2, T=[200, 64],
+                          placements=[(0, 0, 0, 0), (1, 1, 16, 0)], m=16, l0=1, l1=3, seed=9,
+                          strong=True, patch_per_item=True)
+    h = km.create(lay)
+    items = tl.to_device_items(w.items)
+    clean = [dataclasses.replace(it, patch_m=0, patch_l0=0, patch_l1=0, patch_u=None,
+                                 patch_vt=None) for it in items]
+    k, v, status, (_, pt_dev) = tl.run_batch(h, lay, clean, w.page_table, w.num_slots)
+    assert status == 0
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pool = km.Pool(k, v, pt_dev, w.num_slots)
+    for it in items:
+        km.kamera_patch_inplace(h, pool, it.req, it.start_tok, it.num_tokens, it.patch_u,
+                                it.patch_vt, it.patch_m, it.patch_l0, it.patch_l1, 1, st)
+    k2, v2, status2, _ = tl.run_batch(h, lay, items, w.page_table, w.num_slots)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and status2 == 0
+    assert torch.equal(k.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v.view(torch.int16), v2.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind", ["gqa", "mla"])
+def test_batch_patch_inplace_matches_oracle_and_single_calls(kind):
+    lay = gqa_layout() if kind == "gqa" else mla_layout()
+    w = ragged(lay, 16, f"binplace{kind}")
+    h = km.create(lay)
+    items = tl.to_device_items(w.items)
+    clean = [dataclasses.replace(it, patch_m=0, patch_l0=0, patch_l1=0, patch_u=None,
+                                 patch_vt=None) for it in items]
+    k, v, status, (_, pt_dev) = tl.run_batch(h, lay, clean, w.page_table, w.num_slots)
+    assert status == 0
+    k1, v1 = k.clone(), None if v is None else v.clone()
+    before_k, before_v = wl.bf16_bits(k), None if v is None else wl.bf16_bits(v)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_items = km.pack_items(items).cuda()
+    km.kamera_batch_patch_inplace(h, d_items, len(items), max(it.num_tokens for it in items), 16,
+                                  km.Pool(k, v, pt_dev, w.num_slots), -1, st)
+    for it in items:  # the same edits one chunk at a time
+        km.kamera_patch_inplace(h, km.Pool(k1, v1, pt_dev, w.num_slots), it.req, it.start_tok,
+                                it.num_tokens, it.patch_u, it.patch_vt, it.patch_m, it.patch_l0,
+                                it.patch_l1, -1, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(k.view(torch.int16), k1.view(torch.int16))
+    if v is not None:
+        assert torch.equal(v.view(torch.int16), v1.view(torch.int16))
+    # against the oracle, item by item (items cover disjoint rows)
+    pt = w.page_table.numpy()
+    want_k, want_v = before_k.copy(), None if before_v is None else before_v.copy()
+    gk, gv = wl.bf16_bits(k), None if v is None else wl.bf16_bits(v)
+    for it in items:
+        res = _inplace_expected(lay, want_k, want_v, pt, it, -1)
+        want_k, want_v = res[0], res[1]
+        for (layer, ch), y in res[3].items():
+            got = ora.bf16_to_f64((gk if ch == 0 else gv)[layer, res[2]])
+            tol = ora.bf16_ulp(y) + (2 * 16 + 8) * 2.0 ** -24 * res[4][(layer, ch)]
+            assert np.all(np.abs(got - y) <= tol)
+
+
+def test_batch_patch_inplace_rejects_a_bad_item_on_device():
+    lay = gqa_layout()
+    w = ragged(lay, 8, "binplacebad")
+    h = km.create(lay)
+    items = tl.to_device_items(w.items)
+    k, v, status, (_, pt_dev) = tl.run_batch(h, lay, items, w.page_table, w.num_slots)
+    assert status == 0
+    before = k.clone()
+    bad = [dataclasses.replace(items[2], req=99)]  # a request outside the page table
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    km.kamera_batch_patch_inplace(h, km.pack_items(bad).cuda(), 1, 512, 8,
+                                  km.Pool(k, v, pt_dev, w.num_slots), 1, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == km.KAMERA_DEVICE_BAD_ITEM
+    assert torch.equal(k.view(torch.int16), before.view(torch.int16))

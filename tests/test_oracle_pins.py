@@ -435,6 +435,89 @@ def test_relocate_in_place_rotates_only_rope_columns():
 
 
 # ------------------------------------------------------------------------------------------
+# reversible switch: the patch re-added in place (App. E)
+# ------------------------------------------------------------------------------------------
+
+def switch_setup(kind="gqa", delta=0, m=3):
+    """A chunk written clean (rank 0) into a pool, and the patch of its layers 1..2."""
+    if kind == "gqa":
+        lay, it = gqa_item(L=3, T=7, H=2, hd=8, m=m, l0=1, l1=3, delta=delta)
+        W0 = W1 = 16
+        rk, rv = 16, 16
+    else:
+        lay, it = mla_item(L=3, T=7, latent=16, rope=8, m=m, l0=1, l1=3, delta=delta)
+        W0, W1 = 16, 8
+        rk, rv = 24, 0
+    lay.page_size = 4
+    pt = np.array([[5, 2, 7], [0, 3, 1]], np.int32)
+    k_pool = np.full((3, 32, rk), 0x5A5A, np.uint16)
+    v_pool = np.full((3, 32, rv), 0x5A5A, np.uint16) if rv else None
+    clean = ora.as_item(**{**vars(it), "patch_m": 0, "patch_l0": 0, "patch_l1": 0,
+                           "req": 0, "start_tok": 2})
+    ora.apply_reuse(lay, clean, k_pool, v_pool, pt)
+    patched = ora.as_item(**{**vars(clean), "patch_m": m, "patch_l0": 1, "patch_l1": 3})
+    return lay, it, pt, k_pool, v_pool, clean, patched
+
+
+@pytest.mark.parametrize("kind", ["gqa", "mla"])
+def test_patch_readd_on_clean_view_equals_reuse_with_patch(kind):
+    # App. E: the clean view is the stored canonical (an exact copy at δ = 0); re-adding the
+    # rank-m patch on it gives exactly the patched reuse, one rounding each
+    lay, it, pt, k_pool, v_pool, clean, patched = switch_setup(kind, delta=0)
+    ora.patch_inplace(lay, k_pool, v_pool, pt, 0, 2, 7, it.patch_u, it.patch_vt, it.patch_m,
+                      1, 3)
+    want_k = np.full_like(k_pool, 0x5A5A)
+    want_v = None if v_pool is None else np.full_like(v_pool, 0x5A5A)
+    ora.apply_reuse(lay, patched, want_k, want_v, pt)
+    np.testing.assert_array_equal(k_pool, want_k)
+    if v_pool is not None:
+        np.testing.assert_array_equal(v_pool, want_v)
+
+
+def test_patch_inplace_sign_symmetry_and_pure_python_sums():
+    lay, it, pt, k_pool, v_pool, clean, patched = switch_setup("gqa", delta=777, m=2)
+    before_k, before_v = k_pool.copy(), v_pool.copy()
+    a_k, a_v = k_pool.copy(), v_pool.copy()
+    b_k, b_v = k_pool.copy(), v_pool.copy()
+    neg_u = it.patch_u ^ np.uint16(0x8000)  # exact negation of every bf16 factor
+    ora.patch_inplace(lay, a_k, a_v, pt, 0, 2, 7, it.patch_u, it.patch_vt, 2, 1, 3, sign=-1)
+    ora.patch_inplace(lay, b_k, b_v, pt, 0, 2, 7, neg_u, it.patch_vt, 2, 1, 3, sign=+1)
+    np.testing.assert_array_equal(a_k, b_k)
+    np.testing.assert_array_equal(a_v, b_v)
+    # element by element: x - Σ_j U_tj Vt_jc, rounded once; untouched rows and layers stay
+    W = 16
+    for layer in range(3):
+        for ch, (pool, before) in enumerate(((a_k, before_k), (a_v, before_v))):
+            for t in range(7):
+                s = ora.slot_of(pt, 0, 2 + t, 4)
+                for c in range(W):
+                    x = float(ora.bf16_to_f64(before[layer, s, c]))
+                    if 1 <= layer < 3:
+                        li = layer - 1
+                        for j in range(2):
+                            x -= (float(ora.bf16_to_f64(it.patch_u[li, ch, t, j])) *
+                                  float(ora.bf16_to_f64(it.patch_vt[li, ch * 2 * W + j * W + c])))
+                    assert pool[layer, s, c] == ora.f64_to_bf16(np.array([x]))[0]
+    touched = {ora.slot_of(pt, 0, 2 + t, 4) for t in range(7)}
+    for s in set(range(32)) - touched:
+        np.testing.assert_array_equal(a_k[:, s], before_k[:, s])
+
+
+def test_patch_add_then_remove_is_within_two_roundings():
+    # the inverse of a re-add is the subtraction of the same patch, exact up to rounding
+    lay, it, pt, k_pool, v_pool, clean, patched = switch_setup("gqa", delta=-31, m=3)
+    before = ora.bf16_to_f64(k_pool).copy()
+    ora.patch_inplace(lay, k_pool, v_pool, pt, 0, 2, 7, it.patch_u, it.patch_vt, 3, 1, 3)
+    mid = ora.bf16_to_f64(k_pool).copy()
+    ora.patch_inplace(lay, k_pool, v_pool, pt, 0, 2, 7, it.patch_u, it.patch_vt, 3, 1, 3,
+                      sign=-1)
+    after = ora.bf16_to_f64(k_pool)
+    bound = 0.5 * ora.bf16_ulp(mid) + 0.5 * ora.bf16_ulp(after)
+    assert np.all(np.abs(after - before) <= bound * (1 + 1e-9))
+    assert not np.array_equal(mid[1:], before[1:])
+
+
+# ------------------------------------------------------------------------------------------
 # shapes and sizes printed on the pages
 # ------------------------------------------------------------------------------------------
 
