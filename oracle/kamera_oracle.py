@@ -334,6 +334,51 @@ def form_patch(kv_cond, kv_solo_relocated, m: int):
     return u[:, :m] * s[:m], vt[:m]
 
 
+def _sign_rows(us, vt):
+    """Fix the SVD sign freedom: the entry of largest magnitude in each row of Vt is made
+    positive (the matching column of U·Σ flips with it)."""
+    if vt.shape[0] == 0:
+        return us, vt
+    idx = np.argmax(np.abs(vt), axis=1)
+    sgn = np.where(vt[np.arange(vt.shape[0]), idx] < 0, -1.0, 1.0)
+    return us * sgn[None, :], vt * sgn[:, None]
+
+
+def form_patch_svd(delta, m: int):
+    """``form_patch`` on a given deficit Δ with the sign convention of ``_sign_rows``:
+    (U·Σ [T×m], Vt [m×W], σ [m]) from the full SVD (numpy.linalg.svd, float64)."""
+    u, s, vt = np.linalg.svd(np.asarray(delta, np.float64), full_matrices=False)
+    us, vt = _sign_rows(u[:, :m] * s[:m], vt[:m])
+    return us, vt, s[:m]
+
+
+def form_patch_randomized(delta, omega, m: int, q: int):
+    """Top-m patch of a deficit Δ [T×W] by the randomized range finder with q power
+    iterations (Halko, Martinsson & Tropp, SIAM Review 2011, Alg. 4.4), then the SVD of the
+    small projection B = QᵀΔ (their Alg. 5.1), in float64. ``omega`` [W×k] is the random
+    test matrix (k ≥ m columns), drawn by the caller. Steps:
+      Y = Δ Ω; Q = orth(Y); q times: Z = orth(ΔᵀQ), Q = orth(Δ Z);
+      Bᵀ = ΔᵀQ; B Bᵀ = Ũ Λ Ũᵀ (eigenvalues descending); σ = √Λ;
+      U·Σ = Q Ũ_m Σ_m, V_mᵀ = Σ_m⁻¹ Ũ_mᵀ B; signs as in ``_sign_rows``.
+    Columns of σ = 0 give zero factors. Returns (U·Σ, Vt, σ)."""
+    a = np.asarray(delta, np.float64)
+    om = np.asarray(omega, np.float64)
+    q_, _ = np.linalg.qr(a @ om)
+    for _ in range(q):
+        z, _ = np.linalg.qr(a.T @ q_)
+        q_, _ = np.linalg.qr(a @ z)
+    bt = a.T @ q_
+    lam, ut = np.linalg.eigh(bt.T @ bt)
+    order = np.argsort(lam)[::-1]
+    lam, ut = lam[order], ut[:, order]
+    sig = np.sqrt(np.maximum(lam[:m], 0.0))
+    us = (q_ @ ut[:, :m]) * sig[None, :]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        vt = np.where(sig[:, None] > 0, (bt @ ut[:, :m]).T / sig[:, None], 0.0)
+    us, vt = _sign_rows(us, vt)
+    return us, vt, sig
+
+
 def patch_byte_fraction(T: int, W: int, m: int) -> float:
     """Bytes of a rank-m patch (U [T×m] and Vt [m×W]) over the bytes of the [T×W] page it
     patches, same element type on both sides: m·(T + W) / (T·W)."""

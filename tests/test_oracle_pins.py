@@ -518,6 +518,49 @@ def test_patch_add_then_remove_is_within_two_roundings():
 
 
 # ------------------------------------------------------------------------------------------
+# patch forming from a given deficit (App. A form_patch; randomized range finder)
+# ------------------------------------------------------------------------------------------
+
+def test_randomized_patch_recovers_an_exactly_low_rank_deficit():
+    # a deficit of rank r <= k lies in the sketch's range: the randomized factors equal the
+    # truncated SVD's (Eckart–Young), whatever the test matrix
+    rng = np.random.default_rng(11)
+    T, W, r, m, k = 60, 40, 6, 4, 10
+    delta = rng.standard_normal((T, r)) @ np.diag([9, 7, 5, 3, 2, 1.0]) @ rng.standard_normal((r, W))
+    for q in (0, 1):
+        us, vt, sig = ora.form_patch_randomized(delta, rng.standard_normal((W, k)), m, q)
+        us0, vt0, sig0 = ora.form_patch_svd(delta, m)
+        np.testing.assert_allclose(sig, sig0, rtol=1e-10)
+        np.testing.assert_allclose(us, us0, atol=1e-9)
+        np.testing.assert_allclose(vt, vt0, atol=1e-9)
+        np.testing.assert_allclose(vt @ vt.T, np.eye(m), atol=1e-10)
+
+
+def test_randomized_patch_residual_near_the_eckart_young_optimum():
+    # a decaying spectrum: with power iterations the residual approaches sqrt(sum_{i>m} s_i^2)
+    rng = np.random.default_rng(12)
+    T, W, m, k = 120, 80, 8, 16
+    u, _ = np.linalg.qr(rng.standard_normal((T, W)))
+    v, _ = np.linalg.qr(rng.standard_normal((W, W)))
+    s = 0.8 ** np.arange(W)
+    delta = (u * s) @ v.T
+    best = np.sqrt(np.sum(s[m:] ** 2))
+    prev = np.inf
+    for q in (0, 1, 2):
+        us, vt, sig = ora.form_patch_randomized(delta, rng.standard_normal((W, k)), m, q)
+        res = np.linalg.norm(delta - us @ vt)
+        assert best - 1e-12 <= res <= 1.01 * best if q >= 1 else res <= 1.5 * best
+        assert res <= prev * (1 + 1e-9)
+        prev = res
+    np.testing.assert_allclose(sig, s[:m], rtol=1e-3)
+
+
+def test_randomized_patch_zero_deficit_gives_zero_factors():
+    us, vt, sig = ora.form_patch_randomized(np.zeros((10, 6)), np.ones((6, 4)), 3, 1)
+    assert np.all(us == 0) and np.all(vt == 0) and np.all(sig == 0)
+
+
+# ------------------------------------------------------------------------------------------
 # shapes and sizes printed on the pages
 # ------------------------------------------------------------------------------------------
 
