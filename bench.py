@@ -493,8 +493,9 @@ def time_calls(fn, steps, warmup=1):
 
 
 def other_workloads(dev):
-    """Brief timings of the MLA recall, sliding-window survival and recall-sweep workloads
-    (each a parity-tested configuration of its own); reported beside the main line."""
+    """Brief timings of the in-place switch, MLA recall, sliding-window survival, recall-sweep
+    and patch-forming workloads (each a parity-tested configuration of its own); reported
+    beside the main line."""
     import torch
     import position_independent_multimodal_gb300 as km
     import workloads as wl
@@ -599,6 +600,35 @@ def other_workloads(dev):
         "ms_per_step": ms, "gb_s_written": written / ms / 1e6,
         "frac_hbm_peak": alg / ms / 1e6 / peak, "chunks_per_s": 1024 / ms * 1e3}
     del w, launches
+    torch.cuda.empty_cache()
+
+    # patch forming: the 84 deficits of the reorder workload's patched layers (3 chunks x 14
+    # layers x K and V), T = 1024 tokens x W = 512, top m = 32 from a k = 40 sketch with one
+    # power iteration, written into the patch store layout
+    n, T, W, k, q, m = 84, 1024, 512, 40, 1, 32
+    delta, omega = wl.deficit_problems(n, T, W, k=k, rank=64, decay=0.9, noise=1e-2, seed=0,
+                                       device=dev)
+    u = torch.empty(n, T, m, dtype=torch.bfloat16, device=dev)
+    vt = torch.empty(n, m, W, dtype=torch.bfloat16, device=dev)
+    sig = torch.empty(n, m, dtype=torch.float32, device=dev)
+    ws = torch.empty(km.kamera_form_patch_workspace(n, T, W, k), dtype=torch.uint8, device=dev)
+
+    def form():
+        km.kamera_form_patch(delta, omega, k, q, m, u, vt, sig, ws, num_problems=n, T=T, W=W,
+                             ld=W, delta_stride=T * W, omega_stride=0, u_stride=T * m,
+                             vt_stride=m * W)
+    ms = time_calls(form, 5, warmup=2)
+    # algorithmic float32 flops: the (2 + 2q) products with Δ, 12·M·k² per CholeskyQR3 on M
+    # rows, and U·Σ = Q·Ũ_m (the Jacobi sweeps are not counted)
+    flops = n * ((2 + 2 * q) * 2 * T * W * k + 12 * k * k * ((1 + q) * T + q * W) +
+                 2 * T * k * m)
+    out["form_patch_84_deficits"] = {
+        "workload": "patch forming: 84 float32 deficits 1024 x 512 (the reorder workload's "
+                    "patched layers), top 32 of a 40-column sketch, 1 power iteration",
+        "ms_per_call": ms, "deficits_per_s": n / ms * 1e3,
+        "gflop_s": flops / ms / 1e6,
+        "delta_gb_s": (2 + 2 * q) * n * T * W * 4 / ms / 1e6}
+    del delta, omega, u, vt, sig, ws
     torch.cuda.empty_cache()
     return out
 

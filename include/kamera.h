@@ -31,6 +31,7 @@
 #ifndef KAMERA_H
 #define KAMERA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -236,6 +237,44 @@ kamera_status kamera_batch_patch_inplace(const kamera_handle *handle, const kame
  */
 kamera_status kamera_rope_phases(const kamera_handle *handle, const int64_t *d_deltas,
                                  int32_t num_deltas, float *d_out, kamera_stream_t stream);
+
+/*
+ * Patch forming (§3 "Forming and applying the patch"; App. A "form_patch"): for each of
+ * num_problems deficits Delta = KV(B|A) - R(delta)KV(B|empty), one (layer, group) each, the
+ * top-m factors U*Sigma [T x m] and V_m^T [m x W] in the patch store's bf16 format. The
+ * factors come from the randomized range finder with q power iterations and the SVD of the
+ * small projection (Halko, Martinsson & Tropp, SIAM Review 2011, Alg. 4.4 and 5.1):
+ *   Y = Delta Omega; Q = orth(Y); q times: Z = orth(Delta^T Q), Q = orth(Delta Z);
+ *   B^T = Delta^T Q = V_B Sigma Ut^T; U*Sigma = Q Ut_m Sigma_m; V_m^T = (B^T Ut_m)^T / Sigma_m,
+ * sigma descending, each row of V_m^T signed so that its largest-magnitude entry (the first on
+ * a tie) is positive, the matching column of U*Sigma flipped with it. float32 arithmetic.
+ *   d_delta     : float32; problem i is the [T][W] matrix at d_delta + i*delta_stride with row
+ *                 stride ld >= W (elements).
+ *   d_omega     : float32 [W][k] random test matrix of problem i at d_omega + i*omega_stride
+ *                 (omega_stride 0: one matrix for all problems), drawn by the caller.
+ *   k           : sketch width, m <= k <= min(T, W, 96), with
+ *                 4 * (2112 + 3072 + 3k^2 + kW + 3k) <= 232448 (shared memory of the kernel).
+ *   q           : power iterations, 0..16.   m : rank kept, 1..k.
+ *   d_u, d_vt   : bf16 outputs, problem i's U*Sigma [T][m] at d_u + i*u_stride and V_m^T
+ *                 [m][W] at d_vt + i*vt_stride (elements). The strides place the results
+ *                 straight into a kamera_item's patch_u / patch_vt: for group g of layers
+ *                 l0..l1, u at patch_u + g*T*m with u_stride 2*T*m, vt at patch_vt + g*m*W0 with
+ *                 vt_stride m*(W0 + W1). Outputs of different problems must not overlap.
+ *   d_sigma     : float32 [num_problems][m] singular values, or NULL.
+ *   d_workspace : device scratch of at least kamera_form_patch_workspace(num_problems, T, W, k)
+ *                 bytes, 4-byte aligned; contents on entry are ignored and left undefined.
+ * Columns past the numerical rank of Delta come out with sigma near zero (zero factors for an
+ * exactly zero deficit). Host checks return INVALID_ARG (bad pointer, size, stride, too small
+ * a workspace) or UNSUPPORTED (k or the shared memory above the limits) and launch nothing.
+ */
+size_t kamera_form_patch_workspace(int32_t num_problems, int32_t T, int32_t W, int32_t k);
+
+kamera_status kamera_form_patch(const float *d_delta, int64_t ld, int64_t delta_stride,
+                                int32_t num_problems, int32_t T, int32_t W, const float *d_omega,
+                                int64_t omega_stride, int32_t k, int32_t q, int32_t m, void *d_u,
+                                int64_t u_stride, void *d_vt, int64_t vt_stride, float *d_sigma,
+                                void *d_workspace, size_t workspace_bytes,
+                                kamera_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -9,7 +9,7 @@ from ._binding import (  # noqa: F401
     KAMERA_ERR_INVALID_ARG, KAMERA_ERR_UNSUPPORTED, KAMERA_GQA, KAMERA_MLA, KAMERA_OK,
     KAMERA_ROPE_INTERLEAVED, KAMERA_ROPE_NEOX_HALF, LIB_PATH, Handle, KameraError, Pool,
     create, kamera_batch_patch_inplace, kamera_batch_reuse, kamera_batch_reuse_timed,
-    kamera_patch_inplace, kamera_relocate,
+    kamera_form_patch, kamera_form_patch_workspace, kamera_patch_inplace, kamera_relocate,
     kamera_reuse, kamera_rope_phases, lib, make_item, make_layout,
     pack_items, status_string,
 )

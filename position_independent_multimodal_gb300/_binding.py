@@ -87,9 +87,13 @@ def lib() -> ctypes.CDLL:
                                            vp, i32, i32, i32, i32, vp, vp]
         L.kamera_batch_patch_inplace.argtypes = [vp, vp, i32, i32, i32,
                                                  ctypes.POINTER(kamera_pool), i32, vp, vp]
+        L.kamera_form_patch_workspace.argtypes = [i32, i32, i32, i32]
+        L.kamera_form_patch_workspace.restype = ctypes.c_size_t
+        L.kamera_form_patch.argtypes = [vp, i64, i64, i32, i32, i32, vp, i64, i32, i32, i32, vp,
+                                        i64, vp, i64, vp, vp, ctypes.c_size_t, vp]
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
                   "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed",
-                  "kamera_patch_inplace", "kamera_batch_patch_inplace"):
+                  "kamera_patch_inplace", "kamera_batch_patch_inplace", "kamera_form_patch"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -238,3 +242,25 @@ def kamera_batch_reuse_timed(handle: Handle, d_items: torch.Tensor, num_items: i
                                           int(max_tokens), int(max_patch_m), ctypes.byref(p),
                                           _ptr(status), _stream(stream), arr),
            "kamera_batch_reuse_timed")
+
+
+def kamera_form_patch_workspace(num_problems: int, T: int, W: int, k: int) -> int:
+    """Bytes of device workspace ``kamera_form_patch`` needs."""
+    return int(lib().kamera_form_patch_workspace(int(num_problems), int(T), int(W), int(k)))
+
+
+def kamera_form_patch(delta: torch.Tensor, omega: torch.Tensor, k: int, q: int, m: int,
+                      u: torch.Tensor, vt: torch.Tensor, sigma: Optional[torch.Tensor],
+                      workspace: Optional[torch.Tensor], *, num_problems: int, T: int, W: int,
+                      ld: int, delta_stride: int, omega_stride: int, u_stride: int,
+                      vt_stride: int, stream=None) -> None:
+    """Top-m factors of ``num_problems`` float32 deficits into bf16 ``u`` / ``vt`` (strides in
+    elements, as in the C call); ``workspace`` is a device buffer of at least
+    ``kamera_form_patch_workspace`` bytes."""
+    _check(lib().kamera_form_patch(_ptr(delta), int(ld), int(delta_stride), int(num_problems),
+                                   int(T), int(W), _ptr(omega), int(omega_stride), int(k),
+                                   int(q), int(m), _ptr(u), int(u_stride), _ptr(vt),
+                                   int(vt_stride), _ptr(sigma), _ptr(workspace),
+                                   0 if workspace is None else
+                                   int(workspace.numel() * workspace.element_size()),
+                                   _stream(stream)), "kamera_form_patch")

@@ -414,4 +414,52 @@ kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t kamera_form_patch_workspace(int32_t num_problems, int32_t T, int32_t W, int32_t k) {
+  if (num_problems < 0 || T < 0 || W < 0 || k < 0) return 0;
+  return kamera::form_patch_workspace(num_problems, T, W, k);
+}
+
+kamera_status kamera_form_patch(const float *d_delta, int64_t ld, int64_t delta_stride,
+                                int32_t num_problems, int32_t T, int32_t W, const float *d_omega,
+                                int64_t omega_stride, int32_t k, int32_t q, int32_t m, void *d_u,
+                                int64_t u_stride, void *d_vt, int64_t vt_stride, float *d_sigma,
+                                void *d_workspace, size_t workspace_bytes,
+                                kamera_stream_t stream) {
+  if (num_problems < 0 || T < 1 || W < 1) return KAMERA_ERR_INVALID_ARG;
+  if (k < 1 || m < 1 || m > k || q < 0) return KAMERA_ERR_INVALID_ARG;
+  if (k > kamera::kMaxSketch || k > T || k > W || q > 16) return KAMERA_ERR_UNSUPPORTED;
+  if (kamera::form_patch_smem(W, k) > (size_t)kamera::kMaxFormSmem) return KAMERA_ERR_UNSUPPORTED;
+  if (ld < W || delta_stride < 0 || omega_stride < 0 || u_stride < 0 || vt_stride < 0)
+    return KAMERA_ERR_INVALID_ARG;
+  if (num_problems > 1 && (u_stride < (int64_t)T * m || vt_stride < (int64_t)m * W))
+    return KAMERA_ERR_INVALID_ARG;
+  if (num_problems == 0) return KAMERA_OK;
+  auto mis = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (!d_delta || !d_omega || !d_u || !d_vt || !d_workspace) return KAMERA_ERR_INVALID_ARG;
+  if (mis(d_delta, 4) || mis(d_omega, 4) || mis(d_u, 2) || mis(d_vt, 2) ||
+      mis(d_workspace, 4) || (d_sigma && mis(d_sigma, 4)))
+    return KAMERA_ERR_INVALID_ARG;
+  if (workspace_bytes < kamera::form_patch_workspace(num_problems, T, W, k))
+    return KAMERA_ERR_INVALID_ARG;
+  kamera::FormArgs a;
+  a.delta = d_delta;
+  a.ld = ld;
+  a.delta_stride = delta_stride;
+  a.omega = d_omega;
+  a.omega_stride = omega_stride;
+  a.n = num_problems;
+  a.T = T;
+  a.W = W;
+  a.k = k;
+  a.q = q;
+  a.m = m;
+  a.u = static_cast<__nv_bfloat16 *>(d_u);
+  a.u_stride = u_stride;
+  a.vt = static_cast<__nv_bfloat16 *>(d_vt);
+  a.vt_stride = vt_stride;
+  a.sigma = d_sigma;
+  a.work = static_cast<float *>(d_workspace);
+  return from_cuda(kamera::launch_form_patch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

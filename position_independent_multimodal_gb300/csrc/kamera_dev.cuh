@@ -347,7 +347,28 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
   }
 }
 
+// Patch forming (kamera_form.cu): one problem is a float32 deficit [T x W].
+constexpr int kMaxSketch = 96;            // sketch width k
+constexpr int kMaxFormSmem = 232448;      // shared memory per block (opt-in limit of sm_103a)
+
+struct FormArgs {
+  const float *delta;       // problem i at delta + i*delta_stride, row stride ld
+  long long ld, delta_stride;
+  const float *omega;       // [W x k] row-major, problem i at omega + i*omega_stride
+  long long omega_stride;
+  int n, T, W, k, q, m;
+  __nv_bfloat16 *u;         // U*Sigma [T x m] at u + i*u_stride
+  long long u_stride;
+  __nv_bfloat16 *vt;        // V_m^T [m x W] at vt + i*vt_stride
+  long long vt_stride;
+  float *sigma;             // [n][m] or null
+  float *work;              // 2 * max(T, W) * k floats per problem
+};
+
 // Kernel launchers.
+size_t form_patch_workspace(long long n, int T, int W, int k);  // kamera_form.cu
+size_t form_patch_smem(int W, int k);
+cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s);
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
 bool fast_layout(const DevLayout &l);                               // kamera_reuse_tile.cu

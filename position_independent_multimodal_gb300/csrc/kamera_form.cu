@@ -1,0 +1,412 @@
+// Patch forming on the device: the top-m factors of a conditioning deficit, written in the
+// patch store's format (Kamera, App. A "form_patch": Δ = KV(B|A) − R(δ)KV(B|∅), keep
+// U[:, :m]·S[:m] and Vt[:m]; §3 "Forming and applying the patch").
+//
+// The factors come from the randomized range finder with q power iterations (Halko,
+// Martinsson & Tropp, "Finding structure with randomness", SIAM Review 2011, Alg. 4.4) and the
+// SVD of the small projection (their Alg. 5.1):
+//   Y = Δ Ω; Q = orth(Y); q times: Z = orth(ΔᵀQ), Q = orth(Δ Z);
+//   Bᵀ = ΔᵀQ = V_B Σ Ũᵀ; U·Σ = Q Ũ_m Σ_m; V_mᵀ = (Bᵀ Ũ_m)ᵀ Σ_m⁻¹.
+// Ω [W × k] is the caller's random test matrix. Each row of V_mᵀ is signed so that its entry
+// of largest magnitude is positive (the first such entry on a tie); U·Σ's column flips with it.
+//
+// Everything is float32: GB300 runs float64 at a small fraction of its float32 rate, and the
+// steps below stay accurate in float32.
+//   orth() is shifted CholeskyQR3 (Fukaya, Kannan, Nakatsukasa, Yamamoto & Yanagisawa,
+//   "Shifted Cholesky QR for computing the QR factorization of ill-conditioned matrices",
+//   SIAM J. Sci. Comput. 2020): one Cholesky QR pass on G = YᵀY + sI with
+//   s = 11 (M k + k (k + 1)) u ‖Y‖² (u = 2⁻²⁴, ‖Y‖² bounded by trace G), then two plain passes.
+//   A pivot that is not positive (a zero column) drops its column: the column becomes zero and
+//   no later column is reduced against it.
+//   The SVD of the k-column Bᵀ is one-sided cyclic Jacobi (Hestenes 1958; Demmel & Veselić
+//   1992): pairs of columns are rotated until every pair is orthogonal to within √W·2⁻²³ of
+//   their norms (at most 30 sweeps); the rotations accumulate into Ũ and σ_j is the norm of
+//   column j.
+//
+// One CTA of 256 threads per problem (one (layer, group) deficit [T × W]). The tall sketches
+// live in a caller-provided workspace (two [max(T, W) × k] float32 buffers per problem);
+// products go through a shared-memory tiled CTA GEMM; Bᵀ, its rotations and the k × k
+// factors stay in shared memory.
+#include <mutex>
+
+#include "kamera_dev.cuh"
+
+namespace kamera {
+
+namespace {
+
+constexpr int kThr = 256;
+constexpr int kWarps = kThr / 32;
+constexpr int kTM = 64, kTK = 32;  // GEMM tile: 64 rows of C per block, K in steps of 32
+constexpr int kAPitch = kTK + 1;   // padded op(A) tile rows
+
+// Float offsets of the dynamic shared memory (one plan for host and device).
+struct FormPlan {
+  int ta, tb;    // GEMM tiles: op(A) [kTM][kAPitch], B [kTK][kMaxSketch]
+  int g, r;      // k × k: Gram matrix / Cholesky factor, and the triangular inverse
+  int v;         // k × k: Jacobi rotations Ũ, column-major
+  int bc;        // W × k: Bᵀ, column-major (column j at bc + j*W)
+  int nrm;       // k: column norms σ
+  int sc_u;      // k: U·Σ column scales (sign · σ)
+  int order;     // k ints: columns by σ, descending
+  int total;     // floats
+};
+
+__host__ __device__ inline FormPlan form_plan(int W, int k) {
+  FormPlan p;
+  int o = 0;
+  p.ta = o;
+  o += kTM * kAPitch;
+  p.tb = o;
+  o += kTK * kMaxSketch;
+  p.g = o;
+  o += k * k;
+  p.r = o;
+  o += k * k;
+  p.v = o;
+  o += k * k;
+  p.bc = o;
+  o += W * k;
+  p.nrm = o;
+  o += k;
+  p.sc_u = o;
+  o += k;
+  p.order = o;
+  o += k;
+  p.total = o;
+  return p;
+}
+
+template <typename Out>
+__device__ __forceinline__ Out to_out(float x);
+template <>
+__device__ __forceinline__ float to_out<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// C = op(A) · B with float32 accumulation, by all threads of the CTA.
+//   op(A) [M × K]: A itself (row stride lda) or, when TA, the transpose of A stored [K × M].
+//   B [K × N], row stride ldb, N <= kMaxSketch (global or shared memory).
+//   Element (i, j) goes to C[i*ldc + j], or to C[j*ldc + i] when TC, multiplied by scale[j]
+//   when scale is given. C overlaps neither A nor B.
+template <bool TA, bool TC, typename Out>
+__device__ void cta_gemm(const float *A, long long lda, const float *B, long long ldb, Out *C,
+                         long long ldc, int M, int N, int K, const float *scale, float *sm) {
+  float *ta = sm;
+  float *tb = sm + kTM * kAPitch;
+  const int tid = threadIdx.x;
+  const int rg = tid >> 4, cg = tid & 15;  // rows rg*4 + r, columns cg + 16*c
+  constexpr int CPT = kMaxSketch / 16;
+  for (int m0 = 0; m0 < M; m0 += kTM) {
+    float acc[4][CPT];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) acc[r][c] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += kTK) {
+      __syncthreads();  // the previous step's tiles are consumed
+      for (int e = tid; e < kTM * kTK; e += kThr) {
+        int i, j;
+        if (TA) {  // A is [K × M]: consecutive threads walk M
+          j = e / kTM;
+          i = e - j * kTM;
+        } else {   // A is [M × K]: consecutive threads walk K
+          i = e / kTK;
+          j = e - i * kTK;
+        }
+        const int gi = m0 + i, gk = k0 + j;
+        float x = 0.f;
+        if (gi < M && gk < K) x = TA ? A[(long long)gk * lda + gi] : A[(long long)gi * lda + gk];
+        ta[i * kAPitch + j] = x;
+      }
+      for (int e = tid; e < kTK * N; e += kThr) {
+        const int j = e / N, c = e - j * N;
+        const int gk = k0 + j;
+        tb[j * kMaxSketch + c] = gk < K ? B[(long long)gk * ldb + c] : 0.f;
+      }
+      __syncthreads();
+      const int kend = min(kTK, K - k0);
+      for (int kk = 0; kk < kend; ++kk) {
+        float av[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) av[r] = ta[(rg * 4 + r) * kAPitch + kk];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          const int col = cg + 16 * c;
+          if (col < N) {
+            const float bv = tb[kk * kMaxSketch + col];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[r][c] = fmaf(av[r], bv, acc[r][c]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int gi = m0 + rg * 4 + r;
+      if (gi < M) {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          const int col = cg + 16 * c;
+          if (col < N) {
+            const float x = scale ? acc[r][c] * scale[col] : acc[r][c];
+            if (TC)
+              C[(long long)col * ldc + gi] = to_out<Out>(x);
+            else
+              C[(long long)gi * ldc + col] = to_out<Out>(x);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// One Cholesky QR pass: dst [M × k] = src · L⁻ᵀ where L Lᵀ = srcᵀ src (+ sI when shifted).
+// Row stride k for both; src and dst are distinct buffers.
+__device__ void cholqr_pass(const float *src, float *dst, int M, int k, bool shifted, float *sm,
+                            const FormPlan &p) {
+  float *g = sm + p.g;  // row-major k × k; its lower triangle becomes L
+  float *r = sm + p.r;  // r[c*k + j] = (L⁻¹)[j][c]: the [k × k] operand of dst = src · L⁻ᵀ
+  cta_gemm<true, false, float>(src, k, src, k, g, k, k, k, M, nullptr, sm);
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int lane = tid;
+    if (shifted) {
+      float tr = 0.f;
+      for (int j = lane; j < k; j += 32) tr += g[j * k + j];
+      for (int o = 16; o > 0; o >>= 1) tr += __shfl_xor_sync(0xffffffffu, tr, o);
+      const float s = 11.f * ((float)M * k + (float)k * (k + 1)) * 5.9604645e-8f * tr;
+      __syncwarp();
+      for (int j = lane; j < k; j += 32) g[j * k + j] += s;
+      __syncwarp();
+    }
+    // right-looking Cholesky on the lower triangle
+    for (int j = 0; j < k; ++j) {
+      const float d = g[j * k + j];
+      const float ljj = d > 0.f ? sqrtf(d) : 0.f;  // not positive (or NaN): drop column j
+      const float inv = ljj > 0.f ? 1.f / ljj : 0.f;
+      __syncwarp();
+      if (lane == 0) g[j * k + j] = ljj;
+      for (int i = j + 1 + lane; i < k; i += 32) g[i * k + j] *= inv;
+      __syncwarp();
+      const int rem = k - j - 1;
+      for (int e = lane; e < rem * rem; e += 32) {
+        const int i = j + 1 + e / rem, l = j + 1 + e % rem;
+        if (l <= i) g[i * k + l] -= g[i * k + j] * g[l * k + j];
+      }
+      __syncwarp();
+    }
+    // column c of L⁻¹ solves L x = e_c (forward substitution); a dropped pivot gives x = 0
+    for (int c = lane; c < k; c += 32) {
+      for (int i = 0; i < c; ++i) r[c * k + i] = 0.f;
+      for (int i = c; i < k; ++i) {
+        float acc = i == c ? 1.f : 0.f;
+        for (int l = c; l < i; ++l) acc -= g[i * k + l] * r[c * k + l];
+        const float lii = g[i * k + i];
+        r[c * k + i] = lii > 0.f ? acc / lii : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  cta_gemm<false, false, float>(src, k, r, k, dst, k, M, k, k, nullptr, sm);
+}
+
+// Orthonormal basis of the columns of a [M × k] (row stride k) by shifted CholeskyQR3, with b
+// as the second buffer. The basis ends in b.
+__device__ void orth(float *a, float *b, int M, int k, float *sm, const FormPlan &p) {
+  cholqr_pass(a, b, M, k, true, sm, p);
+  cholqr_pass(b, a, M, k, false, sm, p);
+  cholqr_pass(a, b, M, k, false, sm, p);
+}
+
+// Pair i of round `round` in the round-robin schedule over n (even) indices: every pair
+// (p, q), p != q, meets once in n - 1 rounds and no index appears twice in one round.
+__device__ __forceinline__ void rr_pair(int n, int round, int i, int &p, int &q) {
+  if (i == 0) {
+    p = n - 1;
+    q = round;
+  } else {
+    p = (round + i) % (n - 1);
+    q = (round - i + n - 1) % (n - 1);
+  }
+}
+
+// One-sided Jacobi on the columns of bc [W × k] (column-major), rotations accumulated into
+// v [k × k] (column-major, set to I here). A warp owns one pair for its whole rotation.
+__device__ void jacobi_svd(float *bc, float *v, int W, int k) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < k * k; e += kThr) v[e] = (e / k == e % k) ? 1.f : 0.f;
+  __syncthreads();
+  const int n = k + (k & 1);  // an odd k plays a dummy column
+  const float tol = sqrtf((float)W) * 1.1920929e-7f;
+  for (int sweep = 0; sweep < 30; ++sweep) {
+    int rotated = 0;
+    for (int round = 0; round < n - 1; ++round) {
+      for (int i = warp; i < n / 2; i += kWarps) {
+        int pc, qc;
+        rr_pair(n, round, i, pc, qc);
+        if (pc >= k || qc >= k) continue;
+        float *x = bc + (long long)pc * W, *y = bc + (long long)qc * W;
+        float a = 0.f, b = 0.f, c = 0.f;
+        for (int w = lane; w < W; w += 32) {
+          const float xv = x[w], yv = y[w];
+          a = fmaf(xv, xv, a);
+          b = fmaf(yv, yv, b);
+          c = fmaf(xv, yv, c);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          a += __shfl_xor_sync(0xffffffffu, a, o);
+          b += __shfl_xor_sync(0xffffffffu, b, o);
+          c += __shfl_xor_sync(0xffffffffu, c, o);
+        }
+        if (!(fabsf(c) > tol * sqrtf(a) * sqrtf(b))) continue;  // orthogonal, or a zero column
+        const float zeta = (b - a) / (2.f * c);
+        const float t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.f)));
+        const float cs = 1.f / sqrtf(fmaf(t, t, 1.f)), sn = cs * t;
+        __syncwarp();
+        for (int w = lane; w < W; w += 32) {
+          const float xv = x[w], yv = y[w];
+          x[w] = cs * xv - sn * yv;
+          y[w] = sn * xv + cs * yv;
+        }
+        float *vx = v + pc * k, *vy = v + qc * k;
+        for (int j = lane; j < k; j += 32) {
+          const float xv = vx[j], yv = vy[j];
+          vx[j] = cs * xv - sn * yv;
+          vy[j] = sn * xv + cs * yv;
+        }
+        rotated = 1;
+        __syncwarp();
+      }
+      __syncthreads();
+    }
+    if (!__syncthreads_or(rotated)) break;
+  }
+}
+
+__global__ void __launch_bounds__(kThr, 1) form_patch_kernel(const __grid_constant__ FormArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  const FormPlan p = form_plan(a.W, a.k);
+  const int prob = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, W = a.W, k = a.k, m = a.m;
+  const float *D = a.delta + (long long)prob * a.delta_stride;
+  const float *om = a.omega + (long long)prob * a.omega_stride;
+  const long long buf = (long long)max(T, W) * k;
+  float *y = a.work + (long long)prob * 2 * buf;  // the basis Q ends here after every orth
+  float *z = y + buf;
+
+  cta_gemm<false, false, float>(D, a.ld, om, k, z, k, T, k, W, nullptr, sm);  // Y = Δ Ω
+  orth(z, y, T, k, sm, p);
+  for (int it = 0; it < a.q; ++it) {
+    cta_gemm<true, false, float>(D, a.ld, y, k, z, k, W, k, T, nullptr, sm);  // Z = Δᵀ Q
+    orth(z, y, W, k, sm, p);                                                   // Z = orth(Z)
+    cta_gemm<false, false, float>(D, a.ld, y, k, z, k, T, k, W, nullptr, sm);  // Y = Δ Z
+    orth(z, y, T, k, sm, p);                                                   // Q = orth(Y)
+  }
+  float *bc = sm + p.bc, *v = sm + p.v;
+  cta_gemm<true, true, float>(D, a.ld, y, k, bc, W, W, k, T, nullptr, sm);  // Bᵀ = Δᵀ Q
+  jacobi_svd(bc, v, W, k);
+
+  // σ_j = ‖Bᵀ ũ_j‖, then the columns by σ (descending, ties by column index)
+  float *nrm = sm + p.nrm, *sc_u = sm + p.sc_u;
+  int *order = reinterpret_cast<int *>(sm + p.order);
+  for (int j = warp; j < k; j += kWarps) {
+    const float *x = bc + (long long)j * W;
+    float s = 0.f;
+    for (int w = lane; w < W; w += 32) s = fmaf(x[w], x[w], s);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) nrm[j] = sqrtf(s);
+  }
+  __syncthreads();
+  for (int j = tid; j < k; j += kThr) {
+    int rank = 0;
+    for (int i = 0; i < k; ++i) rank += (nrm[i] > nrm[j]) || (nrm[i] == nrm[j] && i < j);
+    order[rank] = j;
+  }
+  __syncthreads();
+  // rows of V_mᵀ, signed by their largest-magnitude entry; the U·Σ column scales
+  __nv_bfloat16 *vt = a.vt + (long long)prob * a.vt_stride;
+  for (int j = warp; j < m; j += kWarps) {
+    const int c = order[j];
+    const float sig = nrm[c];
+    const float *x = bc + (long long)c * W;
+    float best = -1.f, bval = 0.f;
+    int bidx = 0x7fffffff;
+    for (int w = lane; w < W; w += 32) {
+      const float mag = fabsf(x[w]);
+      if (mag > best) {  // w grows along a lane, so a lane keeps its first maximum
+        best = mag;
+        bval = x[w];
+        bidx = w;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const float ov = __shfl_xor_sync(0xffffffffu, bval, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+      if (ob > best || (ob == best && oi < bidx)) {
+        best = ob;
+        bval = ov;
+        bidx = oi;
+      }
+    }
+    const float sgn = bval < 0.f ? -1.f : 1.f;
+    const float sv = sig > 0.f ? sgn / sig : 0.f;
+    for (int w = lane; w < W; w += 32) vt[(long long)j * W + w] = __float2bfloat16_rn(x[w] * sv);
+    if (lane == 0) {
+      sc_u[j] = sgn * sig;
+      if (a.sigma) a.sigma[(long long)prob * m + j] = sig;
+    }
+  }
+  // the columns of Ũ_m in σ order as the [k × m] operand of U·Σ = Q Ũ_m (scaled per column)
+  float *um = sm + p.g;
+  for (int e = tid; e < k * m; e += kThr) {
+    const int i = e / m, j = e - i * m;
+    um[e] = v[order[j] * k + i];
+  }
+  __syncthreads();
+  cta_gemm<false, false, __nv_bfloat16>(y, k, um, m, a.u + (long long)prob * a.u_stride, m, T, m,
+                                        k, sc_u, sm);
+}
+
+}  // namespace
+
+size_t form_patch_workspace(long long n, int T, int W, int k) {
+  const size_t rows = (size_t)(T > W ? T : W);
+  return (size_t)n * 2 * rows * (size_t)k * sizeof(float);
+}
+
+size_t form_patch_smem(int W, int k) { return (size_t)form_plan(W, k).total * sizeof(float); }
+
+cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s) {
+  static int configured[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const size_t smem = form_patch_smem(a.W, a.k);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      int optin = 0;
+      e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(form_patch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               optin);
+      if (e != cudaSuccess) return e;
+      configured[dev] = optin;
+    }
+    if ((size_t)configured[dev] < smem) return cudaErrorInvalidValue;
+  }
+  if (a.n == 0) return cudaSuccess;
+  form_patch_kernel<<<a.n, kThr, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kamera

@@ -27,8 +27,9 @@ def declared_functions():
         if f.endswith(".h"):
             src = open(os.path.join(HEADER, f)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names += re.findall(r"^\s*(?:kamera_status|const char\s*\*)\s*(kamera_\w+)\s*\(",
-                                src, flags=re.M)
+            names += re.findall(
+                r"^\s*(?:kamera_status|const char\s*\*|size_t)\s*(kamera_\w+)\s*\(", src,
+                flags=re.M)
     return sorted(set(names))
 
 
@@ -216,6 +217,63 @@ def test_batch_patch_inplace_host_checks(lib):
                                       stream=0)
     km.kamera_batch_patch_inplace(h, d, 0, 16, 8, fake_pool(), 1, STATUS, stream=0)
     km.kamera_batch_patch_inplace(h, d, 3, 16, 0, fake_pool(), -1, STATUS, stream=0)
+
+
+class FakeWorkspace(FakeTensor):
+    def __init__(self, addr, nbytes):
+        super().__init__(addr)
+        self.nbytes = nbytes
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+def test_form_patch_host_checks(lib):
+    n, T, W, k, q, m = 3, 100, 64, 16, 1, 8
+    need = km.kamera_form_patch_workspace(n, T, W, k)
+    assert need == n * 2 * max(T, W) * k * 4
+    assert km.kamera_form_patch_workspace(n, 40, 300, k) == n * 2 * 300 * k * 4
+    assert km.kamera_form_patch_workspace(-1, T, W, k) == 0
+    d, o = FakeTensor(0x100000), FakeTensor(0x200000)
+    u, vt, sig = FakeTensor(0x300000), FakeTensor(0x400000), FakeTensor(0x500000)
+    ws = FakeWorkspace(0x600000, need)
+    base = dict(k=k, q=q, m=m, num_problems=n, T=T, W=W, ld=W, delta_stride=T * W,
+                omega_stride=0, u_stride=T * m, vt_stride=m * W, d=d, o=o, u=u, vt=vt, sig=sig,
+                ws=ws)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        km.kamera_form_patch(a["d"], a["o"], a["k"], a["q"], a["m"], a["u"], a["vt"], a["sig"],
+                             a["ws"], num_problems=a["num_problems"], T=a["T"], W=a["W"],
+                             ld=a["ld"], delta_stride=a["delta_stride"],
+                             omega_stride=a["omega_stride"], u_stride=a["u_stride"],
+                             vt_stride=a["vt_stride"], stream=0)
+
+    invalid = [dict(num_problems=-1), dict(T=0), dict(W=0), dict(k=0), dict(m=0), dict(m=17),
+               dict(q=-1), dict(ld=W - 1), dict(delta_stride=-1), dict(omega_stride=-1),
+               dict(u_stride=T * m - 1), dict(vt_stride=m * W - 1), dict(d=None), dict(o=None),
+               dict(u=None), dict(vt=None), dict(ws=None), dict(d=FakeTensor(0x100002)),
+               dict(o=FakeTensor(0x200001)), dict(u=FakeTensor(0x300001)),
+               dict(vt=FakeTensor(0x400001)), dict(sig=FakeTensor(0x500002)),
+               dict(ws=FakeWorkspace(0x600000, need - 1)),
+               dict(ws=FakeWorkspace(0x600002, need))]
+    for kw in invalid:
+        with pytest.raises(km.KameraError) as e:
+            call(**kw)
+        assert e.value.status == km.KAMERA_ERR_INVALID_ARG, kw
+    # k above 96, above T or W, too many power iterations, or too much shared memory
+    unsupported = [dict(k=97, m=8, T=200, W=200), dict(k=64, T=63), dict(k=65, W=64),
+                   dict(q=17), dict(k=96, W=600, T=600)]
+    for kw in unsupported:
+        with pytest.raises(km.KameraError) as e:
+            call(**kw)
+        assert e.value.status == km.KAMERA_ERR_UNSUPPORTED, kw
+    # nothing to do: returns OK without touching the device
+    call(num_problems=0)
 
 
 def test_status_strings(lib):

@@ -534,6 +534,9 @@ def test_randomized_patch_recovers_an_exactly_low_rank_deficit():
         np.testing.assert_allclose(us, us0, atol=1e-9)
         np.testing.assert_allclose(vt, vt0, atol=1e-9)
         np.testing.assert_allclose(vt @ vt.T, np.eye(m), atol=1e-10)
+        # the sign convention: each row's largest-magnitude entry is positive
+        for row in (vt, vt0):
+            assert np.all(row[np.arange(m), np.argmax(np.abs(row), axis=1)] > 0)
 
 
 def test_randomized_patch_residual_near_the_eckart_young_optimum():
@@ -545,6 +548,10 @@ def test_randomized_patch_residual_near_the_eckart_young_optimum():
     s = 0.8 ** np.arange(W)
     delta = (u * s) @ v.T
     best = np.sqrt(np.sum(s[m:] ** 2))
+    # the exact SVD returns the planted spectrum and the planted rank-m truncation
+    us0, vt0, sig0 = ora.form_patch_svd(delta, m)
+    np.testing.assert_allclose(sig0, s[:m], rtol=1e-12)
+    np.testing.assert_allclose(us0 @ vt0, (u[:, :m] * s[:m]) @ v[:, :m].T, atol=1e-12)
     prev = np.inf
     for q in (0, 1, 2):
         us, vt, sig = ora.form_patch_randomized(delta, rng.standard_normal((W, k)), m, q)

@@ -358,4 +358,26 @@ def config5_launch_items(wl: Workload, launch: int) -> list:
     return out
 
 
+def deficit_problems(n: int, T: int, W: int, *, k: int, rank: int, decay: float,
+                     noise: float, seed: int = 0, shared_omega: bool = True, scale: float = 0.3,
+                     device="cpu"):
+    """Synthetic conditioning deficits for patch forming and their random test matrices.
+
+    Δ_i = A_i diag(scale·decay^j) B_iᵀ + noise·E_i with A_i ~ N(0, 1/T) [T × rank],
+    B_i ~ N(0, 1/W) [W × rank] and E_i ~ N(0, 1/max(T, W)) [T × W]: a geometric spectrum of
+    ``rank`` terms whose leading value is about ``scale`` (the deficit norms the pages report
+    for deep layers, §4: 0.08 to 0.49) over a noise floor of about 2·noise. Returns
+    (delta float32 [n][T][W], omega float32 [W][k] when shared, else [n][W][k]); Ω ~ N(0, 1).
+    """
+    g = _gen("cpu", seed, "deficit", n, T, W, rank)
+    s = scale * decay ** torch.arange(rank, dtype=torch.float64)
+    a = torch.randn(n, T, rank, generator=g, dtype=torch.float64) / np.sqrt(T)
+    b = torch.randn(n, W, rank, generator=g, dtype=torch.float64) / np.sqrt(W)
+    e = torch.randn(n, T, W, generator=g, dtype=torch.float64) / np.sqrt(max(T, W))
+    delta = (torch.einsum("ntr,r,nwr->ntw", a, s, b) + noise * e).to(torch.float32)
+    go = _gen("cpu", seed, "omega", n, W, k, bool(shared_omega))
+    omega = torch.randn((W, k) if shared_omega else (n, W, k), generator=go, dtype=torch.float32)
+    return delta.to(device), omega.to(device)
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
