@@ -276,6 +276,38 @@ kamera_status kamera_form_patch(const float *d_delta, int64_t ld, int64_t delta_
                                 void *d_workspace, size_t workspace_bytes,
                                 kamera_stream_t stream);
 
+/*
+ * kamera_form_patch without a caller workspace, for callers that cannot allocate device memory
+ * where they call it: a serving engine that hands all device memory left after the weights to
+ * its paged KV pool at start-up (so an allocation at patch-forming time would fail or evict
+ * cache), or host code with no device allocator of its own. The Kamera paper has no
+ * counterpart to this call; it is kamera_form_patch with the workspace taken from a fixed
+ * array of KAMERA_FORM_PATCH_SCRATCH_BYTES in this library's device memory, reserved with the
+ * library's device code.
+ *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library routine.
+ *   - Arguments, outputs, results and errors are those of kamera_form_patch. In addition, a
+ *     call whose kamera_form_patch_workspace(num_problems, T, W, k) exceeds
+ *     KAMERA_FORM_PATCH_SCRATCH_BYTES (32 MiB: e.g. 96 deficits of 1024 x 512 at k = 40)
+ *     returns KAMERA_ERR_UNSUPPORTED and launches nothing.
+ *   - Set-up: the first call with num_problems > 0 on a device looks up the array's device
+ *     address (once per device, with that device current) and keeps it; a failed lookup
+ *     returns KAMERA_ERR_CUDA. Make that first call before any stream capture.
+ *   - Nothing has to start at zero: the array's contents on entry are ignored and left
+ *     undefined.
+ *   - One array per device: calls on the same device that overlap in time (different
+ *     streams, or host threads without ordering) race on it and give undefined results.
+ *     Order them on one stream, or synchronise between them.
+ */
+#define KAMERA_FORM_PATCH_SCRATCH_BYTES (32u << 20)
+
+kamera_status kamera_form_patch_static_scratch(const float *d_delta, int64_t ld,
+                                               int64_t delta_stride, int32_t num_problems,
+                                               int32_t T, int32_t W, const float *d_omega,
+                                               int64_t omega_stride, int32_t k, int32_t q,
+                                               int32_t m, void *d_u, int64_t u_stride,
+                                               void *d_vt, int64_t vt_stride, float *d_sigma,
+                                               kamera_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

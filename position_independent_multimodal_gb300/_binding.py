@@ -26,6 +26,7 @@ KAMERA_GQA = 0
 KAMERA_MLA = 1
 KAMERA_ROPE_NEOX_HALF = 0
 KAMERA_ROPE_INTERLEAVED = 1
+KAMERA_FORM_PATCH_SCRATCH_BYTES = 32 << 20
 
 
 class KameraError(RuntimeError):
@@ -91,9 +92,12 @@ def lib() -> ctypes.CDLL:
         L.kamera_form_patch_workspace.restype = ctypes.c_size_t
         L.kamera_form_patch.argtypes = [vp, i64, i64, i32, i32, i32, vp, i64, i32, i32, i32, vp,
                                         i64, vp, i64, vp, vp, ctypes.c_size_t, vp]
+        L.kamera_form_patch_static_scratch.argtypes = [vp, i64, i64, i32, i32, i32, vp, i64,
+                                                       i32, i32, i32, vp, i64, vp, i64, vp, vp]
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
                   "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed",
-                  "kamera_patch_inplace", "kamera_batch_patch_inplace", "kamera_form_patch"):
+                  "kamera_patch_inplace", "kamera_batch_patch_inplace", "kamera_form_patch",
+                  "kamera_form_patch_static_scratch"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -264,3 +268,18 @@ def kamera_form_patch(delta: torch.Tensor, omega: torch.Tensor, k: int, q: int, 
                                    0 if workspace is None else
                                    int(workspace.numel() * workspace.element_size()),
                                    _stream(stream)), "kamera_form_patch")
+
+
+def kamera_form_patch_static_scratch(delta: torch.Tensor, omega: torch.Tensor, k: int, q: int,
+                                     m: int, u: torch.Tensor, vt: torch.Tensor,
+                                     sigma: Optional[torch.Tensor], *, num_problems: int, T: int,
+                                     W: int, ld: int, delta_stride: int, omega_stride: int,
+                                     u_stride: int, vt_stride: int, stream=None) -> None:
+    """``kamera_form_patch`` with the library's fixed device scratch instead of a caller
+    workspace (no device allocation at the call; at most ``KAMERA_FORM_PATCH_SCRATCH_BYTES``
+    of workspace; calls on one device must not overlap in time)."""
+    _check(lib().kamera_form_patch_static_scratch(
+        _ptr(delta), int(ld), int(delta_stride), int(num_problems), int(T), int(W),
+        _ptr(omega), int(omega_stride), int(k), int(q), int(m), _ptr(u), int(u_stride),
+        _ptr(vt), int(vt_stride), _ptr(sigma), _stream(stream)),
+        "kamera_form_patch_static_scratch")

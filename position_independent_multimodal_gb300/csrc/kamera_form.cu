@@ -410,3 +410,56 @@ cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s) {
 }
 
 }  // namespace kamera
+
+// ---------------------------------------------------------------------------------------
+// kamera_form_patch_static_scratch: kamera_form_patch with its workspace in a fixed array of
+// this library's device memory, for callers that cannot allocate device memory at the call
+// site (see include/kamera.h). The array is reserved with the library's device code, so the
+// call allocates nothing; one array per device, shared by every call on that device.
+// ---------------------------------------------------------------------------------------
+
+namespace {
+
+static __device__ __align__(256) float g_form_scratch[KAMERA_FORM_PATCH_SCRATCH_BYTES /
+                                                      sizeof(float)];
+
+// Device address of g_form_scratch on the current device, looked up once per device (with that
+// device current) and kept; the lookup is the set-up that the first call on a device does.
+cudaError_t form_scratch(void **out) {
+  static void *ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_form_scratch);
+    if (e != cudaSuccess) return e;
+    if (!p) return cudaErrorInvalidSymbol;
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" kamera_status kamera_form_patch_static_scratch(
+    const float *d_delta, int64_t ld, int64_t delta_stride, int32_t num_problems, int32_t T,
+    int32_t W, const float *d_omega, int64_t omega_stride, int32_t k, int32_t q, int32_t m,
+    void *d_u, int64_t u_stride, void *d_vt, int64_t vt_stride, float *d_sigma,
+    kamera_stream_t stream) {
+  if (num_problems < 0 || T < 1 || W < 1 || k < 1) return KAMERA_ERR_INVALID_ARG;
+  if (kamera::form_patch_workspace(num_problems, T, W, k) > KAMERA_FORM_PATCH_SCRATCH_BYTES)
+    return KAMERA_ERR_UNSUPPORTED;
+  if (num_problems == 0)  // argument checks only; nothing to set up or launch
+    return kamera_form_patch(d_delta, ld, delta_stride, 0, T, W, d_omega, omega_stride, k, q, m,
+                             d_u, u_stride, d_vt, vt_stride, d_sigma, nullptr, 0, stream);
+  void *scratch = nullptr;
+  if (form_scratch(&scratch) != cudaSuccess) return KAMERA_ERR_CUDA;
+  return kamera_form_patch(d_delta, ld, delta_stride, num_problems, T, W, d_omega, omega_stride,
+                           k, q, m, d_u, u_stride, d_vt, vt_stride, d_sigma, scratch,
+                           KAMERA_FORM_PATCH_SCRATCH_BYTES, stream);
+}
