@@ -203,7 +203,8 @@ def _worker_init():
                          patch_vt=None if it.patch_vt is None else wl.bf16_bits(it.patch_vt),
                          delta=it.delta, num_tokens=it.num_tokens, req=it.req,
                          start_tok=it.start_tok, patch_m=it.patch_m, patch_l0=it.patch_l0,
-                         patch_l1=it.patch_l1) for it in w.items]
+                         patch_l1=it.patch_l1, delta_h=it.delta_h, delta_w=it.delta_w)
+             for it in w.items]
     _W = (w.layout, items)
 
 
@@ -493,9 +494,9 @@ def time_calls(fn, steps, warmup=1):
 
 
 def other_workloads(dev):
-    """Brief timings of the in-place switch, MLA recall, sliding-window survival, recall-sweep
-    and patch-forming workloads (each a parity-tested configuration of its own); reported
-    beside the main line."""
+    """Brief timings of the in-place switch, M-RoPE reorder, MLA recall, sliding-window
+    survival, recall-sweep and patch-forming workloads (each a parity-tested configuration of
+    its own); reported beside the main line."""
     import torch
     import position_independent_multimodal_gb300 as km
     import workloads as wl
@@ -555,6 +556,17 @@ def other_workloads(dev):
         "ms_per_step": ms, "gb_s_moved": moved / ms / 1e6,
         "frac_hbm_peak": moved / ms / 1e6 / peak}
     del w, k, v, pool
+    torch.cuda.empty_cache()
+
+    w = wl.config2_mrope(device=dev)
+    acc = accounting(w)
+    ms = reuse_calls(w, [w.items])
+    out["mrope_reorder_18_placements"] = {
+        "workload": "the GQA reorder step with Qwen2.5-VL M-RoPE (16|24|24 pairs over t, h, w; "
+                    "t moved by j*1024, h and w by j*16 at ordering position j)",
+        "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
+        "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak}
+    del w
     torch.cuda.empty_cache()
 
     w = wl.config3(device=dev)

@@ -68,6 +68,10 @@ typedef enum kamera_status {
 #define KAMERA_ROPE_NEOX_HALF 0
 #define KAMERA_ROPE_INTERLEAVED 1
 
+/* Assignment of rope pairs to the M-RoPE sections (see kamera_layout). */
+#define KAMERA_MROPE_CONTIGUOUS 0
+#define KAMERA_MROPE_INTERLEAVED 1
+
 /*
  * Layout descriptor: the content | rope split of §3 and Fig. 2.
  *   GQA/MHA: K row = V row = num_kv_heads * head_dim; every K head rotates over its whole
@@ -78,6 +82,13 @@ typedef enum kamera_status {
  * num_kv_heads*head_dim), group 1 = V (W1 = W0); MLA group 0 = c_KV (W0 = latent_dim),
  * group 1 = k_pe (W1 = rope_dim).
  * Limits: head_dim, latent_dim, rope_dim multiples of 16; rope_dim <= 256; rows <= 16384.
+ * M-RoPE (§3 "One mechanism for MLA, GQA, and MHA"; Fig. 2, "64 rope pairs of the 128-d head
+ * (16|24|24 -> t,h,w)" and "(24|20|20 -> t,h,w)"): mrope_section = pairs of the t, h and w
+ * sections, summing to rope_dim/2, or all zero for 1-D RoPE. Which pair belongs to which
+ * section: KAMERA_MROPE_CONTIGUOUS gives pairs [0, s_t) to t, the next s_h to h, the last s_w
+ * to w; KAMERA_MROPE_INTERLEAVED gives pair i to h when i % 3 == 1 and i < 3*s_h, to w when
+ * i % 3 == 2 and i < 3*s_w, and to t otherwise. A pair of section s turns by delta_s (the
+ * item's delta, delta_h or delta_w) times its frequency.
  */
 typedef struct kamera_layout {
   int32_t kind;         /* KAMERA_GQA or KAMERA_MLA                                       */
@@ -89,6 +100,8 @@ typedef struct kamera_layout {
   int32_t rope_dim;     /* GQA: == head_dim; MLA: k_pe width (64 for DeepSeek-V2-style)   */
   int32_t rope_style;   /* KAMERA_ROPE_*                                                  */
   double rope_theta;    /* RoPE base theta > 1                                            */
+  int32_t mrope_section[3]; /* M-RoPE pairs of t, h, w; {0, 0, 0} = 1-D RoPE             */
+  int32_t mrope_style;  /* KAMERA_MROPE_*; ignored for 1-D RoPE                           */
 } kamera_layout;
 
 /*
@@ -100,7 +113,11 @@ typedef struct kamera_layout {
  * patch_vt: bf16 [l1-l0][m*W0 + m*W1]: per patched layer V_m^T of group 0 ([m][W0],
  *           row-major) followed by V_m^T of group 1 ([m][W1]).
  *           Both patch pointers are ignored when patch_m == 0 or patch_l0 == patch_l1.
- * delta   : p1 - p0, any sign (|delta| < 2^62).
+ * delta   : p1 - p0, any sign (|delta| < 2^62). With M-RoPE, the offset of the t section.
+ * delta_h, delta_w: with M-RoPE, the offsets of the h and w sections (|.| < 2^62); ignored for
+ *           1-D RoPE. Moving a chunk along the sequence advances all three coordinates
+ *           (delta_h = delta_w = delta, Fig. 2 "relocate: +delta to the (t,h,w) position id");
+ *           a temporal move changes t alone.
  * num_tokens, req, start_tok: the chunk's T tokens go to logical tokens
  *           [start_tok, start_tok + T) of page-table row req.
  * patch_m : rank, 0 (no patch) or 1..128. Layers in [patch_l0, patch_l1) get the patch.
@@ -118,6 +135,8 @@ typedef struct kamera_item {
   int32_t patch_m;
   int32_t patch_l0;
   int32_t patch_l1;
+  int64_t delta_h;
+  int64_t delta_w;
 } kamera_item;
 
 /*

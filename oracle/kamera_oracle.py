@@ -42,6 +42,8 @@ GQA = 0
 MLA = 1
 NEOX_HALF = 0
 INTERLEAVED = 1
+MROPE_CONTIGUOUS = 0
+MROPE_INTERLEAVED = 1
 
 
 # ----------------------------------------------------------------------------------------
@@ -117,24 +119,85 @@ def rope_pairs(d: int, style: int):
     raise ValueError("unknown rope style")
 
 
-def rotate_band(x, delta: int, theta: float, style: int) -> np.ndarray:
+def rotate_band(x, delta, theta: float, style: int) -> np.ndarray:
     """Apply R(δ) to the last axis of ``x`` (a full rope band of even width d).
 
     Each pair (a, b) turns by φ_k = δ·inv_freq_k:  a' = a cos φ - b sin φ,  b' = b cos φ + a sin φ
-    (§3 "Relocate": re-rotate B's keys by δ). δ = 0 returns the input unchanged.
+    (§3 "Relocate": re-rotate B's keys by δ). ``delta`` is one integer for every pair, or one
+    integer per pair (M-RoPE: each pair takes its section's offset). All zero returns the
+    input unchanged.
     """
     x = np.asarray(x, dtype=np.float64)
     out = x.copy()
-    if delta == 0:
-        return out
     d = x.shape[-1]
-    phi = float(delta) * inv_freq(theta, d)
+    if np.ndim(delta) == 0:
+        if delta == 0:
+            return out
+        phi = float(delta) * inv_freq(theta, d)
+    else:
+        offs = [int(v) for v in delta]
+        if len(offs) != d // 2:
+            raise ValueError("one offset per rope pair")
+        if not any(offs):
+            return out
+        phi = np.array([float(v) for v in offs]) * inv_freq(theta, d)
     c, s = np.cos(phi), np.sin(phi)
     ia, ib = rope_pairs(d, style)
     a, b = x[..., ia], x[..., ib]
     out[..., ia] = a * c - b * s
     out[..., ib] = b * c + a * s
     return out
+
+
+def mrope_pair_axes(npairs: int, sections, style: int) -> np.ndarray:
+    """M-RoPE section of each rope pair: 0 = t, 1 = h, 2 = w (Kamera Fig. 2: the 64 rope pairs
+    of a 128-d head split 16|24|24 or 24|20|20 over t, h, w).
+
+    Contiguous: the first s_t pairs are t, the next s_h are h, the last s_w are w.
+    Interleaved: h takes every third pair from pair 1 (s_h of them), w every third pair from
+    pair 2 (s_w of them), and t takes the rest.
+    """
+    s_t, s_h, s_w = (int(v) for v in sections)
+    if min(s_t, s_h, s_w) < 0 or s_t + s_h + s_w != npairs:
+        raise ValueError("M-RoPE sections must sum to the rope pairs")
+    if style == MROPE_CONTIGUOUS:
+        return np.array([0] * s_t + [1] * s_h + [2] * s_w)
+    if style == MROPE_INTERLEAVED:
+        axes = np.zeros(npairs, dtype=int)
+        h = list(range(1, npairs, 3))[:s_h]
+        w = list(range(2, npairs, 3))[:s_w]
+        if len(h) != s_h or len(w) != s_w:
+            raise ValueError("interleaved M-RoPE sections do not fit the rope pairs")
+        axes[h] = 1
+        axes[w] = 2
+        return axes
+    raise ValueError("unknown M-RoPE style")
+
+
+def has_mrope(layout) -> bool:
+    return any(int(v) != 0 for v in getattr(layout, "mrope_section", (0, 0, 0)))
+
+
+def pair_offsets(layout, item, npairs: int):
+    """The relocation offset of each rope pair of a band: the item's δ for every pair under
+    1-D RoPE; under M-RoPE, pair k takes (δ_t, δ_h, δ_w)[section of k], where δ_t = delta and
+    δ_h, δ_w default to delta (all three coordinates advance together, Fig. 2 "relocate: +δ to
+    the (t,h,w) position id")."""
+    if not has_mrope(layout):
+        return int(item.delta)
+    dh = getattr(item, "delta_h", None)
+    dw = getattr(item, "delta_w", None)
+    offs = (int(item.delta), int(item.delta if dh is None else dh),
+            int(item.delta if dw is None else dw))
+    axes = mrope_pair_axes(npairs, layout.mrope_section, getattr(layout, "mrope_style", 0))
+    return [offs[a] for a in axes]
+
+
+def item_rotates(layout, item) -> bool:
+    """Whether any rope pair of the item turns."""
+    if not has_mrope(layout):
+        return int(item.delta) != 0
+    return any(v != 0 for v in pair_offsets(layout, item, int(sum(layout.mrope_section))))
 
 
 # ----------------------------------------------------------------------------------------
@@ -193,10 +256,10 @@ def reuse_layer(layout, item, layer: int, channel: int, tokens=None):
         rows = rows[np.asarray(tokens)]
     x = bf16_to_f64(rows)
     copy_mask = np.ones(x.shape[-1], dtype=bool)
-    if channel == 0 and item.delta != 0:
+    if channel == 0 and item_rotates(layout, item):
         for c0, d in rope_bands(layout):
-            x[:, c0:c0 + d] = rotate_band(x[:, c0:c0 + d], item.delta, layout.rope_theta,
-                                          layout.rope_style)
+            x[:, c0:c0 + d] = rotate_band(x[:, c0:c0 + d], pair_offsets(layout, item, d // 2),
+                                          layout.rope_theta, layout.rope_style)
             copy_mask[c0:c0 + d] = False
     if layer_patched(item, layer):
         m = item.patch_m
@@ -234,7 +297,7 @@ def magnitude_layer(layout, item, layer: int, channel: int, tokens=None) -> np.n
         rows = rows[np.asarray(tokens)]
     x = bf16_to_f64(rows)
     mag = np.abs(x)
-    if channel == 0 and item.delta != 0:
+    if channel == 0 and item_rotates(layout, item):
         for c0, d in rope_bands(layout):
             ia, ib = rope_pairs(d, layout.rope_style)
             ab = np.abs(x[:, c0 + ia]) + np.abs(x[:, c0 + ib])
@@ -388,7 +451,7 @@ def patch_byte_fraction(T: int, W: int, m: int) -> float:
 def as_item(**kw) -> SimpleNamespace:
     """Convenience record with the fields the oracle reads."""
     base = dict(canon_v=None, patch_u=None, patch_vt=None, patch_m=0, patch_l0=0, patch_l1=0,
-                req=0, start_tok=0)
+                req=0, start_tok=0, delta_h=None, delta_w=None)
     base.update(kw)
     if "num_tokens" not in base:
         base["num_tokens"] = int(np.asarray(base["canon_k"]).shape[1])

@@ -26,6 +26,8 @@ KAMERA_GQA = 0
 KAMERA_MLA = 1
 KAMERA_ROPE_NEOX_HALF = 0
 KAMERA_ROPE_INTERLEAVED = 1
+KAMERA_MROPE_CONTIGUOUS = 0
+KAMERA_MROPE_INTERLEAVED = 1
 KAMERA_FORM_PATCH_SCRATCH_BYTES = 32 << 20
 
 
@@ -40,7 +42,8 @@ class kamera_layout(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("latent_dim", ctypes.c_int32),
                 ("rope_dim", ctypes.c_int32), ("rope_style", ctypes.c_int32),
-                ("rope_theta", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("mrope_section", ctypes.c_int32 * 3),
+                ("mrope_style", ctypes.c_int32)]
 
 
 class kamera_item(ctypes.Structure):
@@ -49,7 +52,8 @@ class kamera_item(ctypes.Structure):
                 ("delta", ctypes.c_int64), ("num_tokens", ctypes.c_int32),
                 ("req", ctypes.c_int32), ("start_tok", ctypes.c_int32),
                 ("patch_m", ctypes.c_int32), ("patch_l0", ctypes.c_int32),
-                ("patch_l1", ctypes.c_int32)]
+                ("patch_l1", ctypes.c_int32), ("delta_h", ctypes.c_int64),
+                ("delta_w", ctypes.c_int64)]
 
 
 class kamera_pool(ctypes.Structure):
@@ -123,10 +127,12 @@ def _stream(stream) -> Optional[int]:
 
 
 def make_layout(layout) -> kamera_layout:
-    """Any object with the descriptor's fields -> the C struct."""
+    """Any object with the descriptor's fields -> the C struct (M-RoPE fields optional)."""
+    sec = tuple(int(x) for x in getattr(layout, "mrope_section", (0, 0, 0)))
     return kamera_layout(int(layout.kind), int(layout.num_layers), int(layout.page_size),
                          int(layout.num_kv_heads), int(layout.head_dim), int(layout.latent_dim),
-                         int(layout.rope_dim), int(layout.rope_style), float(layout.rope_theta))
+                         int(layout.rope_dim), int(layout.rope_style), float(layout.rope_theta),
+                         (ctypes.c_int32 * 3)(*sec), int(getattr(layout, "mrope_style", 0)))
 
 
 class Handle:
@@ -170,12 +176,16 @@ class Pool:
 
 
 def make_item(it) -> kamera_item:
-    """An object with the kamera_item fields (tensors for the pointers) -> the C struct."""
+    """An object with the kamera_item fields (tensors for the pointers) -> the C struct.
+    ``delta_h`` / ``delta_w`` default to ``delta`` (all M-RoPE coordinates move together)."""
+    dh = getattr(it, "delta_h", None)
+    dw = getattr(it, "delta_w", None)
     return kamera_item(_ptr(it.canon_k), _ptr(getattr(it, "canon_v", None)),
                        _ptr(getattr(it, "patch_u", None)), _ptr(getattr(it, "patch_vt", None)),
                        int(it.delta), int(it.num_tokens), int(it.req), int(it.start_tok),
                        int(getattr(it, "patch_m", 0)), int(getattr(it, "patch_l0", 0)),
-                       int(getattr(it, "patch_l1", 0)))
+                       int(getattr(it, "patch_l1", 0)), int(it.delta if dh is None else dh),
+                       int(it.delta if dw is None else dw))
 
 
 def pack_items(items: Sequence) -> torch.Tensor:

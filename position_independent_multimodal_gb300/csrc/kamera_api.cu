@@ -70,6 +70,22 @@ kamera_status fill_layout(const kamera_layout &d, DevLayout *out) {
     return KAMERA_ERR_INVALID_ARG;
   }
   l.npairs = l.rope_d / 2;
+  // M-RoPE sections: pairs of t, h, w summing to the band's pairs (Fig. 2 "16|24|24")
+  const int st = d.mrope_section[0], sh = d.mrope_section[1], sw = d.mrope_section[2];
+  l.mrope = 0;
+  if (st != 0 || sh != 0 || sw != 0) {
+    if (st < 0 || sh < 0 || sw < 0 || st + sh + sw != l.npairs) return KAMERA_ERR_INVALID_ARG;
+    if (d.mrope_style == KAMERA_MROPE_INTERLEAVED) {
+      if (3 * sh > l.npairs + 1 || 3 * sw > l.npairs) return KAMERA_ERR_INVALID_ARG;
+    } else if (d.mrope_style != KAMERA_MROPE_CONTIGUOUS) {
+      return KAMERA_ERR_INVALID_ARG;
+    }
+    l.mrope = 1;
+    l.mrope_t = st;
+    l.mrope_h = sh;
+    l.mrope_w = sw;
+    l.mrope_style = d.mrope_style;
+  }
   *out = l;
   return KAMERA_OK;
 }

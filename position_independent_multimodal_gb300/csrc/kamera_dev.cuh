@@ -27,6 +27,8 @@ struct DevLayout {
   // heads; MLA rows into latent tiles of `tw` plus one tile for the k_pe band
   int tw;            // tile width (<= 256, multiple of 16)
   int ntile;         // tiles per row (same for both GQA channels)
+  int mrope;         // 1: M-RoPE sections (each rope pair turns by its section's offset)
+  int mrope_t, mrope_h, mrope_w, mrope_style;  // pairs per section, KAMERA_MROPE_*
 };
 
 // Engines for patched tiles.
@@ -140,6 +142,9 @@ __host__ __device__ inline int item_check(const kamera_item &it, const DevLayout
   if (it.patch_m < 0 || it.patch_m > kMaxRank) return KAMERA_ERR_UNSUPPORTED;
   if (it.patch_m > max_m) return KAMERA_ERR_INVALID_ARG;
   if (it.delta > (1ll << 62) || it.delta < -(1ll << 62)) return KAMERA_ERR_INVALID_ARG;
+  if (lay.mrope && (it.delta_h > (1ll << 62) || it.delta_h < -(1ll << 62) ||
+                    it.delta_w > (1ll << 62) || it.delta_w < -(1ll << 62)))
+    return KAMERA_ERR_INVALID_ARG;
   if (it.num_tokens == 0) return 0;
   if (!it.canon_k || !aligned16(it.canon_k)) return KAMERA_ERR_INVALID_ARG;
   if (lay.kind == KAMERA_GQA) {
@@ -181,6 +186,31 @@ __host__ __device__ inline int inplace_item_check(const kamera_item &it, const D
        (reinterpret_cast<uintptr_t>(it.patch_u) & 1u)))
     return KAMERA_ERR_INVALID_ARG;
   return 0;
+}
+
+// M-RoPE section of rope pair i: 0 t, 1 h, 2 w. Contiguous: [0, t) t, then h, then w;
+// interleaved: h at i % 3 == 1 below 3h, w at i % 3 == 2 below 3w, t elsewhere.
+__host__ __device__ __forceinline__ int mrope_axis(const DevLayout &l, int i) {
+  if (l.mrope_style == KAMERA_MROPE_INTERLEAVED) {
+    const int r = i % 3;
+    return (r == 1 && i < 3 * l.mrope_h) ? 1 : (r == 2 && i < 3 * l.mrope_w) ? 2 : 0;
+  }
+  return i < l.mrope_t ? 0 : (i < l.mrope_t + l.mrope_h ? 1 : 2);
+}
+
+// Offset of rope pair i: the item's delta under 1-D RoPE; under M-RoPE, delta, delta_h or
+// delta_w by the pair's section.
+__host__ __device__ __forceinline__ long long pair_delta(const kamera_item &it,
+                                                         const DevLayout &l, int i) {
+  if (!l.mrope) return it.delta;
+  const int axis = mrope_axis(l, i);
+  return axis == 0 ? it.delta : (axis == 1 ? it.delta_h : it.delta_w);
+}
+
+// Whether any rope pair of the item turns.
+__host__ __device__ __forceinline__ bool item_rotates(const kamera_item &it,
+                                                      const DevLayout &l) {
+  return it.delta != 0 || (l.mrope && (it.delta_h != 0 || it.delta_w != 0));
 }
 
 __device__ __forceinline__ bool layer_patched(const kamera_item &it, int layer) {

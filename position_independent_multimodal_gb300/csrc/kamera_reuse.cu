@@ -328,9 +328,9 @@ __device__ __forceinline__ void run_task(const ReuseArgs &a, unsigned char *smem
     ptx::mbar_init(s_bar + 8, 1);
     ptx::fence_mbar_init();
   }
-  if (tile.band)  // cos/sin of this item's offset, once per CTA
+  if (tile.band)  // cos/sin of each pair's offset, once per CTA
     for (int i = tid; i < lay.npairs; i += kThr) {
-      const float2 c = rope_phase(a.freq.q[i], it.delta);
+      const float2 c = rope_phase(a.freq.q[i], pair_delta(it, lay, i));
       rot[i] = c.x;
       rot[lay.npairs + i] = c.y;
       rot[2 * lay.npairs + i] = -c.y;
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
     return;
   }
   if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;  // the copy kernel's work
-  const bool rotate = ch == 0 && it.delta != 0;
+  const bool rotate = ch == 0 && item_rotates(it, lay);
   const Tile tile = tile_of(lay, ch, ct, rotate);
   // compile-time shapes of the reference layouts; everything else takes the general path
   // (NeoX tiles of 64 or 128 columns with the tensor engine run in reuse_fast_kernel)

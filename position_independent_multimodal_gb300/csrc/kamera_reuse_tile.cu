@@ -293,9 +293,9 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
     ptx::fence_mbar_init();
     *flag = 0;
   }
-  if (BAND > 0)  // cos/sin of the item's offset, once per CTA
+  if (BAND > 0)  // cos/sin of each pair's offset, once per CTA
     for (int i = tid; i < lay.npairs; i += kThrT) {
-      const float2 c = rope_phase(a.freq.q[i], it.delta);
+      const float2 c = rope_phase(a.freq.q[i], pair_delta(it, lay, i));
       rot[i] = c.x;
       rot[lay.npairs + i] = c.y;
       rot[2 * lay.npairs + i] = -c.y;
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_const
   // rejected items are reported by the copy kernel; unpatched layers are its work too
   if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) return;
   if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;
-  const bool rotate = ch == 0 && it.delta != 0;
+  const bool rotate = ch == 0 && item_rotates(it, lay);
   const Tile tile = tile_of(lay, ch, ct, rotate);
   if (tile.ncols == 128) {
     if (tile.band == 0)

@@ -175,10 +175,11 @@ __global__ void __launch_bounds__(kThreads) reuse_copy_kernel(const __grid_const
   const int t0 = blockIdx.x * kCopyRows;
   if (t0 >= it.num_tokens || layer_patched(it, layer)) return;
   const int rows = min(kCopyRows, it.num_tokens - t0);
-  const bool rotate = ch == 0 && it.delta != 0;
+  const bool rotate = ch == 0 && item_rotates(it, lay);
   const int row = ch == 0 ? lay.row_k : lay.row_v;
   if (rotate)
-    for (int i = tid; i < lay.npairs; i += kThreads) cs[i] = rope_phase(a.freq.q[i], it.delta);
+    for (int i = tid; i < lay.npairs; i += kThreads)
+      cs[i] = rope_phase(a.freq.q[i], pair_delta(it, lay, i));
   for (int r = tid; r < rows; r += kThreads) {
     const long long slot =
         slot_of(a.pool, lay.page_size, it.req, (long long)it.start_tok + t0 + r, a.status);

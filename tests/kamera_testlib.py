@@ -47,7 +47,8 @@ def oracle_item(it: wl.Item, lazy: bool = False):
     return ora.as_item(canon_k=conv(it.canon_k), canon_v=conv(it.canon_v),
                        patch_u=conv(it.patch_u), patch_vt=conv(it.patch_vt), delta=it.delta,
                        num_tokens=it.num_tokens, req=it.req, start_tok=it.start_tok,
-                       patch_m=it.patch_m, patch_l0=it.patch_l0, patch_l1=it.patch_l1)
+                       patch_m=it.patch_m, patch_l0=it.patch_l0, patch_l1=it.patch_l1,
+                       delta_h=it.delta_h, delta_w=it.delta_w)
 
 
 def sentinel_pool(layout: wl.Layout, num_slots: int, device="cuda"):
@@ -161,7 +162,8 @@ def mini_item(layout, it: wl.Item, layer: int, toks: np.ndarray):
         pv = {li: wl.bf16_bits(it.patch_vt[li])}
     return ora.as_item(canon_k=ck, canon_v=cv, patch_u=pu, patch_vt=pv, delta=it.delta,
                        num_tokens=len(toks), req=it.req, start_tok=0, patch_m=it.patch_m,
-                       patch_l0=it.patch_l0, patch_l1=it.patch_l1)
+                       patch_l0=it.patch_l0, patch_l1=it.patch_l1, delta_h=it.delta_h,
+                       delta_w=it.delta_w)
 
 
 def check_sampled(layout, it: wl.Item, layer: int, ch: int, toks, pool: torch.Tensor,

@@ -42,8 +42,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_sizes():
-    assert ctypes.sizeof(kb.kamera_item) == 64
-    assert ctypes.sizeof(kb.kamera_layout) == 40
+    assert ctypes.sizeof(kb.kamera_item) == 80
+    assert ctypes.sizeof(kb.kamera_layout) == 56
     assert ctypes.sizeof(kb.kamera_pool) == 40
 
 
@@ -65,6 +65,12 @@ def gqa(**kw):
     (dict(head_dim=72, rope_dim=72), km.KAMERA_ERR_UNSUPPORTED),
     (dict(head_dim=512, rope_dim=512), km.KAMERA_ERR_UNSUPPORTED),
     (dict(num_kv_heads=200, head_dim=128, rope_dim=128), km.KAMERA_ERR_UNSUPPORTED),
+    # M-RoPE sections must cover the 32 pairs exactly, be non-negative and fit their style
+    (dict(mrope_section=(8, 12, 11)), km.KAMERA_ERR_INVALID_ARG),
+    (dict(mrope_section=(40, -4, -4)), km.KAMERA_ERR_INVALID_ARG),
+    (dict(mrope_section=(8, 12, 12), mrope_style=2), km.KAMERA_ERR_INVALID_ARG),
+    (dict(mrope_section=(0, 12, 20), mrope_style=wl.MROPE_INTERLEAVED),
+     km.KAMERA_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_layouts(lib, kw, status):
     with pytest.raises(km.KameraError) as e:
@@ -74,6 +80,9 @@ def test_create_rejects_bad_layouts(lib, kw, status):
 
 def test_create_accepts_reference_layouts(lib):
     km.create(wl.config1().layout)
+    km.create(gqa(head_dim=128, rope_dim=128, mrope_section=(16, 24, 24)))
+    km.create(gqa(head_dim=128, rope_dim=128, mrope_section=(24, 20, 20),
+                  mrope_style=wl.MROPE_INTERLEAVED))
     km.create(wl.Layout(kind=wl.MLA, num_layers=27, page_size=16, latent_dim=512, rope_dim=64,
                         rope_style=wl.NEOX_HALF, rope_theta=1e4))
     km.create(wl.Layout(kind=wl.MLA, num_layers=2, page_size=16, latent_dim=512, rope_dim=72,

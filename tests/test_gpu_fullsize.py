@@ -67,6 +67,17 @@ def check_units(w, items, k, v, n_units, seed, layers=None):
     return st
 
 
+def test_config2_mrope_reorder_full():
+    # the reorder workload with blocked 16|24|24 M-RoPE sections and different t / h,w offsets
+    w = wl.config2_mrope(device="cuda")
+    assert any(it.delta_h != it.delta for it in w.items)
+    k, v, status = run_batch(w, w.items)
+    assert status == 0
+    assert unwritten_rows(k) == 0 and unwritten_rows(v) == 0
+    st = check_units(w, w.items, k, v, 40, seed=12)
+    assert st.computed > 0
+
+
 def test_config2_gqa_reorder_full():
     w = wl.config2(device="cuda")
     k, v, status = run_batch(w, w.items)

@@ -89,6 +89,56 @@ def test_mla_ragged_batch(m, style):
     run_and_check(ragged(mla_layout(style=style), m, f"mla{m}{style}"))
 
 
+def with_mrope_offsets(w, seed):
+    """Give every item its own (δ_t, δ_h, δ_w): a temporal move (h, w still), a move of all
+    three together, a move with t still, and independent offsets, in turn."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i, it in enumerate(w.items):
+        kind = i % 4
+        if kind == 0:
+            dh = dw = 0
+        elif kind == 1:
+            dh = dw = it.delta
+        elif kind == 2:
+            it = dataclasses.replace(it, delta=0)
+            dh, dw = int(rng.integers(1, 5000)), -int(rng.integers(1, 5000))
+        else:  # within ±2^20, where the float64 angle of the oracle is exact to ~1e-10 rad
+            dh, dw = int(rng.integers(-(1 << 20), 1 << 20)), int(rng.integers(-70000, 70000))
+        out.append(dataclasses.replace(it, delta_h=dh, delta_w=dw))
+    w.items = out
+    return w
+
+
+def mrope_layout(style, sections, H, theta, rope_style=wl.NEOX_HALF, L=3):
+    return wl.Layout(kind=wl.GQA, num_layers=L, page_size=16, num_kv_heads=H, head_dim=128,
+                     rope_dim=128, rope_style=rope_style, rope_theta=theta,
+                     mrope_section=sections, mrope_style=style)
+
+
+@pytest.mark.parametrize("m", [0, 12, 32])
+@pytest.mark.parametrize("which", ["blocked-16-24-24", "interleaved-24-20-20"])
+@pytest.mark.parametrize("batch", [False, True])
+def test_mrope_per_section_offsets(which, m, batch):
+    # Fig. 2: Qwen2.5-VL's 16|24|24 blocked sections (4 KV heads, θ = 1e6) and Qwen3-VL's
+    # 24|20|20 interleaved sections (8 KV heads, θ = 5e6), every pair turning by its
+    # section's offset; rank 32 takes the tensor cores, rank 12 the CUDA cores, rank 0 only
+    # the copy kernel
+    if which.startswith("blocked"):
+        lay = mrope_layout(wl.MROPE_CONTIGUOUS, (16, 24, 24), 4, 1e6)
+    else:
+        lay = mrope_layout(wl.MROPE_INTERLEAVED, (24, 20, 20), 8, 5e6)
+    w = with_mrope_offsets(ragged(lay, m, f"mrope{which}{m}"), seed=m)
+    st = run_and_check(w, batch=batch)
+    assert st.computed > 0
+
+
+def test_mrope_with_interleaved_pairing_takes_the_general_kernel():
+    # interleaved (2i, 2i+1) pairing is served by the general pipeline
+    lay = mrope_layout(wl.MROPE_CONTIGUOUS, (16, 24, 24), 2, 1e6, rope_style=wl.INTERLEAVED)
+    run_and_check(with_mrope_offsets(ragged(lay, 32, "mropeil"), seed=3))
+
+
 def test_mla_latent_is_byte_exact_on_unpatched_layers():
     w = ragged(mla_layout(L=4), 32, "mlab")
     w.items = [it for it in w.items]

@@ -603,6 +603,90 @@ def test_layout_reading_matches_printed_shapes():
     assert c0 == 512 and len(ora.rope_pairs(d, ora.NEOX_HALF)[0]) == g["kimivl_krope_pairs"]
 
 
+# ------------------------------------------------------------------------------------------
+# M-RoPE sections (Fig. 2: 16|24|24 and 24|20|20 pairs over t, h, w)
+# ------------------------------------------------------------------------------------------
+
+def mrope_layout(style, sections, theta=1e6, heads=2):
+    return ns_layout(num_kv_heads=heads, head_dim=128, rope_dim=128, rope_theta=theta,
+                     mrope_section=tuple(sections), mrope_style=style)
+
+
+def test_mrope_sections_match_printed_counts():
+    g = read_golden("pages_shapes.txt")
+    npairs = g["qwen25vl_rope_pairs_per_head"]
+    blocked = [g["qwen25vl_mrope_t"], g["qwen25vl_mrope_h"], g["qwen25vl_mrope_w"]]
+    inter = [g["qwen3vl_mrope_t"], g["qwen3vl_mrope_h"], g["qwen3vl_mrope_w"]]
+    assert sum(blocked) == sum(inter) == npairs
+    for style, sec in ((ora.MROPE_CONTIGUOUS, blocked), (ora.MROPE_INTERLEAVED, inter)):
+        axes = ora.mrope_pair_axes(npairs, sec, style)
+        assert [int(np.sum(axes == a)) for a in range(3)] == sec
+    # blocked: t, then h, then w, in the printed order
+    axes = ora.mrope_pair_axes(npairs, blocked, ora.MROPE_CONTIGUOUS)
+    assert np.all(np.diff(axes) >= 0) and axes[0] == 0 and axes[-1] == 2
+    # interleaved: h and w alternate with t across the pairs, never two h or two w adjacent
+    axes = ora.mrope_pair_axes(npairs, inter, ora.MROPE_INTERLEAVED)
+    assert all(not (axes[i] == axes[i + 1] and axes[i] != 0) for i in range(npairs - 1))
+    with pytest.raises(ValueError):
+        ora.mrope_pair_axes(npairs, [16, 24, 23], ora.MROPE_CONTIGUOUS)
+
+
+@pytest.mark.parametrize("style,sections", [(ora.MROPE_CONTIGUOUS, (16, 24, 24)),
+                                            (ora.MROPE_INTERLEAVED, (24, 20, 20))])
+def test_mrope_equal_offsets_are_one_dimensional_rope(style, sections):
+    # Fig. 2 caption: relocation advances all three coordinates together, so the layout of
+    # the sections does not matter: the result equals 1-D RoPE by the same delta, bit for bit
+    lay = mrope_layout(style, sections)
+    flat = mrope_layout(style, (0, 0, 0))
+    T = 5
+    canon = ora.f64_to_bf16(RNG.standard_normal((1, T, 256)))
+    for delta in (1, -77, 123457):
+        a = ora.as_item(canon_k=canon, canon_v=canon, delta=delta, num_tokens=T)
+        b = ora.as_item(canon_k=canon, canon_v=canon, delta=delta, delta_h=delta, delta_w=delta,
+                        num_tokens=T)
+        assert np.array_equal(ora.reuse_layer_bits(lay, a, 0, 0), ora.reuse_layer_bits(flat, a, 0, 0))
+        assert np.array_equal(ora.reuse_layer_bits(lay, b, 0, 0), ora.reuse_layer_bits(flat, a, 0, 0))
+
+
+@pytest.mark.parametrize("style,sections", [(ora.MROPE_CONTIGUOUS, (16, 24, 24)),
+                                            (ora.MROPE_INTERLEAVED, (24, 20, 20))])
+def test_mrope_pair_turns_by_its_section_offset(style, sections):
+    # each pair, taken one at a time in pure Python: a complex multiplication by
+    # exp(i * delta_section * theta^(-2k/d)) with delta_section chosen by the pair's section
+    lay = mrope_layout(style, sections, heads=1)
+    d = 128
+    offs = (1000, -3, 41)
+    x = RNG.standard_normal((2, d))
+    it = ora.as_item(canon_k=None, delta=offs[0], delta_h=offs[1], delta_w=offs[2], num_tokens=2)
+    got = ora.rotate_band(x, ora.pair_offsets(lay, it, d // 2), lay.rope_theta, ora.NEOX_HALF)
+    axes = ora.mrope_pair_axes(d // 2, sections, style)
+    for k in range(d // 2):
+        phi = offs[axes[k]] * lay.rope_theta ** (-2.0 * k / d)
+        for r in range(2):
+            z = complex(x[r, k], x[r, k + d // 2]) * cmath.exp(1j * phi)
+            assert abs(got[r, k] - z.real) <= 1e-12 and abs(got[r, k + d // 2] - z.imag) <= 1e-12
+    # a temporal move (delta_t only) leaves every h and w pair exactly as it was
+    it_t = ora.as_item(canon_k=None, delta=500, delta_h=0, delta_w=0, num_tokens=2)
+    got_t = ora.rotate_band(x, ora.pair_offsets(lay, it_t, d // 2), lay.rope_theta, ora.NEOX_HALF)
+    still = np.flatnonzero(axes != 0)
+    assert np.array_equal(got_t[:, still], x[:, still])
+    assert np.array_equal(got_t[:, still + d // 2], x[:, still + d // 2])
+    assert not np.allclose(got_t[:, np.flatnonzero(axes == 0)], x[:, np.flatnonzero(axes == 0)])
+
+
+def test_mrope_offsets_compose_per_section():
+    lay = mrope_layout(ora.MROPE_INTERLEAVED, (24, 20, 20), heads=1)
+    x = RNG.standard_normal((3, 128))
+    a = ora.as_item(canon_k=None, delta=7, delta_h=-2000, delta_w=31, num_tokens=3)
+    b = ora.as_item(canon_k=None, delta=-900, delta_h=5, delta_w=1 << 20, num_tokens=3)
+    ab = ora.as_item(canon_k=None, delta=7 - 900, delta_h=-2000 + 5, delta_w=31 + (1 << 20),
+                     num_tokens=3)
+    po = lambda it: ora.pair_offsets(lay, it, 64)
+    two = ora.rotate_band(ora.rotate_band(x, po(a), 1e6, ora.NEOX_HALF), po(b), 1e6, ora.NEOX_HALF)
+    one = ora.rotate_band(x, po(ab), 1e6, ora.NEOX_HALF)
+    np.testing.assert_allclose(two, one, atol=1e-9)
+
+
 def test_patch_byte_fraction_matches_printed_values():
     with open(os.path.join(GOLDEN, "patch_fraction.txt")) as f:
         rows = [l.split("|")[0] for l in f if l.strip() and not l.startswith("#")]

@@ -34,6 +34,8 @@ GQA = 0
 MLA = 1
 NEOX_HALF = 0
 INTERLEAVED = 1
+MROPE_CONTIGUOUS = 0
+MROPE_INTERLEAVED = 1
 
 # sentinel bf16 bit pattern that untouched pool slots keep; chosen finite and unlikely
 POOL_SENTINEL_BITS = 0x5A5A
@@ -50,6 +52,8 @@ class Layout:
     rope_dim: int = 0
     rope_style: int = NEOX_HALF
     rope_theta: float = 10000.0
+    mrope_section: tuple = (0, 0, 0)      # M-RoPE pairs of t, h, w; (0, 0, 0) = 1-D RoPE
+    mrope_style: int = 0                  # MROPE_CONTIGUOUS or MROPE_INTERLEAVED
 
     # widths of the stored rows and of the two patch groups (pure shape bookkeeping)
     @property
@@ -85,6 +89,8 @@ class Item:
     patch_l0: int = 0
     patch_l1: int = 0
     chunk_id: int = -1                    # which distinct canonical this item reads
+    delta_h: Optional[int] = None         # M-RoPE h / w offsets (None: same as delta)
+    delta_w: Optional[int] = None
 
 
 @dataclasses.dataclass
@@ -261,6 +267,19 @@ def config2(seed: int = 0, device="cpu") -> Workload:
             placements.append((c, r, j * T, j * T))
     return reuse_workload("cfg2", lay, n_chunks=3, T=T, placements=placements, m=32,
                           l0=14, l1=28, seed=seed, device=device, outliers=True)
+
+
+def config2_mrope(seed: int = 0, device="cpu") -> Workload:
+    """The GQA reorder workload with Qwen2.5-VL's M-RoPE: sections of 16|24|24 rope pairs over
+    t, h, w (Fig. 2), blocked. Each chunk is a 1024-token video segment of 4 × 16 × 16 merged
+    tokens; position j of an ordering moves its t coordinate by j·1024 (as the 1-D workload
+    does) and its h and w coordinates by j·16 (one 16 × 16 grid per segment), so the three
+    sections turn by different offsets."""
+    w = config2(seed, device)
+    lay = dataclasses.replace(w.layout, mrope_section=(16, 24, 24), mrope_style=MROPE_CONTIGUOUS)
+    items = [dataclasses.replace(it, delta_h=(it.delta // 1024) * 16,
+                                 delta_w=(it.delta // 1024) * 16) for it in w.items]
+    return dataclasses.replace(w, name="cfg2_mrope", layout=lay, items=items)
 
 
 def config3(seed: int = 0, device="cpu", n_chunks: int = 64) -> Workload:
