@@ -494,8 +494,8 @@ def time_calls(fn, steps, warmup=1):
 
 
 def other_workloads(dev):
-    """Brief timings of the in-place switch, M-RoPE reorder, MLA recall, sliding-window
-    survival, recall-sweep and patch-forming workloads (each a parity-tested configuration of
+    """Brief timings of the in-place switch, M-RoPE reorder, re-anchoring, MLA recall,
+    sliding-window survival, recall-sweep and patch-forming workloads (each a parity-tested configuration of
     its own); reported beside the main line."""
     import torch
     import position_independent_multimodal_gb300 as km
@@ -567,6 +567,34 @@ def other_workloads(dev):
         "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
         "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak}
     del w
+    torch.cuda.empty_cache()
+
+    # QV-PIC-style re-anchoring: 18 placements of three unrotated 1024-token images, every
+    # layer, per-token (t, h, w) positions
+    w = wl.config_reanchor(device=dev)
+    lay = w.layout
+    h = km.create(lay)
+    k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_items = km.pack_anchor_items(w.items).to(dev)
+    ms = time_calls(lambda: km.kamera_reanchor(h, d_items, len(w.items), 1024, pool, st), 20,
+                    warmup=3)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    written = sum(it.num_tokens for it in w.items) * lay.num_layers * (lay.row_k + lay.row_v) * 2
+    distinct = {it.chunk_id: it for it in w.items}.values()
+    read = sum(it.num_tokens for it in distinct) * lay.num_layers * (lay.row_k + lay.row_v) * 2 \
+        + sum(it.positions.numel() * 8 for it in w.items)
+    out["reanchor_18_placements"] = {
+        "workload": "QV-PIC-style re-anchoring: three 32 x 32-token images stored before rotation "
+                    "(Qwen2.5-VL layout, 28 layers, H_kv=4 x 128, M-RoPE 16|24|24) placed in all "
+                    "6 orderings, every layer, per-token (t, h, w) positions",
+        "ms_per_call": ms, "gb_s_written": written / ms / 1e6,
+        "frac_hbm_peak": (written + read) / ms / 1e6 / peak}
+    del w, k, v, pool, d_items
     torch.cuda.empty_cache()
 
     w = wl.config3(device=dev)

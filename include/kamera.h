@@ -258,6 +258,42 @@ kamera_status kamera_rope_phases(const kamera_handle *handle, const int64_t *d_d
                                  int32_t num_deltas, float *d_out, kamera_stream_t stream);
 
 /*
+ * Re-anchoring of keys stored before rotation (QV-PIC, "Model-Native Template-Conditioned
+ * Compilation", Eq. 2: K = R(K_bar, P(q)); values are position-independent and stitched as
+ * they are). Each token is rotated from zero to its own absolute position, so there is no
+ * common offset:
+ * canon_k  : bf16 [L][T][row_k] keys before any rotation (MLA: the whole c_KV || k_pe row).
+ * canon_v  : bf16 [L][T][row_v] values (GQA); must be NULL for MLA.
+ * positions: int64, device. 1-D RoPE: [T], the position of each token. M-RoPE layouts:
+ *            [T][3], the (t, h, w) position of each token; a pair of section s turns by
+ *            position[s] times its frequency. Any int64 (the angle is reduced exactly).
+ * num_tokens, req, start_tok: the T tokens go to logical tokens [start_tok, start_tok + T) of
+ *            page-table row req.
+ * canon_k / canon_v 16-byte aligned, positions 8-byte aligned.
+ */
+typedef struct kamera_anchor_item {
+  const void *canon_k;
+  const void *canon_v;
+  const int64_t *positions;
+  int32_t num_tokens;
+  int32_t req;
+  int32_t start_tok;
+  int32_t reserved; /* set to 0 */
+} kamera_anchor_item;
+
+/*
+ * Re-anchors num_items items (a device array of kamera_anchor_item) into the pool in one
+ * launch: rope columns of K rotated per token (one float32 rotation, one rounding to bf16),
+ * the MLA latent and all of V copied byte for byte. Items are checked on the device (the rules
+ * above, plus num_tokens <= max_tokens); a failing item sets KAMERA_DEVICE_BAD_ITEM and is
+ * skipped. Rows whose page falls outside the pool are skipped with KAMERA_DEVICE_SLOT_OOB.
+ * max_tokens sizes the grid. Items must not map tokens to the same slot.
+ */
+kamera_status kamera_reanchor(const kamera_handle *handle, const kamera_anchor_item *d_items,
+                              int32_t num_items, int32_t max_tokens, const kamera_pool *pool,
+                              uint32_t *d_status, kamera_stream_t stream);
+
+/*
  * Patch forming (§3 "Forming and applying the patch"; App. A "form_patch"): for each of
  * num_problems deficits Delta = KV(B|A) - R(delta)KV(B|empty), one (layer, group) each, the
  * top-m factors U*Sigma [T x m] and V_m^T [m x W] in the patch store's bf16 format. The

@@ -19,6 +19,10 @@ Reuse, Eq. 1 in §1 and §3; App. A "Forming and applying the patch"):
   * The result is written into a paged KV pool at the chunk's new slots (§6 "Recompute-free
     on a live engine": SGLang's paged KV pool).
 
+Also: re-anchoring of keys stored before rotation to per-token request positions (QV-PIC,
+"Model-Native Template-Conditioned Compilation", Eq. 2), per-section M-RoPE offsets (Kamera
+Fig. 2), and patch forming from a given deficit (App. A ``form_patch``).
+
 Readings taken where the pages are silent:
   * inv_freq_i = θ^(-2i/d), i < d/2, d = rotary dim (head_dim for GQA/MHA, the 64-dim k_pe band
     for MLA); the angle δ·inv_freq_i is formed in float64 and cos/sin taken in float64.
@@ -384,6 +388,73 @@ def patch_inplace(layout, k_pool, v_pool, page_table, req: int, start_tok: int,
             bits = f64_to_bf16(rows)
             for t, s in enumerate(slots):
                 pool[layer, s, :] = bits[t]
+
+
+# ----------------------------------------------------------------------------------------
+# re-anchoring keys stored before rotation (QV-PIC, Eq. 2)
+# ----------------------------------------------------------------------------------------
+
+def token_offsets(layout, position, npairs: int):
+    """The rotation of every rope pair of one token at an absolute ``position``: one integer
+    under 1-D RoPE; under M-RoPE ``position`` is (t, h, w) and pair k takes the coordinate of
+    its section."""
+    if not has_mrope(layout):
+        return int(position)
+    axes = mrope_pair_axes(npairs, layout.mrope_section, getattr(layout, "mrope_style", 0))
+    coords = [int(v) for v in position]
+    return [coords[a] for a in axes]
+
+
+def reanchor_layer(layout, item, layer: int, channel: int, tokens=None):
+    """Exact result of re-anchoring one (item, layer, channel) before rounding (QV-PIC,
+    "Model-Native Template-Conditioned Compilation", Eq. 2: K = R(K̄, P(q)), keys stored before
+    rotation turned to each token's request position; values position-independent).
+
+    ``item.positions`` holds one position per token ([T], or [T][3] = (t, h, w) under M-RoPE).
+    Token j's rope pairs turn from zero by its own position; values and the MLA latent are
+    copied. Returns (values float64 [t][row], copy_mask bool [row]).
+    """
+    canon = item.canon_k if channel == 0 else item.canon_v
+    rows = np.asarray(canon[layer])
+    pos = np.asarray(item.positions, dtype=np.int64)
+    if tokens is not None:
+        rows = rows[np.asarray(tokens)]
+        pos = pos[np.asarray(tokens)]
+    x = bf16_to_f64(rows)
+    copy_mask = np.ones(x.shape[-1], dtype=bool)
+    if channel == 0:
+        for c0, d in rope_bands(layout):
+            for j in range(x.shape[0]):
+                x[j, c0:c0 + d] = rotate_band(x[j, c0:c0 + d], token_offsets(layout, pos[j], d // 2),
+                                              layout.rope_theta, layout.rope_style)
+            copy_mask[c0:c0 + d] = False
+    return x, copy_mask
+
+
+def reanchor_layer_bits(layout, item, layer: int, channel: int, tokens=None) -> np.ndarray:
+    """bf16 bits re-anchoring writes for one (item, layer, channel): one rounding of the rotated
+    columns, byte copies elsewhere."""
+    vals, copy_mask = reanchor_layer(layout, item, layer, channel, tokens)
+    canon = item.canon_k if channel == 0 else item.canon_v
+    src = np.asarray(canon[layer])
+    if tokens is not None:
+        src = src[np.asarray(tokens)]
+    bits = f64_to_bf16(vals)
+    bits[:, copy_mask] = src[:, copy_mask]
+    return bits
+
+
+def apply_reanchor(layout, item, k_pool, v_pool, page_table) -> None:
+    """Write one re-anchored item into the pools at its slots (all layers, both channels)."""
+    n_layers = len(item.canon_k)
+    for layer in range(n_layers):
+        for channel, pool in ((0, k_pool), (1, v_pool)):
+            if channel == 1 and (layout.kind != GQA or pool is None):
+                continue
+            bits = reanchor_layer_bits(layout, item, layer, channel)
+            for j in range(item.num_tokens):
+                pool[layer][slot_of(page_table, item.req, item.start_tok + j,
+                                    layout.page_size)] = bits[j]
 
 
 # ----------------------------------------------------------------------------------------

@@ -62,6 +62,13 @@ class kamera_pool(ctypes.Structure):
                 ("pt_stride", ctypes.c_int32)]
 
 
+class kamera_anchor_item(ctypes.Structure):
+    _fields_ = [("canon_k", ctypes.c_void_p), ("canon_v", ctypes.c_void_p),
+                ("positions", ctypes.c_void_p), ("num_tokens", ctypes.c_int32),
+                ("req", ctypes.c_int32), ("start_tok", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 ITEM_BYTES = ctypes.sizeof(kamera_item)
 _lib = None
 
@@ -92,6 +99,7 @@ def lib() -> ctypes.CDLL:
                                            vp, i32, i32, i32, i32, vp, vp]
         L.kamera_batch_patch_inplace.argtypes = [vp, vp, i32, i32, i32,
                                                  ctypes.POINTER(kamera_pool), i32, vp, vp]
+        L.kamera_reanchor.argtypes = [vp, vp, i32, i32, ctypes.POINTER(kamera_pool), vp, vp]
         L.kamera_form_patch_workspace.argtypes = [i32, i32, i32, i32]
         L.kamera_form_patch_workspace.restype = ctypes.c_size_t
         L.kamera_form_patch.argtypes = [vp, i64, i64, i32, i32, i32, vp, i64, i32, i32, i32, vp,
@@ -101,7 +109,7 @@ def lib() -> ctypes.CDLL:
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
                   "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed",
                   "kamera_patch_inplace", "kamera_batch_patch_inplace", "kamera_form_patch",
-                  "kamera_form_patch_static_scratch"):
+                  "kamera_form_patch_static_scratch", "kamera_reanchor"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -236,6 +244,24 @@ def kamera_batch_patch_inplace(handle: Handle, d_items: torch.Tensor, num_items:
                                             int(max_tokens), int(max_patch_m), ctypes.byref(p),
                                             int(sign), _ptr(status), _stream(stream)),
            "kamera_batch_patch_inplace")
+
+
+def pack_anchor_items(items: Sequence) -> torch.Tensor:
+    """Objects with canon_k, canon_v, positions (tensors), num_tokens, req, start_tok -> a host
+    uint8 tensor of packed kamera_anchor_item structs."""
+    arr = (kamera_anchor_item * len(items))(*[
+        kamera_anchor_item(_ptr(it.canon_k), _ptr(getattr(it, "canon_v", None)),
+                           _ptr(it.positions), int(it.num_tokens), int(it.req),
+                           int(it.start_tok), 0) for it in items])
+    return torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8)
+
+
+def kamera_reanchor(handle: Handle, d_items: torch.Tensor, num_items: int, max_tokens: int,
+                    pool: Pool, status: torch.Tensor, stream=None) -> None:
+    p = pool.c()
+    _check(lib().kamera_reanchor(handle.ptr, _ptr(d_items), int(num_items), int(max_tokens),
+                                 ctypes.byref(p), _ptr(status), _stream(stream)),
+           "kamera_reanchor")
 
 
 def kamera_rope_phases(handle: Handle, d_deltas: torch.Tensor, d_out: torch.Tensor,

@@ -417,6 +417,28 @@ kamera_status kamera_batch_patch_inplace(const kamera_handle *h, const kamera_it
       kamera::launch_reuse_tile(a, num_items, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kamera_status kamera_reanchor(const kamera_handle *h, const kamera_anchor_item *d_items,
+                              int32_t num_items, int32_t max_tokens, const kamera_pool *pool,
+                              uint32_t *d_status, kamera_stream_t stream) {
+  if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
+  if (num_items < 0 || max_tokens < 0) return KAMERA_ERR_INVALID_ARG;
+  kamera::AnchorArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  if (num_items == 0 || max_tokens == 0) return KAMERA_OK;
+  if (!d_items || (reinterpret_cast<uintptr_t>(d_items) & 7u)) return KAMERA_ERR_INVALID_ARG;
+  if (num_items > 65535 || (long long)h->lay.L * h->lay.n_ch > 65535)
+    return KAMERA_ERR_UNSUPPORTED;
+  a.items = d_items;
+  a.n_items = num_items;
+  a.max_tokens = max_tokens;
+  a.status = d_status;
+  a.freq = h->freq;
+  return from_cuda(kamera::launch_reanchor(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,
                                  int32_t num_deltas, float *d_out, kamera_stream_t stream) {
   if (!h || num_deltas < 0) return KAMERA_ERR_INVALID_ARG;

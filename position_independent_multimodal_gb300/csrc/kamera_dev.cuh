@@ -130,6 +130,15 @@ struct RelocArgs {
   FreqQ64 freq;
 };
 
+struct AnchorArgs {
+  DevLayout lay;
+  DevPool pool;
+  const kamera_anchor_item *items;
+  int n_items, max_tokens;
+  unsigned *status;
+  FreqQ64 freq;
+};
+
 // The rules an item must satisfy (host: kamera_reuse; device: each batch item).
 __host__ __device__ inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -211,6 +220,26 @@ __host__ __device__ __forceinline__ long long pair_delta(const kamera_item &it,
 __host__ __device__ __forceinline__ bool item_rotates(const kamera_item &it,
                                                       const DevLayout &l) {
   return it.delta != 0 || (l.mrope && (it.delta_h != 0 || it.delta_w != 0));
+}
+
+// The rules of a re-anchoring item (checked on the device for every item).
+__host__ __device__ inline int anchor_item_check(const kamera_anchor_item &it,
+                                                 const DevLayout &lay, const DevPool &pool,
+                                                 int max_tokens) {
+  if (it.num_tokens < 0 || it.num_tokens > max_tokens) return KAMERA_ERR_INVALID_ARG;
+  if (it.num_tokens == 0) return 0;
+  if (!it.canon_k || !aligned16(it.canon_k)) return KAMERA_ERR_INVALID_ARG;
+  if (lay.kind == KAMERA_GQA) {
+    if (!it.canon_v || !aligned16(it.canon_v)) return KAMERA_ERR_INVALID_ARG;
+  } else if (it.canon_v) {
+    return KAMERA_ERR_INVALID_ARG;
+  }
+  if (!it.positions || (reinterpret_cast<uintptr_t>(it.positions) & 7u))
+    return KAMERA_ERR_INVALID_ARG;
+  if (it.req < 0 || it.req >= pool.num_reqs || it.start_tok < 0) return KAMERA_ERR_INVALID_ARG;
+  if ((long long)it.start_tok + it.num_tokens > (long long)pool.pt_stride * lay.page_size)
+    return KAMERA_ERR_INVALID_ARG;
+  return 0;
 }
 
 __device__ __forceinline__ bool layer_patched(const kamera_item &it, int layer) {
@@ -407,6 +436,7 @@ SmemPlan reuse_tile_plan(const DevLayout &l, int max_m);
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
+cudaError_t launch_reanchor(const AnchorArgs &a, cudaStream_t s);   // kamera_anchor.cu
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,
                                float *out, cudaStream_t s);
 

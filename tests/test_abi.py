@@ -45,6 +45,7 @@ def test_struct_sizes():
     assert ctypes.sizeof(kb.kamera_item) == 80
     assert ctypes.sizeof(kb.kamera_layout) == 56
     assert ctypes.sizeof(kb.kamera_pool) == 40
+    assert ctypes.sizeof(kb.kamera_anchor_item) == 40
 
 
 def gqa(**kw):
@@ -283,6 +284,24 @@ def test_form_patch_host_checks(lib):
         assert e.value.status == km.KAMERA_ERR_UNSUPPORTED, kw
     # nothing to do: returns OK without touching the device
     call(num_problems=0)
+
+
+def test_reanchor_host_checks(lib):
+    h = km.create(gqa())
+    d = FakeTensor(0x90000)
+    for args in [(-1, 16), (1, -1)]:
+        with pytest.raises(km.KameraError) as e:
+            km.kamera_reanchor(h, d, args[0], args[1], fake_pool(), STATUS, stream=0)
+        assert e.value.status == km.KAMERA_ERR_INVALID_ARG
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_reanchor(h, FakeTensor(0x90004), 1, 16, fake_pool(), STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_INVALID_ARG
+    with pytest.raises(km.KameraError) as e:
+        km.kamera_reanchor(h, d, 70000, 16, fake_pool(), STATUS, stream=0)
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+    # nothing to do: returns OK without touching the device
+    km.kamera_reanchor(h, d, 0, 16, fake_pool(), STATUS, stream=0)
+    km.kamera_reanchor(h, d, 3, 0, fake_pool(), STATUS, stream=0)
 
 
 def test_status_strings(lib):

@@ -687,6 +687,80 @@ def test_mrope_offsets_compose_per_section():
     np.testing.assert_allclose(two, one, atol=1e-9)
 
 
+# ------------------------------------------------------------------------------------------
+# re-anchoring keys stored before rotation (QV-PIC, Eq. 2)
+# ------------------------------------------------------------------------------------------
+
+def anchor_item(layout, T, positions, seed=0):
+    rng = np.random.default_rng(seed)
+    row = layout.num_kv_heads * layout.head_dim if layout.kind == ora.GQA else \
+        layout.latent_dim + layout.rope_dim
+    k = ora.f64_to_bf16(rng.standard_normal((1, T, row)))
+    v = ora.f64_to_bf16(rng.standard_normal((1, T, row))) if layout.kind == ora.GQA else None
+    from types import SimpleNamespace
+    return SimpleNamespace(canon_k=k, canon_v=v, positions=np.asarray(positions), num_tokens=T,
+                           req=0, start_tok=0)
+
+
+def test_reanchor_turns_each_token_by_its_own_position():
+    lay = ns_layout(num_kv_heads=2, head_dim=16, rope_dim=16)
+    pos = [0, 5, -3, 1 << 20, 77]
+    it = anchor_item(lay, len(pos), pos)
+    vals, mask = ora.reanchor_layer(lay, it, 0, 0)
+    assert not mask.any()
+    x = ora.bf16_to_f64(it.canon_k[0])
+    d = 16
+    for j, p in enumerate(pos):
+        for h in range(2):
+            for k in range(d // 2):
+                z = complex(x[j, h * d + k], x[j, h * d + k + d // 2]) * \
+                    cmath.exp(1j * p * 1e4 ** (-2.0 * k / d))
+                assert abs(vals[j, h * d + k] - z.real) <= 1e-12
+                assert abs(vals[j, h * d + k + d // 2] - z.imag) <= 1e-12
+    assert np.array_equal(vals[0], x[0])                      # position 0: unchanged
+    vbits = ora.reanchor_layer_bits(lay, it, 0, 1)
+    assert np.array_equal(vbits, it.canon_v[0])               # values: byte copies
+
+
+def test_reanchor_mrope_coordinates():
+    sec = (16, 24, 24)
+    lay = mrope_layout(ora.MROPE_CONTIGUOUS, sec, heads=1)
+    flat = mrope_layout(ora.MROPE_CONTIGUOUS, (0, 0, 0), heads=1)
+    pos3 = [(3, 40, 41), (0, 0, 0), (1000, -5, 7)]
+    it = anchor_item(lay, 3, pos3)
+    vals, _ = ora.reanchor_layer(lay, it, 0, 0)
+    x = ora.bf16_to_f64(it.canon_k[0])
+    axes = ora.mrope_pair_axes(64, sec, ora.MROPE_CONTIGUOUS)
+    for j, p in enumerate(pos3):
+        for k in (0, 15, 16, 39, 40, 63):
+            z = complex(x[j, k], x[j, k + 64]) * cmath.exp(1j * p[axes[k]] * 1e6 ** (-k / 64))
+            assert abs(vals[j, k] - z.real) <= 1e-12 and abs(vals[j, k + 64] - z.imag) <= 1e-12
+    # equal coordinates: 1-D RoPE at that position, bit for bit
+    same = anchor_item(lay, 3, [(p, p, p) for p in (9, -2, 123456)], seed=1)
+    flat_it = anchor_item(flat, 3, [9, -2, 123456], seed=1)
+    assert np.array_equal(ora.reanchor_layer_bits(lay, same, 0, 0),
+                          ora.reanchor_layer_bits(flat, flat_it, 0, 0))
+
+
+def test_reanchor_then_relocate_is_reanchor_at_moved_positions():
+    # R(δ) R(P) K̄ = R(P + δ) K̄: Kamera's relocation of a re-anchored key moves its anchor
+    lay = ns_layout(num_kv_heads=1, head_dim=32, rope_dim=32)
+    pos = np.array([4, 100, -7, 65536])
+    it = anchor_item(lay, 4, pos)
+    moved = anchor_item(lay, 4, pos + 999)
+    a, _ = ora.reanchor_layer(lay, it, 0, 0)
+    b, _ = ora.reanchor_layer(lay, moved, 0, 0)
+    np.testing.assert_allclose(ora.rotate_band(a, 999, 1e4, ora.NEOX_HALF), b, atol=1e-9)
+
+
+def test_reanchor_mla_rotates_only_k_pe():
+    lay = ns_layout(kind=ora.MLA, num_kv_heads=0, head_dim=0, latent_dim=32, rope_dim=16)
+    it = anchor_item(lay, 3, [1, 2, 3])
+    bits = ora.reanchor_layer_bits(lay, it, 0, 0)
+    assert np.array_equal(bits[:, :32], it.canon_k[0][:, :32])
+    assert not np.array_equal(bits[:, 32:], it.canon_k[0][:, 32:])
+
+
 def test_patch_byte_fraction_matches_printed_values():
     with open(os.path.join(GOLDEN, "patch_fraction.txt")) as f:
         rows = [l.split("|")[0] for l in f if l.strip() and not l.startswith("#")]

@@ -94,6 +94,18 @@ class Item:
 
 
 @dataclasses.dataclass
+class AnchorItem:
+    """One placement of keys stored before rotation, re-anchored at per-token positions."""
+    canon_k: torch.Tensor                 # bf16 [L][T][row_k], unrotated keys
+    canon_v: Optional[torch.Tensor]       # bf16 [L][T][row_v] (GQA) or None (MLA)
+    positions: torch.Tensor               # int64 [T] (1-D RoPE) or [T][3] (t, h, w; M-RoPE)
+    num_tokens: int
+    req: int
+    start_tok: int
+    chunk_id: int = -1
+
+
+@dataclasses.dataclass
 class Span:
     """A run of tokens already in the pool, to be relocated in place (survivors)."""
     req: int
@@ -280,6 +292,56 @@ def config2_mrope(seed: int = 0, device="cpu") -> Workload:
     items = [dataclasses.replace(it, delta_h=(it.delta // 1024) * 16,
                                  delta_w=(it.delta // 1024) * 16) for it in w.items]
     return dataclasses.replace(w, name="cfg2_mrope", layout=lay, items=items)
+
+
+def image_positions(layout: Layout, base: int, grid) -> torch.Tensor:
+    """Request positions of the tokens of one image or video segment placed at ``base``:
+    [T] = base + token index under 1-D RoPE; [T][3] = (base + frame, base + row, base + col)
+    for a (frames, rows, cols) grid of merged tokens under M-RoPE (Fig. 2 (a): every merged
+    token gets a (t, h, w) coordinate)."""
+    f, r, c = grid
+    if not any(layout.mrope_section):
+        return base + torch.arange(f * r * c, dtype=torch.int64)
+    ft, rt, ct = torch.meshgrid(torch.arange(f), torch.arange(r), torch.arange(c), indexing="ij")
+    return base + torch.stack([ft, rt, ct], dim=-1).reshape(-1, 3).to(torch.int64)
+
+
+def anchor_workload(name: str, layout: Layout, *, grids, placements, seed: int = 0,
+                    device="cpu", extra_pages: int = 0) -> Workload:
+    """Keys stored before rotation (one per grid), placed by ``placements`` =
+    [(chunk, req, start_tok, base_position)] and re-anchored at their request positions."""
+    g = _gen(device, seed, name, "canon")
+    Ts = [f * r * c for f, r, c in grids]
+    canon_k = [normal_bf16((layout.num_layers, T, layout.row_k), 1.0, g, device) for T in Ts]
+    canon_v = [normal_bf16((layout.num_layers, T, layout.row_v), 1.0, g, device)
+               if layout.kind == GQA else None for T in Ts]
+    reqs = max(p[1] for p in placements) + 1
+    end = max(p[2] + Ts[p[0]] for p in placements)
+    pages_per_req = (end + layout.page_size - 1) // layout.page_size + extra_pages
+    pt = shuffled_page_table(reqs, pages_per_req, _gen("cpu", seed, name, "pages"))
+    items = [AnchorItem(canon_k=canon_k[c], canon_v=canon_v[c],
+                        positions=image_positions(layout, base, grids[c]).to(device),
+                        num_tokens=Ts[c], req=r, start_tok=s, chunk_id=c)
+             for c, r, s, base in placements]
+    return Workload(name=name, layout=layout, items=items, page_table=pt,
+                    num_slots=reqs * pages_per_req * layout.page_size)
+
+
+def config_reanchor(seed: int = 0, device="cpu") -> Workload:
+    """QV-PIC-style re-anchoring on the reorder shape: Qwen2.5-VL layout (28 layers, H_kv=4 x
+    128, θ=1e6, M-RoPE 16|24|24), three rendered images of 32 x 32 merged tokens (T = 1024)
+    stored before rotation, placed in all 6 orderings (18 placements) after a 16-token prefix;
+    the image at ordering position j starts at position 16 + 33·j (an image spans 32 rows /
+    columns, and the next starts one past its largest coordinate)."""
+    lay = Layout(kind=GQA, num_layers=28, page_size=16, num_kv_heads=4, head_dim=128,
+                 rope_dim=128, rope_style=NEOX_HALF, rope_theta=1e6, mrope_section=(16, 24, 24),
+                 mrope_style=MROPE_CONTIGUOUS)
+    placements = []
+    for r, perm in enumerate(itertools.permutations(range(3))):
+        for j, c in enumerate(perm):
+            placements.append((c, r, 16 + j * 1024, 16 + 33 * j))
+    return anchor_workload("reanchor", lay, grids=[(1, 32, 32)] * 3, placements=placements,
+                           seed=seed, device=device)
 
 
 def config3(seed: int = 0, device="cpu", n_chunks: int = 64) -> Workload:
