@@ -294,6 +294,41 @@ kamera_status kamera_reanchor(const kamera_handle *handle, const kamera_anchor_i
                               uint32_t *d_status, kamera_stream_t stream);
 
 /*
+ * Decode attention over the paged pool: the consumer-side check that the rows the other calls
+ * write are the KV an attention kernel reads (§1: attention over KV(A) || KV(B) equals
+ * attending each part separately and merging by softmax mass, o = (1 - mu) o_B + mu o_A, the
+ * log-sum-exp merge of FlashAttention). One query token per request and query head:
+ *   s_t = scale * q . K_t,  o = sum_t softmax(s)_t V_t,  lse = log sum_t exp(s_t),
+ * over the request's logical tokens [0, ctx_len[r]) of pool layer `layer`, gathered through
+ * page-table row r. The context is cut into splits of 256 tokens; each split's (o, lse) is
+ * computed independently and the splits are merged by their log-sum-exp.
+ *   GQA: K_t, V_t = head (h / (num_q_heads / num_kv_heads)) of the K and V rows; Dk = Dv =
+ *        head_dim; num_q_heads a multiple of num_kv_heads.
+ *   MLA: the absorbed form: K_t = the whole c_KV || k_pe row (Dk = latent + rope), V_t = its
+ *        c_KV part (Dv = latent); every query head reads the one latent head.
+ * d_q      : bf16 [num_reqs][num_q_heads][Dk], device.
+ * d_ctx_len: int32 [num_reqs], device; each in [0, max_ctx] (a larger one sets
+ *            KAMERA_DEVICE_BAD_ITEM and that request's outputs are not written).
+ * d_out    : float32 [num_reqs][num_q_heads][Dv]; d_lse: float32 [num_reqs][num_q_heads]
+ *            (natural log). An empty context gives o = 0 and lse = -inf.
+ * d_workspace: at least kamera_decode_attention_workspace(handle, num_reqs, num_q_heads,
+ *            max_ctx) bytes of device memory, 4-byte aligned (0 bytes when max_ctx is 0);
+ *            contents ignored and left undefined.
+ * Requests are page-table rows 0 .. num_reqs - 1 (num_reqs <= the pool's num_reqs).
+ * Pages outside the pool set KAMERA_DEVICE_SLOT_OOB and their tokens are left out. Limits:
+ * num_q_heads <= 256 (GQA: a multiple of num_kv_heads), Dk <= 1024.
+ */
+size_t kamera_decode_attention_workspace(const kamera_handle *handle, int32_t num_reqs,
+                                         int32_t num_q_heads, int32_t max_ctx);
+
+kamera_status kamera_decode_attention(const kamera_handle *handle, const kamera_pool *pool,
+                                      int32_t layer, const void *d_q, int32_t num_reqs,
+                                      int32_t num_q_heads, const int32_t *d_ctx_len,
+                                      int32_t max_ctx, float scale, float *d_out, float *d_lse,
+                                      void *d_workspace, size_t workspace_bytes,
+                                      uint32_t *d_status, kamera_stream_t stream);
+
+/*
  * Patch forming (§3 "Forming and applying the patch"; App. A "form_patch"): for each of
  * num_problems deficits Delta = KV(B|A) - R(delta)KV(B|empty), one (layer, group) each, the
  * top-m factors U*Sigma [T x m] and V_m^T [m x W] in the patch store's bf16 format. The

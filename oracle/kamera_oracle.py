@@ -458,6 +458,74 @@ def apply_reanchor(layout, item, k_pool, v_pool, page_table) -> None:
 
 
 # ----------------------------------------------------------------------------------------
+# consumer check: decode attention over the pool (§1, the log-sum-exp readout merge)
+# ----------------------------------------------------------------------------------------
+
+def attend(k, v, q, scale: float):
+    """Attention of one query over key rows ``k`` [T][Dk] and value rows ``v`` [T][Dv], float64:
+    s = scale·k q, o = softmax(s)·v, lse = log Σ_t exp(s_t). No keys: o = 0, lse = -inf."""
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    if k.shape[0] == 0:
+        return np.zeros(v.shape[-1]), -np.inf
+    s = scale * (k @ np.asarray(q, np.float64))
+    m = np.max(s)
+    p = np.exp(s - m)
+    return (p @ v) / np.sum(p), m + np.log(np.sum(p))
+
+
+def lse_merge(parts):
+    """Attention over the union of disjoint key sets from each set's (o, lse): weights
+    exp(lse_s - lse) with lse = log Σ_s exp(lse_s) (§1: attention over KV(A) ‖ KV(B) equals
+    attending each part and merging by softmax mass, o = (1 - μ) o_B + μ o_A)."""
+    lses = np.array([l for _, l in parts], dtype=np.float64)
+    if len(parts) == 0 or np.all(np.isneginf(lses)):
+        dv = parts[0][0].shape[-1] if parts else 0
+        return np.zeros(dv), -np.inf
+    m = np.max(lses)
+    w = np.exp(lses - m)
+    o = sum(wi * np.asarray(oi, np.float64) for wi, (oi, _) in zip(w, parts)) / np.sum(w)
+    return o, m + np.log(np.sum(w))
+
+
+def head_columns(layout, h: int, num_q_heads: int):
+    """Columns of query head h's key and value in the pool rows: ((k0, dk), (v0, dv), channel of
+    V). GQA/MHA: head h // (H_q / H_kv) of the K and V rows. MLA (absorbed form): K is the whole
+    c_KV ‖ k_pe row and V its c_KV part, both in channel 0."""
+    if layout.kind == GQA:
+        group = num_q_heads // layout.num_kv_heads
+        c0 = (h // group) * layout.head_dim
+        return (c0, layout.head_dim), (c0, layout.head_dim), 1
+    return (0, layout.latent_dim + layout.rope_dim), (0, layout.latent_dim), 0
+
+
+def decode_attention(layout, k_pool, v_pool, page_table, req: int, ctx_len: int, q,
+                     scale: float, layer: int):
+    """One query token per query head attending over logical tokens [0, ctx_len) of page-table
+    row ``req`` in pool layer ``layer``. ``q`` [H_q][Dk] (values); pools hold bf16 bits.
+    Returns (o [H_q][Dv], lse [H_q])."""
+    q = np.asarray(q, np.float64)
+    hq = q.shape[0]
+    slots = [slot_of(page_table, req, t, layout.page_size) for t in range(ctx_len)]
+    krows = bf16_to_f64(np.asarray(k_pool[layer])[slots]) if slots else None
+    vrows = None
+    if layout.kind == GQA and slots:
+        vrows = bf16_to_f64(np.asarray(v_pool[layer])[slots])
+    outs, lses = [], []
+    for h in range(hq):
+        (k0, dk), (v0, dv), vch = head_columns(layout, h, hq)
+        if not slots:
+            outs.append(np.zeros(dv))
+            lses.append(-np.inf)
+            continue
+        src_v = vrows if vch == 1 else krows
+        o, l = attend(krows[:, k0:k0 + dk], src_v[:, v0:v0 + dv], q[h], scale)
+        outs.append(o)
+        lses.append(l)
+    return np.array(outs), np.array(lses)
+
+
+# ----------------------------------------------------------------------------------------
 # compile side, for the pins only (App. A ``form_patch``)
 # ----------------------------------------------------------------------------------------
 

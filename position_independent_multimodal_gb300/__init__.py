@@ -12,7 +12,8 @@ from ._binding import (  # noqa: F401
     KAMERA_ROPE_INTERLEAVED, KAMERA_ROPE_NEOX_HALF, LIB_PATH, Handle, KameraError, Pool,
     create, kamera_batch_patch_inplace, kamera_batch_reuse, kamera_batch_reuse_timed,
     kamera_form_patch, kamera_form_patch_static_scratch, kamera_form_patch_workspace,
-    kamera_patch_inplace, kamera_reanchor, pack_anchor_items, kamera_relocate,
+    kamera_decode_attention, kamera_decode_attention_workspace, kamera_patch_inplace,
+    kamera_reanchor, pack_anchor_items, kamera_relocate,
     kamera_reuse, kamera_rope_phases, lib, make_item, make_layout,
     pack_items, status_string,
 )

@@ -100,6 +100,11 @@ def lib() -> ctypes.CDLL:
         L.kamera_batch_patch_inplace.argtypes = [vp, vp, i32, i32, i32,
                                                  ctypes.POINTER(kamera_pool), i32, vp, vp]
         L.kamera_reanchor.argtypes = [vp, vp, i32, i32, ctypes.POINTER(kamera_pool), vp, vp]
+        L.kamera_decode_attention_workspace.argtypes = [vp, i32, i32, i32]
+        L.kamera_decode_attention_workspace.restype = ctypes.c_size_t
+        L.kamera_decode_attention.argtypes = [vp, ctypes.POINTER(kamera_pool), i32, vp, i32, i32,
+                                              vp, i32, ctypes.c_float, vp, vp, vp,
+                                              ctypes.c_size_t, vp, vp]
         L.kamera_form_patch_workspace.argtypes = [i32, i32, i32, i32]
         L.kamera_form_patch_workspace.restype = ctypes.c_size_t
         L.kamera_form_patch.argtypes = [vp, i64, i64, i32, i32, i32, vp, i64, i32, i32, i32, vp,
@@ -109,7 +114,8 @@ def lib() -> ctypes.CDLL:
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
                   "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed",
                   "kamera_patch_inplace", "kamera_batch_patch_inplace", "kamera_form_patch",
-                  "kamera_form_patch_static_scratch", "kamera_reanchor"):
+                  "kamera_form_patch_static_scratch", "kamera_reanchor",
+                  "kamera_decode_attention"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -262,6 +268,29 @@ def kamera_reanchor(handle: Handle, d_items: torch.Tensor, num_items: int, max_t
     _check(lib().kamera_reanchor(handle.ptr, _ptr(d_items), int(num_items), int(max_tokens),
                                  ctypes.byref(p), _ptr(status), _stream(stream)),
            "kamera_reanchor")
+
+
+def kamera_decode_attention_workspace(handle: Handle, num_reqs: int, num_q_heads: int,
+                                      max_ctx: int) -> int:
+    return int(lib().kamera_decode_attention_workspace(handle.ptr, int(num_reqs),
+                                                       int(num_q_heads), int(max_ctx)))
+
+
+def kamera_decode_attention(handle: Handle, pool: Pool, layer: int, q: torch.Tensor,
+                            ctx_len: torch.Tensor, max_ctx: int, scale: float,
+                            out: torch.Tensor, lse: torch.Tensor,
+                            workspace: Optional[torch.Tensor], status: torch.Tensor,
+                            stream=None) -> None:
+    """Decode attention of ``q`` [R][H_q][Dk] over pool layer ``layer`` (requests = page-table
+    rows 0..R-1, contexts ``ctx_len`` int32 [R]) into ``out`` float32 [R][H_q][Dv] and ``lse``
+    float32 [R][H_q]."""
+    p = pool.c()
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kamera_decode_attention(handle.ptr, ctypes.byref(p), int(layer), _ptr(q),
+                                         int(q.shape[0]), int(q.shape[1]), _ptr(ctx_len),
+                                         int(max_ctx), float(scale), _ptr(out), _ptr(lse),
+                                         _ptr(workspace), int(nbytes), _ptr(status),
+                                         _stream(stream)), "kamera_decode_attention")
 
 
 def kamera_rope_phases(handle: Handle, d_deltas: torch.Tensor, d_out: torch.Tensor,

@@ -439,6 +439,61 @@ kamera_status kamera_reanchor(const kamera_handle *h, const kamera_anchor_item *
   return from_cuda(kamera::launch_reanchor(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t kamera_decode_attention_workspace(const kamera_handle *h, int32_t num_reqs,
+                                         int32_t num_q_heads, int32_t max_ctx) {
+  if (!h || num_reqs < 0 || num_q_heads < 0 || max_ctx < 0) return 0;
+  const int dv = h->lay.kind == KAMERA_GQA ? h->lay.hd : h->lay.latent;
+  return kamera::attn_workspace(num_reqs, num_q_heads, max_ctx, dv);
+}
+
+kamera_status kamera_decode_attention(const kamera_handle *h, const kamera_pool *pool,
+                                      int32_t layer, const void *d_q, int32_t num_reqs,
+                                      int32_t num_q_heads, const int32_t *d_ctx_len,
+                                      int32_t max_ctx, float scale, float *d_out, float *d_lse,
+                                      void *d_workspace, size_t workspace_bytes,
+                                      uint32_t *d_status, kamera_stream_t stream) {
+  if (!h || !d_status) return KAMERA_ERR_INVALID_ARG;
+  kamera::AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.lay = h->lay;
+  kamera_status st = check_pool(h->lay, pool, &a.pool);
+  if (st != KAMERA_OK) return st;
+  const kamera::DevLayout &l = h->lay;
+  if (layer < 0 || layer >= l.L || num_reqs < 0 || num_q_heads < 1 || max_ctx < 0)
+    return KAMERA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KAMERA_ERR_INVALID_ARG;
+  if (num_q_heads > 256) return KAMERA_ERR_UNSUPPORTED;
+  if (l.kind == KAMERA_GQA && num_q_heads % l.H != 0) return KAMERA_ERR_INVALID_ARG;
+  const int dk = l.kind == KAMERA_GQA ? l.hd : l.latent + l.rope_d;
+  const int dv = l.kind == KAMERA_GQA ? l.hd : l.latent;
+  if (dk > 1024 || (dv & 7) != 0) return KAMERA_ERR_UNSUPPORTED;
+  if (num_reqs > a.pool.num_reqs) return KAMERA_ERR_INVALID_ARG;
+  if (num_reqs > 65535) return KAMERA_ERR_UNSUPPORTED;
+  if (num_reqs == 0) return KAMERA_OK;
+  auto mis = [](const void *p, uintptr_t al) { return !p || (reinterpret_cast<uintptr_t>(p) & (al - 1)); };
+  if (mis(d_q, 2) || mis(d_ctx_len, 4) || mis(d_out, 4) || mis(d_lse, 4))
+    return KAMERA_ERR_INVALID_ARG;
+  const size_t need = kamera::attn_workspace(num_reqs, num_q_heads, max_ctx, dv);
+  if (need > 0 && (mis(d_workspace, 4) || workspace_bytes < need)) return KAMERA_ERR_INVALID_ARG;
+  a.layer = layer;
+  a.q = static_cast<const __nv_bfloat16 *>(d_q);
+  a.ctx_len = d_ctx_len;
+  a.n_reqs = num_reqs;
+  a.hq = num_q_heads;
+  a.dk = dk;
+  a.dv = dv;
+  a.max_ctx = max_ctx;
+  a.split = kamera::attn_split_tokens(l);
+  a.n_splits = (max_ctx + a.split - 1) / a.split;
+  a.scale = scale;
+  a.part_o = static_cast<float *>(d_workspace);
+  a.part_lse = a.part_o + (size_t)num_reqs * num_q_heads * a.n_splits * dv;
+  a.out = d_out;
+  a.lse = d_lse;
+  a.status = d_status;
+  return from_cuda(kamera::launch_attention(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas,
                                  int32_t num_deltas, float *d_out, kamera_stream_t stream) {
   if (!h || num_deltas < 0) return KAMERA_ERR_INVALID_ARG;

@@ -139,6 +139,20 @@ struct AnchorArgs {
   FreqQ64 freq;
 };
 
+struct AttnArgs {
+  DevLayout lay;
+  DevPool pool;
+  int layer;
+  const __nv_bfloat16 *q;  // [n_reqs][hq][dk]
+  const int *ctx_len;      // [n_reqs]
+  int n_reqs, hq, dk, dv, max_ctx, n_splits;
+  int split;               // tokens per split (the kernel's; n_splits = ceil(max_ctx / split))
+  float scale;
+  float *part_o, *part_lse;  // workspace: [n_reqs][hq][n_splits][dv], [n_reqs][hq][n_splits]
+  float *out, *lse;          // [n_reqs][hq][dv], [n_reqs][hq]
+  unsigned *status;
+};
+
 // The rules an item must satisfy (host: kamera_reuse; device: each batch item).
 __host__ __device__ inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -437,6 +451,10 @@ cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
 cudaError_t launch_reanchor(const AnchorArgs &a, cudaStream_t s);   // kamera_anchor.cu
+size_t attn_workspace(long long n_reqs, int hq, int max_ctx, int dv);  // kamera_attn.cu
+size_t attn_smem(int dk, int dv);
+int attn_split_tokens(const DevLayout &l);
+cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_rope_phases(const FreqQ64 &f, int npairs, const long long *deltas, int n,
                                float *out, cudaStream_t s);
 

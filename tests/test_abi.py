@@ -304,6 +304,37 @@ def test_reanchor_host_checks(lib):
     km.kamera_reanchor(h, d, 3, 0, fake_pool(), STATUS, stream=0)
 
 
+def test_decode_attention_host_checks(lib):
+    h = km.create(gqa())  # H_kv = 2, head_dim = 64
+    q = FakeTensor(0xA0000, shape=(3, 4, 64))
+    ctx = FakeTensor(0xB0000)
+    out, lse, ws = FakeTensor(0xC0000), FakeTensor(0xD0000), FakeWorkspace(0xE0000, 1 << 20)
+    need = km.kamera_decode_attention_workspace(h, 3, 4, 600)
+    assert need == 3 * 4 * 3 * (64 + 1) * 4  # splits of 256 tokens: ceil(600 / 256) = 3
+    assert km.kamera_decode_attention_workspace(h, 3, 4, 0) == 0
+
+    def call(**kw):
+        a = dict(layer=0, q=q, ctx=ctx, max_ctx=600, scale=0.125, out=out, lse=lse, ws=ws)
+        a.update(kw)
+        km.kamera_decode_attention(h, fake_pool(reqs=4), a["layer"], a["q"], a["ctx"], a["max_ctx"],
+                                   a["scale"], a["out"], a["lse"], a["ws"], STATUS, stream=0)
+
+    invalid = [dict(layer=-1), dict(layer=2), dict(max_ctx=-1), dict(scale=float("nan")),
+               dict(q=FakeTensor(0xA0000, shape=(3, 3, 64))),      # 3 heads over 2 KV heads
+               dict(q=FakeTensor(0xA0001, shape=(3, 4, 64))), dict(ctx=FakeTensor(0xB0002)),
+               dict(out=FakeTensor(0xC0002)), dict(lse=FakeTensor(0xD0001)),
+               dict(ws=FakeWorkspace(0xE0000, need - 4)), dict(ws=None),
+               dict(q=FakeTensor(0xA0000, shape=(9, 4, 64)))]     # more requests than rows
+    for kw in invalid:
+        with pytest.raises(km.KameraError) as e:
+            call(**kw)
+        assert e.value.status == km.KAMERA_ERR_INVALID_ARG, kw
+    with pytest.raises(km.KameraError) as e:
+        call(q=FakeTensor(0xA0000, shape=(3, 258, 64)))
+    assert e.value.status == km.KAMERA_ERR_UNSUPPORTED
+    call(q=FakeTensor(0xA0000, shape=(0, 4, 64)))  # no requests: nothing launched
+
+
 def test_status_strings(lib):
     for s in range(4):
         assert km.status_string(s)

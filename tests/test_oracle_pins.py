@@ -761,6 +761,81 @@ def test_reanchor_mla_rotates_only_k_pe():
     assert not np.array_equal(bits[:, 32:], it.canon_k[0][:, 32:])
 
 
+# ------------------------------------------------------------------------------------------
+# consumer check: decode attention and the log-sum-exp merge (§1)
+# ------------------------------------------------------------------------------------------
+
+def test_attention_of_a_union_is_the_lse_merge_of_its_parts():
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((50, 16))
+    v = rng.standard_normal((50, 8))
+    q = rng.standard_normal(16)
+    whole = ora.attend(k, v, q, 0.3)
+    for cut in ((20,), (1, 49), (10, 11, 30)):
+        bounds = (0,) + cut + (50,)
+        parts = [ora.attend(k[a:b], v[a:b], q, 0.3) for a, b in zip(bounds[:-1], bounds[1:])]
+        o, l = ora.lse_merge(parts)
+        np.testing.assert_allclose(o, whole[0], atol=1e-12)
+        assert abs(l - whole[1]) <= 1e-12
+    # the two-part form printed on the page: o = (1 - mu) o_B + mu o_A, mu = A's softmax mass
+    (oa, la), (ob, lb) = ora.attend(k[:20], v[:20], q, 0.3), ora.attend(k[20:], v[20:], q, 0.3)
+    mu = math.exp(la) / (math.exp(la) + math.exp(lb))
+    np.testing.assert_allclose((1 - mu) * ob + mu * oa, whole[0], atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(22)
+    v = rng.standard_normal((7, 5))
+    # one key: the output is its value, lse its score
+    o, l = ora.attend(np.ones((1, 3)), v[:1], np.array([1.0, 2.0, 3.0]), 0.5)
+    np.testing.assert_array_equal(o, v[0])
+    assert l == 3.0
+    # equal scores: the mean of the values, lse = s + log T
+    o, l = ora.attend(np.zeros((7, 3)), v, np.ones(3), 1.0)
+    np.testing.assert_allclose(o, v.mean(axis=0), atol=1e-15)
+    assert abs(l - math.log(7)) <= 1e-15
+    # a dominant key takes all the mass; an empty context gives (0, -inf)
+    k = np.zeros((7, 2))
+    k[4] = [100.0, 0.0]
+    o, _ = ora.attend(k, v, np.array([1.0, 0.0]), 1.0)
+    np.testing.assert_allclose(o, v[4], atol=1e-30)
+    o, l = ora.attend(np.zeros((0, 2)), np.zeros((0, 5)), np.ones(2), 1.0)
+    assert np.all(o == 0) and l == -np.inf
+    o, l = ora.lse_merge([(np.zeros(5), -np.inf), (np.zeros(5), -np.inf)])
+    assert np.all(o == 0) and l == -np.inf
+
+
+def test_decode_attention_gathers_heads_and_pages():
+    # brute force on a tiny pool: GQA head grouping and the MLA absorbed form against explicit
+    # loops over tokens
+    rng = np.random.default_rng(23)
+    pt = np.array([[2, 0], [1, 3]])
+    gqa = ns_layout(num_kv_heads=2, head_dim=4, rope_dim=4, page_size=2)
+    kp = ora.f64_to_bf16(rng.standard_normal((1, 8, 8)))
+    vp = ora.f64_to_bf16(rng.standard_normal((1, 8, 8)))
+    q = rng.standard_normal((4, 4))
+    o, l = ora.decode_attention(gqa, kp, vp, pt, 1, 3, q, 0.5, 0)
+    slots = [1 * 2 + 0, 1 * 2 + 1, 3 * 2 + 0]
+    for h in range(4):
+        kvh = h // 2
+        s = [0.5 * sum(ora.bf16_to_f64(kp[0][t][kvh * 4 + d]) * q[h][d] for d in range(4))
+             for t in slots]
+        w = [math.exp(x - max(s)) for x in s]
+        for d in range(4):
+            ref = sum(wi * ora.bf16_to_f64(vp[0][t][kvh * 4 + d]) for wi, t in zip(w, slots)) / sum(w)
+            assert abs(o[h][d] - ref) <= 1e-12
+        assert abs(l[h] - (max(s) + math.log(sum(w)))) <= 1e-12
+    mla = ns_layout(kind=ora.MLA, num_kv_heads=0, head_dim=0, latent_dim=4, rope_dim=2,
+                    page_size=2)
+    kp = ora.f64_to_bf16(rng.standard_normal((1, 8, 6)))
+    qm = rng.standard_normal((3, 6))
+    o, l = ora.decode_attention(mla, kp, None, pt, 0, 4, qm, 1.0, 0)
+    rows = ora.bf16_to_f64(kp[0][[4, 5, 0, 1]])
+    for h in range(3):
+        ref_o, ref_l = ora.attend(rows, rows[:, :4], qm[h], 1.0)
+        np.testing.assert_allclose(o[h], ref_o, atol=1e-12)
+
+
 def test_patch_byte_fraction_matches_printed_values():
     with open(os.path.join(GOLDEN, "patch_fraction.txt")) as f:
         rows = [l.split("|")[0] for l in f if l.strip() and not l.startswith("#")]
