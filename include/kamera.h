@@ -343,7 +343,7 @@ kamera_status kamera_decode_attention(const kamera_handle *handle, const kamera_
  *   d_omega     : float32 [W][k] random test matrix of problem i at d_omega + i*omega_stride
  *                 (omega_stride 0: one matrix for all problems), drawn by the caller.
  *   k           : sketch width, m <= k <= min(T, W, 96), with
- *                 4 * (2112 + 3072 + 3k^2 + kW + 3k) <= 232448 (shared memory of the kernel).
+ *                 4 * (14400 + 3k^2 + kW + 3k) <= 232448 (shared memory of the kernel).
  *   q           : power iterations, 0..16.   m : rank kept, 1..k.
  *   d_u, d_vt   : bf16 outputs, problem i's U*Sigma [T][m] at d_u + i*u_stride and V_m^T
  *                 [m][W] at d_vt + i*vt_stride (elements). The strides place the results

@@ -37,12 +37,13 @@ namespace {
 
 constexpr int kThr = 256;
 constexpr int kWarps = kThr / 32;
-constexpr int kTM = 64, kTK = 32;  // GEMM tile: 64 rows of C per block, K in steps of 32
-constexpr int kAPitch = kTK + 1;   // padded op(A) tile rows
+constexpr int kBM = 128, kBK = 32;  // GEMM: 128 rows of C per block, K in steps of 32
+constexpr int kAPitch = kBM + 1;    // op(A) tile [kBK][kAPitch]: conflict-free stores and reads
+constexpr int kStageF = kBK * kAPitch + kBK * kMaxSketch;  // floats of one GEMM stage
 
 // Float offsets of the dynamic shared memory (one plan for host and device).
 struct FormPlan {
-  int ta, tb;    // GEMM tiles: op(A) [kTM][kAPitch], B [kTK][kMaxSketch]
+  int tiles;     // GEMM: two stages of op(A) [kBK][kAPitch] and B [kBK][kMaxSketch]
   int g, r;      // k × k: Gram matrix / Cholesky factor, and the triangular inverse
   int v;         // k × k: Jacobi rotations Ũ, column-major
   int bc;        // W × k: Bᵀ, column-major (column j at bc + j*W)
@@ -55,10 +56,8 @@ struct FormPlan {
 __host__ __device__ inline FormPlan form_plan(int W, int k) {
   FormPlan p;
   int o = 0;
-  p.ta = o;
-  o += kTM * kAPitch;
-  p.tb = o;
-  o += kTK * kMaxSketch;
+  p.tiles = o;
+  o += 2 * kStageF;
   p.g = o;
   o += k * k;
   p.r = o;
@@ -93,66 +92,101 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) {
 //   B [K × N], row stride ldb, N <= kMaxSketch (global or shared memory).
 //   Element (i, j) goes to C[i*ldc + j], or to C[j*ldc + i] when TC, multiplied by scale[j]
 //   when scale is given. C overlaps neither A nor B.
+// Blocks of 128 rows of C; warp w owns columns [w·cpt, (w+1)·cpt) (cpt = ceil(N / 8)) and lane
+// l rows l, l + 32, l + 64, l + 96, so op(A) reads are conflict-free and B reads broadcast.
+// K advances in steps of 32 through two shared-memory stages: the next step's global loads
+// are in registers while the current step computes, one barrier per step.
 template <bool TA, bool TC, typename Out>
 __device__ void cta_gemm(const float *A, long long lda, const float *B, long long ldb, Out *C,
                          long long ldc, int M, int N, int K, const float *scale, float *sm) {
-  float *ta = sm;
-  float *tb = sm + kTM * kAPitch;
-  const int tid = threadIdx.x;
-  const int rg = tid >> 4, cg = tid & 15;  // rows rg*4 + r, columns cg + 16*c
-  constexpr int CPT = kMaxSketch / 16;
-  for (int m0 = 0; m0 < M; m0 += kTM) {
-    float acc[4][CPT];
+  constexpr int kAper = kBK * kBM / kThr;          // op(A) elements a thread stages per step
+  constexpr int kBper = kBK * kMaxSketch / kThr;   // B elements (upper bound) per step
+  constexpr int kCols = kMaxSketch / 8;            // columns a warp can own
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cpt = (N + 7) / 8, c0 = warp * cpt;
+  for (int m0 = 0; m0 < M; m0 += kBM) {
+    float acc[4][kCols];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) acc[r][c] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += kTK) {
-      __syncthreads();  // the previous step's tiles are consumed
-      for (int e = tid; e < kTM * kTK; e += kThr) {
-        int i, j;
+      for (int c = 0; c < kCols; ++c) acc[r][c] = 0.f;
+    float ra[kAper], rb[kBper];
+    auto load = [&](int k0) {  // global -> registers (zero outside the matrices)
+#pragma unroll
+      for (int j = 0; j < kAper; ++j) {
+        const int e = tid + j * kThr;
+        int kk, mm;
         if (TA) {  // A is [K × M]: consecutive threads walk M
-          j = e / kTM;
-          i = e - j * kTM;
+          kk = e / kBM;
+          mm = e - kk * kBM;
         } else {   // A is [M × K]: consecutive threads walk K
-          i = e / kTK;
-          j = e - i * kTK;
+          mm = e / kBK;
+          kk = e - mm * kBK;
         }
-        const int gi = m0 + i, gk = k0 + j;
-        float x = 0.f;
-        if (gi < M && gk < K) x = TA ? A[(long long)gk * lda + gi] : A[(long long)gi * lda + gk];
-        ta[i * kAPitch + j] = x;
+        const int gm = m0 + mm, gk = k0 + kk;
+        ra[j] = (gm < M && gk < K) ? (TA ? A[(long long)gk * lda + gm] : A[(long long)gm * lda + gk])
+                                   : 0.f;
       }
-      for (int e = tid; e < kTK * N; e += kThr) {
-        const int j = e / N, c = e - j * N;
-        const int gk = k0 + j;
-        tb[j * kMaxSketch + c] = gk < K ? B[(long long)gk * ldb + c] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kBper; ++j) {
+        const int e = tid + j * kThr;
+        const int kk = e / kMaxSketch, n = e - kk * kMaxSketch;
+        const int gk = k0 + kk;
+        rb[j] = (n < N && gk < K) ? B[(long long)gk * ldb + n] : 0.f;
       }
-      __syncthreads();
-      const int kend = min(kTK, K - k0);
+    };
+    auto store = [&](int st) {  // registers -> stage st
+      float *ta = sm + st * kStageF, *tb = ta + kBK * kAPitch;
+#pragma unroll
+      for (int j = 0; j < kAper; ++j) {
+        const int e = tid + j * kThr;
+        int kk, mm;
+        if (TA) {
+          kk = e / kBM;
+          mm = e - kk * kBM;
+        } else {
+          mm = e / kBK;
+          kk = e - mm * kBK;
+        }
+        ta[kk * kAPitch + mm] = ra[j];
+      }
+#pragma unroll
+      for (int j = 0; j < kBper; ++j) tb[tid + j * kThr] = rb[j];
+    };
+    __syncthreads();  // the previous use of the stages is over
+    load(0);
+    store(0);
+    __syncthreads();
+    int st = 0;
+    for (int k0 = 0; k0 < K; k0 += kBK, st ^= 1) {
+      const bool more = k0 + kBK < K;
+      if (more) load(k0 + kBK);
+      const float *ta = sm + st * kStageF, *tb = ta + kBK * kAPitch;
+      const int kend = min(kBK, K - k0);
       for (int kk = 0; kk < kend; ++kk) {
         float av[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) av[r] = ta[(rg * 4 + r) * kAPitch + kk];
+        for (int r = 0; r < 4; ++r) av[r] = ta[kk * kAPitch + lane + 32 * r];
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) {
-          const int col = cg + 16 * c;
-          if (col < N) {
-            const float bv = tb[kk * kMaxSketch + col];
+        for (int c = 0; c < kCols; ++c) {
+          if (c < cpt) {
+            const float bv = tb[kk * kMaxSketch + c0 + c];
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[r][c] = fmaf(av[r], bv, acc[r][c]);
           }
         }
       }
+      if (more) store(st ^ 1);
+      __syncthreads();
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int gi = m0 + rg * 4 + r;
+      const int gi = m0 + lane + 32 * r;
       if (gi < M) {
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) {
-          const int col = cg + 16 * c;
-          if (col < N) {
+        for (int c = 0; c < kCols; ++c) {
+          const int col = c0 + c;
+          if (c < cpt && col < N) {
             const float x = scale ? acc[r][c] * scale[col] : acc[r][c];
             if (TC)
               C[(long long)col * ldc + gi] = to_out<Out>(x);
