@@ -163,6 +163,7 @@ __device__ void cta_gemm(const float *A, long long lda, const float *B, long lon
       if (more) load(k0 + kBK);
       const float *ta = sm + st * kStageF, *tb = ta + kBK * kAPitch;
       const int kend = min(kBK, K - k0);
+#pragma unroll 4
       for (int kk = 0; kk < kend; ++kk) {
         float av[4];
 #pragma unroll
@@ -200,50 +201,115 @@ __device__ void cta_gemm(const float *A, long long lda, const float *B, long lon
   __syncthreads();
 }
 
+// G [k × k] (shared, row-major) = Yᵀ Y for Y [M × k] (row stride k). Each thread owns a 4 × 4
+// block of the upper block triangle and a share of the rows (S row subsets when the blocks
+// leave threads over); the subsets' partial blocks meet in `scratch` (S · k² floats) and the
+// lower triangle is mirrored from the upper one.
+__device__ void cta_gram(const float *Y, int M, int k, float *g, float *scratch) {
+  const int tid = threadIdx.x;
+  const int nb = (k + 3) >> 2, nblk = nb * (nb + 1) / 2;
+  const int S = max(1, kThr / nblk);
+  for (int w = tid; w < S * nblk; w += kThr) {
+    const int sub = w / nblk;
+    int b = w - sub * nblk, bi = 0;
+    while (b >= nb - bi) {  // block b of the upper block triangle, row by row
+      b -= nb - bi;
+      ++bi;
+    }
+    const int bj = bi + b;
+    const int i0 = 4 * bi, j0 = 4 * bj;
+    float acc[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 2
+    for (int r = sub; r < M; r += S) {
+      const float *row = Y + (long long)r * k;
+      float u[4], v[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        u[x] = i0 + x < k ? row[i0 + x] : 0.f;
+        v[x] = j0 + x < k ? row[j0 + x] : 0.f;
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(u[x], v[y], acc[x][y]);
+    }
+    float *out = scratch + (long long)sub * k * k;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+        if (i0 + x < k && j0 + y < k) out[(i0 + x) * k + j0 + y] = acc[x][y];
+  }
+  __syncthreads();
+  for (int e = tid; e < k * k; e += kThr) {
+    int i = e / k, j = e - i * k;
+    if ((i >> 2) > (j >> 2)) {  // below the block diagonal: the mirror entry was computed
+      const int t = i;
+      i = j;
+      j = t;
+    }
+    float sum = 0.f;
+    for (int sub = 0; sub < S; ++sub) sum += scratch[(long long)sub * k * k + i * k + j];
+    g[e] = sum;
+  }
+  __syncthreads();
+}
+
 // One Cholesky QR pass: dst [M × k] = src · L⁻ᵀ where L Lᵀ = srcᵀ src (+ sI when shifted).
 // Row stride k for both; src and dst are distinct buffers.
 __device__ void cholqr_pass(const float *src, float *dst, int M, int k, bool shifted, float *sm,
                             const FormPlan &p) {
   float *g = sm + p.g;  // row-major k × k; its lower triangle becomes L
   float *r = sm + p.r;  // r[c*k + j] = (L⁻¹)[j][c]: the [k × k] operand of dst = src · L⁻ᵀ
-  cta_gemm<true, false, float>(src, k, src, k, g, k, k, k, M, nullptr, sm);
+  cta_gram(src, M, k, g, sm + p.tiles);
   const int tid = threadIdx.x;
-  if (tid < 32) {
-    const int lane = tid;
-    if (shifted) {
+  if (shifted) {
+    if (tid < 32) {
       float tr = 0.f;
-      for (int j = lane; j < k; j += 32) tr += g[j * k + j];
+      for (int j = tid; j < k; j += 32) tr += g[j * k + j];
       for (int o = 16; o > 0; o >>= 1) tr += __shfl_xor_sync(0xffffffffu, tr, o);
       const float s = 11.f * ((float)M * k + (float)k * (k + 1)) * 5.9604645e-8f * tr;
       __syncwarp();
-      for (int j = lane; j < k; j += 32) g[j * k + j] += s;
-      __syncwarp();
+      for (int j = tid; j < k; j += 32) g[j * k + j] += s;
     }
-    // right-looking Cholesky on the lower triangle
-    for (int j = 0; j < k; ++j) {
-      const float d = g[j * k + j];
-      const float ljj = d > 0.f ? sqrtf(d) : 0.f;  // not positive (or NaN): drop column j
-      const float inv = ljj > 0.f ? 1.f / ljj : 0.f;
-      __syncwarp();
-      if (lane == 0) g[j * k + j] = ljj;
-      for (int i = j + 1 + lane; i < k; i += 32) g[i * k + j] *= inv;
-      __syncwarp();
-      const int rem = k - j - 1;
-      for (int e = lane; e < rem * rem; e += 32) {
-        const int i = j + 1 + e / rem, l = j + 1 + e % rem;
-        if (l <= i) g[i * k + l] -= g[i * k + j] * g[l * k + j];
-      }
-      __syncwarp();
+    __syncthreads();
+  }
+  // right-looking Cholesky on the lower triangle, all threads: scale column j by its pivot,
+  // then update the trailing triangle
+  for (int j = 0; j < k; ++j) {
+    const float d = g[j * k + j];
+    const float ljj = d > 0.f ? sqrtf(d) : 0.f;  // not positive (or NaN): drop column j
+    const float inv = ljj > 0.f ? 1.f / ljj : 0.f;
+    for (int i = j + 1 + tid; i < k; i += kThr) g[i * k + j] *= inv;
+    __syncthreads();
+    if (tid == 0) g[j * k + j] = ljj;
+    const int rem = k - j - 1;
+    for (int e = tid; e < rem * rem; e += kThr) {
+      const int i = j + 1 + e / rem, l = j + 1 + e % rem;
+      if (l <= i) g[i * k + l] -= g[i * k + j] * g[l * k + j];
     }
-    // column c of L⁻¹ solves L x = e_c (forward substitution); a dropped pivot gives x = 0
-    for (int c = lane; c < k; c += 32) {
-      for (int i = 0; i < c; ++i) r[c * k + i] = 0.f;
-      for (int i = c; i < k; ++i) {
-        float acc = i == c ? 1.f : 0.f;
-        for (int l = c; l < i; ++l) acc -= g[i * k + l] * r[c * k + l];
-        const float lii = g[i * k + i];
-        r[c * k + i] = lii > 0.f ? acc / lii : 0.f;
+    __syncthreads();
+  }
+  // column c of L⁻¹ solves L x = e_c (forward substitution), one thread per column; a dropped
+  // pivot gives x = 0. Four partial sums shorten the dependent chain.
+  for (int c = tid; c < k; c += kThr) {
+    for (int i = 0; i < c; ++i) r[c * k + i] = 0.f;
+    for (int i = c; i < k; ++i) {
+      float a0 = i == c ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      int l = c;
+      for (; l + 3 < i; l += 4) {
+        a0 -= g[i * k + l] * r[c * k + l];
+        a1 -= g[i * k + l + 1] * r[c * k + l + 1];
+        a2 -= g[i * k + l + 2] * r[c * k + l + 2];
+        a3 -= g[i * k + l + 3] * r[c * k + l + 3];
       }
+      for (; l < i; ++l) a0 -= g[i * k + l] * r[c * k + l];
+      const float lii = g[i * k + i];
+      r[c * k + i] = lii > 0.f ? ((a0 + a1) + (a2 + a3)) / lii : 0.f;
     }
   }
   __syncthreads();
