@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the brief timings of the MLA, survival and recall-sweep workloads")
+    ap.add_argument("--workload", choices=OTHER_WORKLOADS, default=None,
+                    help="time only this one of the other workloads and print it (a profiling "
+                         "entry point; not the bench line)")
     return ap.parse_args()
 
 
@@ -493,17 +496,26 @@ def time_calls(fn, steps, warmup=1):
     return e0.elapsed_time(e1) / steps
 
 
-def other_workloads(dev):
+OTHER_WORKLOADS = ("patch_readd_in_place_18_placements", "decode_attention_reorder_pool",
+                   "mrope_reorder_18_placements", "reanchor_18_placements", "mla_recall_64_chunks",
+                   "mha_sliding_window_448_survivors", "gqa_recall_sweep_1024_items",
+                   "form_patch_84_deficits")
+
+
+def other_workloads(dev, only=None):
     """Brief timings of the in-place switch, decode attention over the written pool, M-RoPE
     reorder, re-anchoring, MLA recall, sliding-window survival, recall-sweep and
-    patch-forming workloads (each a parity-tested configuration of
-    its own); reported beside the main line."""
+    patch-forming workloads (each a parity-tested configuration of its own); reported beside
+    the main line. ``only`` names one of them to run alone."""
     import torch
     import position_independent_multimodal_gb300 as km
     import workloads as wl
 
     peak, _ = measured_peak()
     out = {}
+
+    def want(name):
+        return only is None or only == name
 
     def reuse_calls(w, launches):
         lay = w.layout
@@ -526,191 +538,199 @@ def other_workloads(dev):
             raise RuntimeError(f"device status {int(st.item())}")
         return ms
 
-    # reversible switch: the patch re-added in place on the cached rows of the 18 reorder
-    # placements (their patched layers), alternately added and removed
-    w = wl.config2(device=dev)
-    lay = w.layout
-    h = km.create(lay)
-    k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
-    v = torch.empty_like(k)
-    pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
-    st = torch.zeros(1, dtype=torch.int32, device=dev)
-    d_items = km.pack_items(w.items).to(dev)
-    km.kamera_batch_reuse(h, d_items, len(w.items), 1024, 32, pool, st)
-    flips = [1]
+    if want("patch_readd_in_place_18_placements") or want("decode_attention_reorder_pool"):
+        # reversible switch: the patch re-added in place on the cached rows of the 18 reorder
+        # placements (their patched layers), alternately added and removed
+        w = wl.config2(device=dev)
+        lay = w.layout
+        h = km.create(lay)
+        k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        d_items = km.pack_items(w.items).to(dev)
+        km.kamera_batch_reuse(h, d_items, len(w.items), 1024, 32, pool, st)
+        flips = [1]
 
-    def readd():
-        sign = flips[0]
-        flips[0] = -sign
-        km.kamera_batch_patch_inplace(h, d_items, len(w.items), 1024, 32, pool, sign, st)
-    ms = time_calls(readd, 20, warmup=4)
-    torch.cuda.synchronize()
-    if int(st.item()) != 0:
-        raise RuntimeError(f"device status {int(st.item())}")
-    rows = sum(it.num_tokens * (it.patch_l1 - it.patch_l0) for it in w.items)
-    moved = rows * (lay.row_k + lay.row_v) * 2 * 2 + \
-        sum((it.patch_u.numel() + it.patch_vt.numel()) * 2 for it in w.items[:3])
-    out["patch_readd_in_place_18_placements"] = {
-        "workload": "GQA reorder pool (28 layers, H_kv=4 x 128): rank-32 patch re-added in place "
-                    "on layers 14-27 of all 18 placements (one batched call), alternately +1 "
-                    "and -1",
-        "ms_per_step": ms, "gb_s_moved": moved / ms / 1e6,
-        "frac_hbm_peak": moved / ms / 1e6 / peak}
+        def readd():
+            sign = flips[0]
+            flips[0] = -sign
+            km.kamera_batch_patch_inplace(h, d_items, len(w.items), 1024, 32, pool, sign, st)
+        ms = time_calls(readd, 20, warmup=4)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        rows = sum(it.num_tokens * (it.patch_l1 - it.patch_l0) for it in w.items)
+        moved = rows * (lay.row_k + lay.row_v) * 2 * 2 + \
+            sum((it.patch_u.numel() + it.patch_vt.numel()) * 2 for it in w.items[:3])
+        out["patch_readd_in_place_18_placements"] = {
+            "workload": "GQA reorder pool (28 layers, H_kv=4 x 128): rank-32 patch re-added in place "
+                        "on layers 14-27 of all 18 placements (one batched call), alternately +1 "
+                        "and -1",
+            "ms_per_step": ms, "gb_s_moved": moved / ms / 1e6,
+            "frac_hbm_peak": moved / ms / 1e6 / peak}
 
-    # consumer check: decode attention of one query token per head (Qwen2-VL-7B: 28 query
-    # heads over the 4 KV heads) over the six 3072-token requests of that pool, every layer
-    hq, ctx = 28, 3 * 1024
-    reqs = int(w.page_table.shape[0])
-    g = torch.Generator(device=dev)
-    g.manual_seed(5)
-    q = torch.randn(reqs, hq, lay.head_dim, generator=g, device=dev).to(torch.bfloat16)
-    ctx_len = torch.full((reqs,), ctx, dtype=torch.int32, device=dev)
-    o_buf = torch.empty(reqs, hq, lay.head_dim, device=dev)
-    lse = torch.empty(reqs, hq, device=dev)
-    ws = torch.empty(km.kamera_decode_attention_workspace(h, reqs, hq, ctx), dtype=torch.uint8,
-                     device=dev)
+        # consumer check: decode attention of one query token per head (Qwen2-VL-7B: 28 query
+        # heads over the 4 KV heads) over the six 3072-token requests of that pool, every layer
+        hq, ctx = 28, 3 * 1024
+        reqs = int(w.page_table.shape[0])
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        q = torch.randn(reqs, hq, lay.head_dim, generator=g, device=dev).to(torch.bfloat16)
+        ctx_len = torch.full((reqs,), ctx, dtype=torch.int32, device=dev)
+        o_buf = torch.empty(reqs, hq, lay.head_dim, device=dev)
+        lse = torch.empty(reqs, hq, device=dev)
+        ws = torch.empty(km.kamera_decode_attention_workspace(h, reqs, hq, ctx), dtype=torch.uint8,
+                         device=dev)
 
-    def attend_all_layers():
-        for layer in range(lay.num_layers):
-            km.kamera_decode_attention(h, pool, layer, q, ctx_len, ctx, lay.head_dim ** -0.5,
-                                       o_buf, lse, ws, st)
-    # a decode step runs its per-layer calls from a CUDA graph: capture the 28 calls once and
-    # time the replays (the calls are made once before capture, which sets up the kernels)
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        attend_all_layers()
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        attend_all_layers()
-    ms = time_calls(graph.replay, 20, warmup=3)
-    torch.cuda.synchronize()
-    if int(st.item()) != 0:
-        raise RuntimeError(f"device status {int(st.item())}")
-    kv_bytes = reqs * ctx * lay.num_layers * (lay.row_k + lay.row_v) * 2
-    out["decode_attention_reorder_pool"] = {
-        "workload": "decode attention over the reorder pool: 6 requests x 3072 tokens, 28 query "
-                    "heads over 4 KV heads x 128, all 28 layers (one call per layer, replayed "
-                    "from a CUDA graph)",
-        "ms_per_step": ms, "gb_s_read": kv_bytes / ms / 1e6,
-        "frac_hbm_peak": kv_bytes / ms / 1e6 / peak}
-    del w, k, v, pool, q, ws, o_buf, graph
-    torch.cuda.empty_cache()
+        def attend_all_layers():
+            for layer in range(lay.num_layers):
+                km.kamera_decode_attention(h, pool, layer, q, ctx_len, ctx, lay.head_dim ** -0.5,
+                                           o_buf, lse, ws, st)
+        # a decode step runs its per-layer calls from a CUDA graph: capture the 28 calls once and
+        # time the replays (the calls are made once before capture, which sets up the kernels)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            attend_all_layers()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            attend_all_layers()
+        ms = time_calls(graph.replay, 20, warmup=3)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        kv_bytes = reqs * ctx * lay.num_layers * (lay.row_k + lay.row_v) * 2
+        out["decode_attention_reorder_pool"] = {
+            "workload": "decode attention over the reorder pool: 6 requests x 3072 tokens, 28 query "
+                        "heads over 4 KV heads x 128, all 28 layers (one call per layer, replayed "
+                        "from a CUDA graph)",
+            "ms_per_step": ms, "gb_s_read": kv_bytes / ms / 1e6,
+            "frac_hbm_peak": kv_bytes / ms / 1e6 / peak}
+        del w, k, v, pool, q, ws, o_buf, graph
+        torch.cuda.empty_cache()
 
-    w = wl.config2_mrope(device=dev)
-    acc = accounting(w)
-    ms = reuse_calls(w, [w.items])
-    out["mrope_reorder_18_placements"] = {
-        "workload": "the GQA reorder step with Qwen2.5-VL M-RoPE (16|24|24 pairs over t, h, w; "
-                    "t moved by j*1024, h and w by j*16 at ordering position j)",
-        "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
-        "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak}
-    del w
-    torch.cuda.empty_cache()
+    if want("mrope_reorder_18_placements"):
+        w = wl.config2_mrope(device=dev)
+        acc = accounting(w)
+        ms = reuse_calls(w, [w.items])
+        out["mrope_reorder_18_placements"] = {
+            "workload": "the GQA reorder step with Qwen2.5-VL M-RoPE (16|24|24 pairs over t, h, w; "
+                        "t moved by j*1024, h and w by j*16 at ordering position j)",
+            "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
+            "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak}
+        del w
+        torch.cuda.empty_cache()
 
-    # QV-PIC-style re-anchoring: 18 placements of three unrotated 1024-token images, every
-    # layer, per-token (t, h, w) positions
-    w = wl.config_reanchor(device=dev)
-    lay = w.layout
-    h = km.create(lay)
-    k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
-    v = torch.empty_like(k)
-    pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
-    st = torch.zeros(1, dtype=torch.int32, device=dev)
-    d_items = km.pack_anchor_items(w.items).to(dev)
-    ms = time_calls(lambda: km.kamera_reanchor(h, d_items, len(w.items), 1024, pool, st), 20,
-                    warmup=3)
-    torch.cuda.synchronize()
-    if int(st.item()) != 0:
-        raise RuntimeError(f"device status {int(st.item())}")
-    written = sum(it.num_tokens for it in w.items) * lay.num_layers * (lay.row_k + lay.row_v) * 2
-    distinct = {it.chunk_id: it for it in w.items}.values()
-    read = sum(it.num_tokens for it in distinct) * lay.num_layers * (lay.row_k + lay.row_v) * 2 \
-        + sum(it.positions.numel() * 8 for it in w.items)
-    out["reanchor_18_placements"] = {
-        "workload": "QV-PIC-style re-anchoring: three 32 x 32-token images stored before rotation "
-                    "(Qwen2.5-VL layout, 28 layers, H_kv=4 x 128, M-RoPE 16|24|24) placed in all "
-                    "6 orderings, every layer, per-token (t, h, w) positions",
-        "ms_per_call": ms, "gb_s_written": written / ms / 1e6,
-        "frac_hbm_peak": (written + read) / ms / 1e6 / peak}
-    del w, k, v, pool, d_items
-    torch.cuda.empty_cache()
+    if want("reanchor_18_placements"):
+        # QV-PIC-style re-anchoring: 18 placements of three unrotated 1024-token images, every
+        # layer, per-token (t, h, w) positions
+        w = wl.config_reanchor(device=dev)
+        lay = w.layout
+        h = km.create(lay)
+        k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        d_items = km.pack_anchor_items(w.items).to(dev)
+        ms = time_calls(lambda: km.kamera_reanchor(h, d_items, len(w.items), 1024, pool, st), 20,
+                        warmup=3)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        written = sum(it.num_tokens for it in w.items) * lay.num_layers * (lay.row_k + lay.row_v) * 2
+        distinct = {it.chunk_id: it for it in w.items}.values()
+        read = sum(it.num_tokens for it in distinct) * lay.num_layers * (lay.row_k + lay.row_v) * 2 \
+            + sum(it.positions.numel() * 8 for it in w.items)
+        out["reanchor_18_placements"] = {
+            "workload": "QV-PIC-style re-anchoring: three 32 x 32-token images stored before rotation "
+                        "(Qwen2.5-VL layout, 28 layers, H_kv=4 x 128, M-RoPE 16|24|24) placed in all "
+                        "6 orderings, every layer, per-token (t, h, w) positions",
+            "ms_per_call": ms, "gb_s_written": written / ms / 1e6,
+            "frac_hbm_peak": (written + read) / ms / 1e6 / peak}
+        del w, k, v, pool, d_items
+        torch.cuda.empty_cache()
 
-    w = wl.config3(device=dev)
-    acc = accounting(w)
-    ms = reuse_calls(w, [w.items])
-    out["mla_recall_64_chunks"] = {
-        "workload": "MLA (DeepSeek-V2-Lite-shaped) 27 layers, c_KV 512 + k_pe 64, 64 chunks "
-                    "T=1024, delta in [-32768, 32768], m=32 on layers 13-26",
-        "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
-        "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
-        "chunks_per_s": len(w.items) / ms * 1e3}
-    del w
-    torch.cuda.empty_cache()
+    if want("mla_recall_64_chunks"):
+        w = wl.config3(device=dev)
+        acc = accounting(w)
+        ms = reuse_calls(w, [w.items])
+        out["mla_recall_64_chunks"] = {
+            "workload": "MLA (DeepSeek-V2-Lite-shaped) 27 layers, c_KV 512 + k_pe 64, 64 chunks "
+                        "T=1024, delta in [-32768, 32768], m=32 on layers 13-26",
+            "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
+            "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
+            "chunks_per_s": len(w.items) / ms * 1e3}
+        del w
+        torch.cuda.empty_cache()
 
-    w = wl.config4(device=dev)
-    h = km.create(w.layout)
-    vd = torch.zeros(1, 1, 8, dtype=torch.bfloat16, device=dev)
-    pool = km.Pool(w.k_pool, vd, w.page_table.to(dev), w.num_slots)
-    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if want("mha_sliding_window_448_survivors"):
+        w = wl.config4(device=dev)
+        h = km.create(w.layout)
+        vd = torch.zeros(1, 1, 8, dtype=torch.bfloat16, device=dev)
+        pool = km.Pool(w.k_pool, vd, w.page_table.to(dev), w.num_slots)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def reloc():
-        for sp in w.spans:
-            km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, st)
-    ms = time_calls(reloc, 3)
-    moved = sum(sp.num_tokens for sp in w.spans) * w.layout.num_layers * w.layout.row_k * 2 * 2
-    out["mha_sliding_window_448_survivors"] = {
-        "workload": "MHA 32 layers x 32 heads x 128, 64 sequences x 7 survivor chunks of 576 "
-                    "tokens re-rotated in place by delta=-576 (K pool 77 GB)",
-        "ms_per_step": ms, "gb_s_written": moved / 2 / ms / 1e6,
-        "frac_hbm_peak": moved / ms / 1e6 / peak,
-        "chunks_per_s": 448 / ms * 1e3}
-    del w, pool
-    torch.cuda.empty_cache()
+        def reloc():
+            for sp in w.spans:
+                km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, st)
+        ms = time_calls(reloc, 3)
+        moved = sum(sp.num_tokens for sp in w.spans) * w.layout.num_layers * w.layout.row_k * 2 * 2
+        out["mha_sliding_window_448_survivors"] = {
+            "workload": "MHA 32 layers x 32 heads x 128, 64 sequences x 7 survivor chunks of 576 "
+                        "tokens re-rotated in place by delta=-576 (K pool 77 GB)",
+            "ms_per_step": ms, "gb_s_written": moved / 2 / ms / 1e6,
+            "frac_hbm_peak": moved / ms / 1e6 / peak,
+            "chunks_per_s": 448 / ms * 1e3}
+        del w, pool
+        torch.cuda.empty_cache()
 
-    w = wl.config5(device=dev)
-    launches = [wl.config5_launch_items(w, g) for g in range(8)]
-    ms = reuse_calls(w, launches)
-    written = sum(accounting(w, items)["written"] for items in launches)
-    alg = sum(accounting(w, items)["algorithmic"] for items in launches)
-    out["gqa_recall_sweep_1024_items"] = {
-        "workload": "GQA 64 layers (8 launches of 8-layer slices), H_kv=8 x 128, 256 requests x "
-                    "4 recalls T=1024, delta in [0, 131072), m=64 on layers 32-63",
-        "ms_per_step": ms, "gb_s_written": written / ms / 1e6,
-        "frac_hbm_peak": alg / ms / 1e6 / peak, "chunks_per_s": 1024 / ms * 1e3}
-    del w, launches
-    torch.cuda.empty_cache()
+    if want("gqa_recall_sweep_1024_items"):
+        w = wl.config5(device=dev)
+        launches = [wl.config5_launch_items(w, g) for g in range(8)]
+        ms = reuse_calls(w, launches)
+        written = sum(accounting(w, items)["written"] for items in launches)
+        alg = sum(accounting(w, items)["algorithmic"] for items in launches)
+        out["gqa_recall_sweep_1024_items"] = {
+            "workload": "GQA 64 layers (8 launches of 8-layer slices), H_kv=8 x 128, 256 requests x "
+                        "4 recalls T=1024, delta in [0, 131072), m=64 on layers 32-63",
+            "ms_per_step": ms, "gb_s_written": written / ms / 1e6,
+            "frac_hbm_peak": alg / ms / 1e6 / peak, "chunks_per_s": 1024 / ms * 1e3}
+        del w, launches
+        torch.cuda.empty_cache()
 
-    # patch forming: the 84 deficits of the reorder workload's patched layers (3 chunks x 14
-    # layers x K and V), T = 1024 tokens x W = 512, top m = 32 from a k = 40 sketch with one
-    # power iteration, written into the patch store layout
-    n, T, W, k, q, m = 84, 1024, 512, 40, 1, 32
-    delta, omega = wl.deficit_problems(n, T, W, k=k, rank=64, decay=0.9, noise=1e-2, seed=0,
-                                       device=dev)
-    u = torch.empty(n, T, m, dtype=torch.bfloat16, device=dev)
-    vt = torch.empty(n, m, W, dtype=torch.bfloat16, device=dev)
-    sig = torch.empty(n, m, dtype=torch.float32, device=dev)
-    ws = torch.empty(km.kamera_form_patch_workspace(n, T, W, k), dtype=torch.uint8, device=dev)
+    if want("form_patch_84_deficits"):
+        # patch forming: the 84 deficits of the reorder workload's patched layers (3 chunks x 14
+        # layers x K and V), T = 1024 tokens x W = 512, top m = 32 from a k = 40 sketch with one
+        # power iteration, written into the patch store layout
+        n, T, W, k, q, m = 84, 1024, 512, 40, 1, 32
+        delta, omega = wl.deficit_problems(n, T, W, k=k, rank=64, decay=0.9, noise=1e-2, seed=0,
+                                           device=dev)
+        u = torch.empty(n, T, m, dtype=torch.bfloat16, device=dev)
+        vt = torch.empty(n, m, W, dtype=torch.bfloat16, device=dev)
+        sig = torch.empty(n, m, dtype=torch.float32, device=dev)
+        ws = torch.empty(km.kamera_form_patch_workspace(n, T, W, k), dtype=torch.uint8, device=dev)
 
-    def form():
-        km.kamera_form_patch(delta, omega, k, q, m, u, vt, sig, ws, num_problems=n, T=T, W=W,
-                             ld=W, delta_stride=T * W, omega_stride=0, u_stride=T * m,
-                             vt_stride=m * W)
-    ms = time_calls(form, 5, warmup=2)
-    # algorithmic float32 flops: the (2 + 2q) products with Δ, 12·M·k² per CholeskyQR3 on M
-    # rows, and U·Σ = Q·Ũ_m (the Jacobi sweeps are not counted)
-    flops = n * ((2 + 2 * q) * 2 * T * W * k + 12 * k * k * ((1 + q) * T + q * W) +
-                 2 * T * k * m)
-    out["form_patch_84_deficits"] = {
-        "workload": "patch forming: 84 float32 deficits 1024 x 512 (the reorder workload's "
-                    "patched layers), top 32 of a 40-column sketch, 1 power iteration",
-        "ms_per_call": ms, "deficits_per_s": n / ms * 1e3,
-        "gflop_s": flops / ms / 1e6,
-        "delta_gb_s": (2 + 2 * q) * n * T * W * 4 / ms / 1e6}
-    del delta, omega, u, vt, sig, ws
-    torch.cuda.empty_cache()
+        def form():
+            km.kamera_form_patch(delta, omega, k, q, m, u, vt, sig, ws, num_problems=n, T=T, W=W,
+                                 ld=W, delta_stride=T * W, omega_stride=0, u_stride=T * m,
+                                 vt_stride=m * W)
+        ms = time_calls(form, 5, warmup=2)
+        # algorithmic float32 flops: the (2 + 2q) products with Δ, 12·M·k² per CholeskyQR3 on M
+        # rows, and U·Σ = Q·Ũ_m (the Jacobi sweeps are not counted)
+        flops = n * ((2 + 2 * q) * 2 * T * W * k + 12 * k * k * ((1 + q) * T + q * W) +
+                     2 * T * k * m)
+        out["form_patch_84_deficits"] = {
+            "workload": "patch forming: 84 float32 deficits 1024 x 512 (the reorder workload's "
+                        "patched layers), top 32 of a 40-column sketch, 1 power iteration",
+            "ms_per_call": ms, "deficits_per_s": n / ms * 1e3,
+            "gflop_s": flops / ms / 1e6,
+            "delta_gb_s": (2 + 2 * q) * n * T * W * 4 / ms / 1e6}
+        del delta, omega, u, vt, sig, ws
+        torch.cuda.empty_cache()
+
     return out
 
 
@@ -784,6 +804,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         reference_arm(args, rank)
+        return
+    if args.workload is not None:
+        import torch
+        print(json.dumps(other_workloads(torch.device("cuda", local_rank), only=args.workload)))
         return
     if world > 1:
         import torch
