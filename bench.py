@@ -736,53 +736,78 @@ def other_workloads(dev, only=None):
 
 def end_to_end(args, w, h, dev, stream):
     """Same metric through the C-ABI with host buffers: every step copies the canonical and
-    patch stores, the items and the page table from pinned host memory, runs the batch and
-    reads the written pool back."""
+    patch stores, the items and the page table from pinned host memory (a KV store kept in
+    host memory), runs the batch into the device pool, where attention reads it, and reads the
+    step's result back: the call's device status word.
+
+    Steps are pipelined the way a serving loop would run them: each step's input copies are
+    spread over four copy streams into one of two device buffer sets, so step i + 1's copies
+    overlap step i's kernels; a set is refilled only after the kernels that read it finished."""
     import torch
     import position_independent_multimodal_gb300 as km
     import workloads as wl
 
     lay = w.layout
-    host, dev_bufs, seen = [], {}, {}
+    n_sets, n_copy = 2, 4
+    host, seen = [], {}
     for t in [x for it in w.items for x in (it.canon_k, it.canon_v, it.patch_u, it.patch_vt)]:
         if t is None or t.data_ptr() in seen:
             continue
         hb = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         hb.copy_(t)
-        db = torch.empty_like(t)
-        seen[t.data_ptr()] = db
-        host.append((hb, db))
-    items = [wl.Item(**{**it.__dict__,
-                        "canon_k": seen[it.canon_k.data_ptr()],
-                        "canon_v": seen[it.canon_v.data_ptr()],
-                        "patch_u": None if it.patch_u is None else seen[it.patch_u.data_ptr()],
-                        "patch_vt": None if it.patch_vt is None else
-                        seen[it.patch_vt.data_ptr()]}) for it in w.items]
-    h_items = km.pack_items(items).pin_memory()
-    d_items = torch.empty_like(h_items, device=dev)
+        seen[t.data_ptr()] = len(host)
+        host.append(hb)
+    sets = []
+    for _ in range(n_sets):
+        dbs = [torch.empty_like(hb, device=dev) for hb in host]
+        items = [wl.Item(**{**it.__dict__,
+                            "canon_k": dbs[seen[it.canon_k.data_ptr()]],
+                            "canon_v": dbs[seen[it.canon_v.data_ptr()]],
+                            "patch_u": None if it.patch_u is None else
+                            dbs[seen[it.patch_u.data_ptr()]],
+                            "patch_vt": None if it.patch_vt is None else
+                            dbs[seen[it.patch_vt.data_ptr()]]}) for it in w.items]
+        h_items = km.pack_items(items).pin_memory()
+        sets.append({"dbs": dbs, "h_items": h_items,
+                     "d_items": torch.empty_like(h_items, device=dev),
+                     "d_pt": torch.empty(w.page_table.shape, dtype=w.page_table.dtype,
+                                         device=dev),
+                     "done": torch.cuda.Event()})
     h_pt = w.page_table.pin_memory()
-    d_pt = torch.empty_like(h_pt, device=dev)
     k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
     v = torch.empty_like(k)
-    hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
-    hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-    pool = km.Pool(k, v, d_pt, w.num_slots)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    h_status = torch.zeros(1, dtype=torch.int32, pin_memory=True)
     max_m = max(it.patch_m for it in w.items)
-    h2d = sum(hb.numel() * hb.element_size() for hb, _ in host) + h_items.numel() + \
-        h_pt.numel() * 4
-    d2h = (hk.numel() + hv.numel()) * 2
+    n_items = len(w.items)
+    copy_streams = [torch.cuda.Stream(device=dev) for _ in range(n_copy)]
+    h2d = sum(hb.numel() * hb.element_size() for hb in host) + \
+        sets[0]["h_items"].numel() + h_pt.numel() * 4
+    d2h = h_status.numel() * 4
+    count = [0]
 
     def step():
-        for hb, db in host:
-            db.copy_(hb, non_blocking=True)
-        d_items.copy_(h_items, non_blocking=True)
-        d_pt.copy_(h_pt, non_blocking=True)
-        km.kamera_batch_reuse(h, d_items, len(items), 1024, max_m, pool, status, stream)
-        hk.copy_(k, non_blocking=True)
-        hv.copy_(v, non_blocking=True)
+        cur = sets[count[0] % n_sets]
+        count[0] += 1
+        pieces = [(db, hb) for db, hb in zip(cur["dbs"], host)] + \
+            [(cur["d_items"], cur["h_items"]), (cur["d_pt"], h_pt)]
+        joined = []
+        for j, cs in enumerate(copy_streams):
+            cs.wait_event(cur["done"])  # the kernels that last read this set are finished
+            with torch.cuda.stream(cs):
+                for db, hb in pieces[j::n_copy]:
+                    db.copy_(hb, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            joined.append(ev)
+        for ev in joined:
+            stream.wait_event(ev)
+        pool = km.Pool(k, v, cur["d_pt"], w.num_slots)
+        km.kamera_batch_reuse(h, cur["d_items"], n_items, 1024, max_m, pool, status, stream)
+        cur["done"].record(stream)
+        h_status.copy_(status, non_blocking=True)
 
-    for _ in range(2):
+    for _ in range(2 * n_sets):
         step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -792,9 +817,13 @@ def end_to_end(args, w, h, dev, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.e2e_steps
-    written = sum(lay.num_layers * it.num_tokens * (lay.row_k + lay.row_v) * 2 for it in items)
+    if int(h_status.item()) != 0:
+        raise RuntimeError(f"device status {int(h_status.item())}")
+    written = sum(lay.num_layers * it.num_tokens * (lay.row_k + lay.row_v) * 2
+                  for it in w.items)
     return {"value": written / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipeline": f"{n_copy} copy streams, {n_sets} input buffer sets"}
 
 
 def main():
