@@ -164,3 +164,106 @@ def test_config5_recall_sweep_full():
         del k, v
     del w
     torch.cuda.empty_cache()
+
+
+def test_reanchor_full():
+    # the QV-PIC re-anchoring workload at bench size, in the bench's single launch: every slot
+    # written, sampled rows against the oracle (rotated columns within one ulp plus the float32
+    # rotation bound, V byte copies)
+    from types import SimpleNamespace
+    w = wl.config_reanchor(device="cuda")
+    lay = w.layout
+    k, v = tl.sentinel_pool(lay, w.num_slots)
+    h = km.create(lay)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    km.kamera_reanchor(h, km.pack_anchor_items(w.items).cuda(), len(w.items), 1024,
+                       km.Pool(k, v, w.page_table.cuda(), w.num_slots), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # every slot an item covers is written; only the 16-token prefix of each request is not
+    uncovered = lay.num_layers * (w.num_slots - sum(it.num_tokens for it in w.items))
+    assert unwritten_rows(k) == uncovered and unwritten_rows(v) == uncovered
+    rng = np.random.default_rng(31)
+    pt = w.page_table.numpy()
+    for _ in range(24):
+        it = w.items[int(rng.integers(len(w.items)))]
+        layer = int(rng.integers(lay.num_layers))
+        toks = sample_tokens(rng, it.num_tokens)
+        idx = torch.as_tensor(toks, device="cuda")
+        oi = SimpleNamespace(canon_k={layer: wl.bf16_bits(it.canon_k[layer].index_select(0, idx))},
+                             canon_v={layer: wl.bf16_bits(it.canon_v[layer].index_select(0, idx))},
+                             positions=it.positions.cpu().numpy()[toks], num_tokens=len(toks))
+        sl = torch.as_tensor(pt[it.req, (it.start_tok + toks) // lay.page_size].astype(np.int64)
+                             * lay.page_size + (it.start_tok + toks) % lay.page_size,
+                             device="cuda")
+        for ch, pool in ((0, k), (1, v)):
+            got = wl.bf16_bits(pool[layer].index_select(0, sl))
+            vals, copy_mask = ora.reanchor_layer(lay, oi, layer, ch)
+            src = (oi.canon_k if ch == 0 else oi.canon_v)[layer]
+            assert np.array_equal(got[:, copy_mask], src[:, copy_mask])
+            if not copy_mask.all():
+                x = ora.bf16_to_f64(src)
+                S = np.abs(x)
+                for c0, d in ora.rope_bands(lay):
+                    ia, ib = ora.rope_pairs(d, lay.rope_style)
+                    S[:, c0 + ia] = S[:, c0 + ib] = np.abs(x[:, c0 + ia]) + np.abs(x[:, c0 + ib])
+                y = vals[:, ~copy_mask]
+                g = ora.bf16_to_f64(got[:, ~copy_mask])
+                assert np.all(np.abs(g - y) <= ora.bf16_ulp(y) + 8 * 2.0 ** -24 * S[:, ~copy_mask])
+    del k, v, w
+    torch.cuda.empty_cache()
+
+
+def test_decode_attention_full():
+    # decode attention over the reorder pool at bench size (6 requests x 3072 tokens, 28 query
+    # heads over 4 KV heads), sampled layers, against float64 attention over the same pool
+    from tests.test_gpu_attention import compare
+    w = wl.config2(device="cuda")
+    lay = w.layout
+    k, v, status = run_batch(w, w.items)
+    assert status == 0
+    h = km.create(lay)
+    reqs, hq, ctx = int(w.page_table.shape[0]), 28, 3 * 1024
+    q = wl.normal_bf16((reqs, hq, lay.head_dim), 1.0, torch.Generator().manual_seed(8), "cpu")
+    ws = torch.empty(km.kamera_decode_attention_workspace(h, reqs, hq, ctx), dtype=torch.uint8,
+                     device="cuda")
+    kb, vb = wl.bf16_bits(k), wl.bf16_bits(v)
+    for layer in (0, 14, 27):
+        out = torch.full((reqs, hq, lay.head_dim), float("nan"), device="cuda")
+        lse = torch.full((reqs, hq), float("nan"), device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        km.kamera_decode_attention(h, km.Pool(k, v, w.page_table.cuda(), w.num_slots), layer,
+                                   q.cuda(), torch.full((reqs,), ctx, dtype=torch.int32,
+                                                        device="cuda"),
+                                   ctx, lay.head_dim ** -0.5, out, lse, ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        compare(lay, kb, vb, kb, vb, w.page_table.numpy(), q, [ctx] * reqs,
+                lay.head_dim ** -0.5, layer, out.cpu().numpy(), lse.cpu().numpy(),
+                pool_diff=False)
+    del k, v, w
+    torch.cuda.empty_cache()
+
+
+def test_form_patch_full():
+    # patch forming at bench size (84 deficits of 1024 x 512, k = 40, m = 32, q = 1), in the
+    # bench's single launch; three sampled problems against the oracle on the same inputs
+    from tests.test_gpu_form import check_problem
+    n, T, W, k, q, m = 84, 1024, 512, 40, 1, 32
+    delta, omega = wl.deficit_problems(n, T, W, k=k, rank=64, decay=0.9, noise=1e-2, seed=0,
+                                       device="cuda")
+    u = torch.full((n, T, m), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vt = torch.full((n, m, W), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sig = torch.full((n, m), float("nan"), device="cuda")
+    ws = torch.empty(km.kamera_form_patch_workspace(n, T, W, k), dtype=torch.uint8, device="cuda")
+    km.kamera_form_patch(delta, omega, k, q, m, u, vt, sig, ws, num_problems=n, T=T, W=W, ld=W,
+                         delta_stride=T * W, omega_stride=0, u_stride=T * m, vt_stride=m * W)
+    torch.cuda.synchronize()
+    assert not torch.isnan(u.float()).any() and not torch.isnan(vt.float()).any()
+    om64 = omega.double().cpu().numpy()
+    for i in (0, 41, 83):
+        check_problem(delta[i].double().cpu().numpy(), om64, q, m,
+                      u[i].float().double().cpu().numpy(), vt[i].float().double().cpu().numpy(),
+                      sig[i].double().cpu().numpy(), need_columns=8)
+    del delta, u, vt, ws
+    torch.cuda.empty_cache()
