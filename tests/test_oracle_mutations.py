@@ -1,8 +1,11 @@
 """The pins must fail when a plausible mistake is planted in the oracle (CPU only).
 
-Each case monkeypatches one oracle function with a wrong variant (a flipped sign, a dropped
-term, a transposed pairing, a patch that is rotated too, a double rounding, an off-by-one
-slot) and checks that at least one pin in tests/test_oracle_pins.py then fails.
+Each case monkeypatches one oracle function with a wrong variant and checks that at least one
+pin in tests/test_oracle_pins.py then fails. The variants: a flipped sign, a dropped term, a
+transposed pairing, a patch that is rotated too, a double rounding, an off-by-one slot, M-RoPE
+offsets or sections taken wrongly, a re-anchoring position of the wrong sign or with its
+coordinates reversed, attention without its scale, an unnormalised split merge, singular
+values in ascending order, and the opposite sign convention.
 """
 import numpy as np
 import pytest
@@ -58,8 +61,67 @@ def off_by_one_slot(page_table, req, tok, page_size):
     return int(page_table[req][tok // page_size]) * page_size + (tok + 1) % page_size
 
 
+def offsets_ignore_sections(layout, item, npairs):
+    return int(item.delta)            # every pair turns by δ_t, the h and w offsets dropped
+
+
+def sections_off_by_one(npairs, sections, style):
+    s_t, s_h, s_w = (int(v) for v in sections)
+    if style == ora.MROPE_CONTIGUOUS:  # the t section one pair too long
+        return np.array([0] * (s_t + 1) + [1] * (s_h - 1) + [2] * s_w)
+    return ora_axes_orig(npairs, sections, style)
+
+
+def token_offsets_wrong_sign(layout, position, npairs):
+    off = ora_token_offsets_orig(layout, position, npairs)
+    return -off if np.ndim(off) == 0 else [-v for v in off]
+
+
+def token_offsets_reversed_coords(layout, position, npairs):
+    if not ora.has_mrope(layout):
+        return int(position)
+    return ora_token_offsets_orig(layout, list(position)[::-1], npairs)  # (w, h, t) for (t, h, w)
+
+
+def attend_without_scale(k, v, q, scale):
+    return ora_attend_orig(k, v, q, 1.0)
+
+
+def merge_unnormalised(parts):
+    lses = np.array([l for _, l in parts], dtype=np.float64)
+    m = np.max(lses)
+    w = np.exp(lses - m)
+    o = sum(wi * np.asarray(oi, np.float64) for wi, (oi, _) in zip(w, parts))  # no / sum(w)
+    return o, m + np.log(np.sum(w))
+
+
+def randomized_ascending(delta, omega, m, q):
+    # eigenvalues taken in ascending order: the smallest directions of the sketch
+    a = np.asarray(delta, np.float64)
+    q_, _ = np.linalg.qr(a @ np.asarray(omega, np.float64))
+    for _ in range(q):
+        z, _ = np.linalg.qr(a.T @ q_)
+        q_, _ = np.linalg.qr(a @ z)
+    bt = a.T @ q_
+    lam, ut = np.linalg.eigh(bt.T @ bt)
+    sig = np.sqrt(np.maximum(lam[:m], 0.0))
+    us = (q_ @ ut[:, :m]) * sig[None, :]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        vt = np.where(sig[:, None] > 0, (bt @ ut[:, :m]).T / sig[:, None], 0.0)
+    return us, vt, sig
+
+
+def sign_rows_flipped(us, vt):
+    us, vt = ora_sign_rows_orig(us, vt)
+    return -us, -vt                   # the largest entry of each row made negative
+
+
 ora_rotate_orig = ora.rotate_band
 ora_f64_to_bf16_orig = ora.f64_to_bf16
+ora_axes_orig = ora.mrope_pair_axes
+ora_token_offsets_orig = ora.token_offsets
+ora_attend_orig = ora.attend
+ora_sign_rows_orig = ora._sign_rows
 
 
 CASES = [
@@ -73,13 +135,28 @@ CASES = [
     ("f64_to_bf16", double_rounding, [pins.test_bf16_ties_to_even_and_single_rounding]),
     ("slot_of", off_by_one_slot, [pins.test_slots_match_independent_page_expansion,
                                   pins.test_identity_mode_scatter_is_byte_exact]),
+    ("pair_offsets", offsets_ignore_sections,
+     [lambda: pins.test_mrope_pair_turns_by_its_section_offset(ora.MROPE_CONTIGUOUS,
+                                                               (16, 24, 24))]),
+    ("mrope_pair_axes", sections_off_by_one, [pins.test_mrope_sections_match_printed_counts]),
+    ("token_offsets", token_offsets_wrong_sign,
+     [pins.test_reanchor_turns_each_token_by_its_own_position]),
+    ("token_offsets", token_offsets_reversed_coords, [pins.test_reanchor_mrope_coordinates]),
+    ("attend", attend_without_scale, [pins.test_attention_closed_forms,
+                                      pins.test_decode_attention_gathers_heads_and_pages]),
+    ("lse_merge", merge_unnormalised, [pins.test_attention_of_a_union_is_the_lse_merge_of_its_parts]),
+    ("form_patch_randomized", randomized_ascending,
+     [pins.test_randomized_patch_recovers_an_exactly_low_rank_deficit,
+      pins.test_randomized_patch_residual_near_the_eckart_young_optimum]),
+    ("_sign_rows", sign_rows_flipped,
+     [pins.test_randomized_patch_recovers_an_exactly_low_rank_deficit]),
 ]
 
 
 @pytest.mark.parametrize("name,bad,checks", CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in CASES])
 def test_planted_mistake_is_caught(monkeypatch, name, bad, checks):
     monkeypatch.setattr(ora, name, bad)
-    caught = [c.__name__ for c in checks if _fails(c)]
+    caught = [getattr(c, "__name__", "pin") for c in checks if _fails(c)]
     assert caught, f"no pin caught the planted {bad.__name__}"
 
 
