@@ -142,7 +142,7 @@ typedef struct kamera_item {
 /*
  * The paged KV pool (§6: the engine's paged KV pool; page size 16 in the reference workloads).
  * k, v      : bf16 [L][num_slots][row]; v is NULL for MLA. 16-byte aligned.
- * num_slots : slots per layer; a multiple of page_size.
+ * num_slots : slots per layer; a multiple of page_size, below 2^31 (UNSUPPORTED otherwise).
  * page_table: int32 [num_reqs][pt_stride] of physical page ids; logical token t of request r
  *             lives at slot page_table[r][t / page_size] * page_size + t % page_size.
  * All device memory, read by the kernels only (page_table) or written (k, v).
@@ -193,6 +193,12 @@ kamera_status kamera_reuse(const kamera_handle *handle, const kamera_item *item,
  * kamera_reuse plus num_tokens <= max_tokens and patch_m <= max_patch_m (a failing item sets
  * KAMERA_DEVICE_BAD_ITEM and is skipped). max_tokens sizes the grid; max_patch_m picks the
  * kernel (0..128).
+ * Shared chunks (§5 "Reorder": one orbit patch serves every ordering of a chunk): valid items
+ * of the same aligned block of 32 consecutive items (items 0-31, 32-63, ...) that name the
+ * same canonical rows, length, factors and patched layers (and, for the columns that turn,
+ * the same offsets) are read and computed once and written to each item's own slots. The
+ * bytes written are those of separate calls; only the reads and arithmetic are shared. On
+ * patched layers the block may be smaller (16, 8, ...) when shared memory is short.
  */
 kamera_status kamera_batch_reuse(const kamera_handle *handle, const kamera_item *d_items,
                                  int32_t num_items, int32_t max_tokens, int32_t max_patch_m,

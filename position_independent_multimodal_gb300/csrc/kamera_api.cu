@@ -120,6 +120,7 @@ kamera_status check_pool(const DevLayout &l, const kamera_pool *p, DevPool *out)
     return KAMERA_ERR_INVALID_ARG;
   }
   if (p->num_slots <= 0 || p->num_slots % l.page_size != 0) return KAMERA_ERR_INVALID_ARG;
+  if (p->num_slots > 0x7FFFFFFFll) return KAMERA_ERR_UNSUPPORTED;  // slots are int32 on device
   if (!p->page_table || p->num_reqs < 1 || p->pt_stride < 1) return KAMERA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(p->page_table) & 3u) != 0) return KAMERA_ERR_INVALID_ARG;
   DevPool d;
@@ -189,13 +190,29 @@ cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, c
 // Unpatched layers always stream through the copy kernel. Patched layers take the per-tile
 // tensor-core kernel on the layouts it serves (with the tensor engine), else the general
 // patched pipeline.
-kamera::SmemPlan reuse_plan(const kamera_handle *h, int max_m) {
+kamera::SmemPlan reuse_plan(const kamera_handle *h, int max_m, int max_run) {
   if (h->engine == kamera::kEngineTensor && kamera::fast_layout(h->lay))
-    return kamera::reuse_tile_plan(h->lay, max_m);
+    return kamera::reuse_tile_plan(h->lay, max_m, max_run);
   return kamera::reuse_smem_plan(h->lay, max_m);
 }
 
 
+
+int env_int(const char *name, int dflt) {
+  const char *e = std::getenv(name);
+  return e ? std::atoi(e) : dflt;
+}
+
+// Most members of a group of shared rows that one CTA writes: the patched-layer kernel and
+// the copy kernel.
+int share_run_tile() {
+  static const int r = env_int("KAMERA_SHARE_RUN_TILE", 3);
+  return r < 1 ? 1 : (r > kamera::kShareBlock ? kamera::kShareBlock : r);
+}
+int share_run_copy() {
+  static const int r = env_int("KAMERA_SHARE_RUN_COPY", 2);
+  return r < 1 ? 1 : (r > 8 ? 8 : r);
+}
 
 }  // namespace
 
@@ -273,7 +290,7 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.max_tokens = item->num_tokens;
   a.max_m = item->patch_m;
   a.engine = h->engine;
-  a.smem = reuse_plan(h, a.max_m);
+  a.smem = reuse_plan(h, a.max_m, 1);
   a.status = d_status;
   a.freq = h->freq;
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
@@ -303,7 +320,8 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
   a.max_tokens = max_tokens;
   a.max_m = max_patch_m;
   a.engine = h->engine;
-  a.smem = reuse_plan(h, a.max_m);
+  a.smem = reuse_plan(h, a.max_m, share_run_tile());
+  a.run_copy = share_run_copy();
   a.status = d_status;
   a.freq = h->freq;
   if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
@@ -375,7 +393,7 @@ kamera_status kamera_patch_inplace(const kamera_handle *h, const kamera_pool *po
   a.max_tokens = num_tokens;
   a.max_m = patch_m;
   a.engine = kamera::kEngineTensor;
-  a.smem = kamera::reuse_tile_plan(h->lay, patch_m);
+  a.smem = kamera::reuse_tile_plan(h->lay, patch_m, 1);
   a.inplace = 1;
   a.sign = sign;
   a.status = d_status;
@@ -408,7 +426,7 @@ kamera_status kamera_batch_patch_inplace(const kamera_handle *h, const kamera_it
   a.max_tokens = max_tokens;
   a.max_m = max_patch_m;
   a.engine = kamera::kEngineTensor;
-  a.smem = kamera::reuse_tile_plan(h->lay, max_patch_m);
+  a.smem = kamera::reuse_tile_plan(h->lay, max_patch_m, 1);
   a.inplace = 1;
   a.sign = sign;
   a.status = d_status;

@@ -45,9 +45,12 @@ struct SmemPlan {
   int canon, stage;      // two stages of [128][pitch] bf16 canonical rows
   int pitch;             // row pitch in bytes (tile width * 2 + 16: rows land on distinct banks)
   int cs, cs_stage;      // two float2 cos/sin tables [npairs]
-  int pages, pages_stage;  // two stages of page ids of the tile's tokens
+  int pages, pages_stage;  // two stages of page ids of the tile's tokens, per run member
+  int pg_per_member;     // page ids per member and stage (tile rows / page size + 2)
   int desc;              // two stage descriptors
-  int slots;             // long long [128]: slot of each row of the tile being stored
+  int slots;             // slots (fast plan: int [run][128], -1 skips) of the tile's rows
+  int members;           // run members' (req, start_tok): int [2][kShareBlock]
+  int run;               // most group members one CTA writes (1: no groups)
   int misc;              // TMEM address (4 B), the MMA mbarrier and the two stage mbarriers
   int total;
   int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
@@ -116,6 +119,7 @@ struct ReuseArgs {
   int engine;                // kEngineTensor or kEngineFma for patched tiles
   int inplace;               // 1: patch re-add on cached rows (read from and written to the pool)
   int sign;                  // inplace: +1 adds U V_m^T, -1 subtracts it
+  int run_copy;              // most group members one CTA of the copy kernel writes
   SmemPlan smem;
   unsigned *status;
   FreqQ64 freq;
@@ -258,6 +262,69 @@ __host__ __device__ inline int anchor_item_check(const kamera_anchor_item &it,
 
 __device__ __forceinline__ bool layer_patched(const kamera_item &it, int layer) {
   return it.patch_m > 0 && layer >= it.patch_l0 && layer < it.patch_l1;
+}
+
+// Shared chunks in a batch. Placements of one chunk (the reorder of §5 puts each chunk in
+// several orderings; one orbit patch serves them all) read the same canonical rows and add the
+// same patch, and where nothing in a tile turns, or it turns by the same offsets, they produce
+// the same bytes. The batch kernels therefore group the items of each aligned block of
+// consecutive items (at most kShareBlock): the lowest valid item of a set of equal sources
+// reads and computes the rows once and writes them to every member's slots.
+constexpr int kShareBlock = 32;
+
+__device__ __forceinline__ bool same_offsets(const kamera_item &a, const kamera_item &b,
+                                             const DevLayout &l) {
+  return a.delta == b.delta && (!l.mrope || (a.delta_h == b.delta_h && a.delta_w == b.delta_w));
+}
+
+// Lane j of a warp loads the channel-ch canonical pointer of item (self's aligned block of
+// kShareBlock items) + j for the group search (null when there is none, or `on` is false).
+__device__ __forceinline__ const void *share_candidate(const kamera_item *items, int n_items,
+                                                       int self, int ch, bool on) {
+  const int j = (self & ~(kShareBlock - 1)) + (int)(threadIdx.x & 31);
+  if (!on || !items || j >= n_items || j == self) return nullptr;
+  return ch == 0 ? items[j].canon_k : items[j].canon_v;
+}
+
+// Called by whole warps for item `self` (its item `me`, its channel's canonical `src`, and
+// each lane's share_candidate `cand`) of a batch: the group of self is every valid item of
+// self's aligned block of kShareBlock items with the same canonical for which `same` holds;
+// its members, in item order, are split into runs of `run` items, and the CTA of each run's
+// first item takes the run. Every lane returns the size of self's run (0: self belongs to a
+// run that another CTA takes). When `record`, the run's requests and first tokens are written
+// to members[f] and members[kShareBlock + f] (f = 0 is self). Other items are read in full
+// only when their canonical pointer equals src.
+template <class Same>
+__device__ __forceinline__ int share_run(const kamera_item *items, int self,
+                                         const kamera_item &me, const void *src,
+                                         const void *cand, int run, int *members, bool record,
+                                         Same same) {
+  const int lane = threadIdx.x & 31;
+  const int b0 = self & ~(kShareBlock - 1);
+  const int j = b0 + lane;
+  const bool is_cand = cand != nullptr && cand == src;
+  bool mem = j == self;
+  int req = me.req, start = me.start_tok;
+  if (__ballot_sync(0xffffffffu, is_cand)) {
+    if (is_cand) {
+      const kamera_item o = items[j];
+      mem = same(o);
+      req = o.req;
+      start = o.start_tok;
+    }
+  }
+  const unsigned mask = __ballot_sync(0xffffffffu, mem);
+  const int f_self = __popc(mask & ((1u << (self - b0)) - 1u));
+  if (f_self % run != 0) return 0;
+  if (mem && record) {
+    const int f = __popc(mask & ((1u << lane) - 1u)) - f_self;
+    if (f >= 0 && f < run) {
+      members[f] = req;
+      members[kShareBlock + f] = start;
+    }
+  }
+  const int left = __popc(mask) - f_self;
+  return left < run ? left : run;
 }
 
 // cos/sin of delta * inv_freq_i: exact modular range reduction in Q0.64 turns, then the
@@ -446,7 +513,7 @@ SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
 bool fast_layout(const DevLayout &l);                               // kamera_reuse_tile.cu
 bool inplace_layout(const DevLayout &l);
-SmemPlan reuse_tile_plan(const DevLayout &l, int max_m);
+SmemPlan reuse_tile_plan(const DevLayout &l, int max_m, int max_run);
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu

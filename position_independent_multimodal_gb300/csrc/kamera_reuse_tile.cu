@@ -46,6 +46,9 @@ __device__ __forceinline__ int lds_i32t(uint32_t a) {
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
+__device__ __forceinline__ void sts_i32t(uint32_t a, int v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 
 // Canonical folded into the accumulator: round and write back. Half h owns the contiguous
 // chunks [h*NC/16, (h+1)*NC/16).
@@ -159,10 +162,13 @@ __device__ __noinline__ void epi_fma(uint32_t x, int r, int half, int nc, int ba
   }
 }
 
-template <int NC, int BAND, bool INPLACE>
+// The tile is computed from item `it` and stored to its slots or, when MULTI, to the slots of
+// nmem group members, whose requests and first tokens are in shared memory at P.members
+// (member 0 is `it`).
+template <int NC, int BAND, bool INPLACE, bool MULTI>
 __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsigned char *sp,
                                           const kamera_item &it, int layer, int ch,
-                                          const Tile &tile) {
+                                          const Tile &tile, int nmem) {
   constexpr int ATOMS = NC / 64;
   constexpr int NCORE = NC / 8;
   const SmemPlan &P = a.smem;
@@ -179,7 +185,11 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
   const uint32_t id_op = s0 + P.desc, pg_op = s0 + P.pages;
   const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
   volatile int *flag = reinterpret_cast<volatile int *>(sp + P.misc + 4);
+  // MULTI: int slot [member][row] (-1 skips); else the global address of each row (0 skips)
   unsigned long long *rowptr = reinterpret_cast<unsigned long long *>(sp + P.slots);
+  const uint32_t slots = s0 + P.slots;
+  auto mreq = [&](int f) { return lds_i32t(s0 + P.members + 4 * f); };
+  auto mstart = [&](int f) { return lds_i32t(s0 + P.members + 4 * (kShareBlock + f)); };
   float *rot = reinterpret_cast<float *>(sp + P.cs);
   const int li = layer - it.patch_l0;
   const __nv_bfloat16 *U = static_cast<const __nv_bfloat16 *>(it.patch_u) +
@@ -231,12 +241,25 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
         }
       }
     }
-    int p_first, off0, npages, dummy;
-    psd.split(it.start_tok + t0, &p_first, &off0);
-    psd.split(off0 + rows - 1, &npages, &dummy);
-    const int32_t *ptab = a.pool.pt + (long long)it.req * a.pool.pt_stride + p_first;
-    for (int e = tid; e <= npages; e += kThrT)
-      ptx::cp_async4(pg_op + s * P.pages_stage + 4 * e, ptab + e);
+    if constexpr (MULTI) {  // page ids of each member's tokens [t0, t0 + rows)
+      const int pgs = P.pg_per_member;
+      for (int e = tid; e < nmem * pgs; e += kThrT) {
+        const int f = e / pgs, k = e - f * pgs;
+        int p_first, off0, npages, dummy;
+        psd.split(mstart(f) + t0, &p_first, &off0);
+        psd.split(off0 + rows - 1, &npages, &dummy);
+        if (k <= npages)
+          ptx::cp_async4(pg_op + s * P.pages_stage + 4 * e,
+                         a.pool.pt + (long long)mreq(f) * a.pool.pt_stride + p_first + k);
+      }
+    } else {
+      int p_first, off0, npages, dummy;
+      psd.split(it.start_tok + t0, &p_first, &off0);
+      psd.split(off0 + rows - 1, &npages, &dummy);
+      const int32_t *ptab = a.pool.pt + (long long)it.req * a.pool.pt_stride + p_first;
+      for (int e = tid; e <= npages; e += kThrT)
+        ptx::cp_async4(pg_op + s * P.pages_stage + 4 * e, ptab + e);
+    }
   };
   // U rows of tile t as the A operand (K-major core matrices). Rows past the chunk stay stale
   // (their accumulator rows are never stored); the rank padding was zeroed once.
@@ -383,7 +406,23 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
         epi_fma(xs, r, half, NC, BAND, u_buf(t), v_op, m, rot, lay.npairs);
       }
     }
-    if (half == 0 && r < rows) {  // the row's owner finds its slot
+    if constexpr (MULTI) {
+      if (r < rows)  // the row's two owners find its slot in each member (alternating)
+        for (int f = half; f < nmem; f += 2) {
+          int pg, in_page, p_first, off0;
+          const int st = mstart(f);
+          psd.split(st + t0 + r, &pg, &in_page);
+          psd.split(st + t0, &p_first, &off0);
+          const int page = lds_i32t(pg_op + s * P.pages_stage +
+                                    4 * (f * P.pg_per_member + pg - p_first));
+          int slot = -1;
+          if (page >= 0 && (long long)(page + 1) * ps <= a.pool.num_slots)
+            slot = page * ps + in_page;
+          else
+            atomicOr(a.status, KAMERA_DEVICE_SLOT_OOB);
+          sts_i32t(slots + 4 * (f * kTileRows + r), slot);
+        }
+    } else if (half == 0 && r < rows) {  // the row's owner finds its slot
       int pg, in_page, p_first, off0;
       psd.split(it.start_tok + t0 + r, &pg, &in_page);
       psd.split(it.start_tok + t0, &p_first, &off0);
@@ -409,7 +448,7 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
     if (use_tc) ptx::tc_fence_before();
     __syncthreads();  // rows of tile t complete, tile t+1 staged
     if (tensor && !timed_out && t + 1 < ntt && tid == 0) issue_mma(t + 1);
-    if (write) {  // 4 rows x 128 bytes per warp instruction
+    if (write && !MULTI) {  // 4 rows x 128 bytes per warp instruction
       const uint32_t src = xs + lr * 128 + swc;
 #pragma unroll
       for (int pr = 0; pr < 4; ++pr) {
@@ -421,6 +460,26 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
             for (int at = 0; at < ATOMS; ++at)
               stg16_global(reinterpret_cast<void *>(dst + 128ull * at + 16ull * lc),
                            lds16(src + at * kAtomT + pr * 32 * 128));
+          }
+        }
+      }
+    } else if (write) {  // the same, once per member
+      const uint32_t src = xs + lr * 128 + swc;
+      const unsigned long long out_base = static_cast<unsigned long long>(
+          __cvta_generic_to_global(pool_ch + (long long)layer * a.pool.num_slots * row + tile.col0));
+      for (int f = 0; f < nmem; ++f) {
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          const int rr = lr + 32 * pr;
+          if (rr < rows) {
+            const int slot = lds_i32t(slots + 4 * (f * kTileRows + rr));
+            if (slot >= 0) {
+              const unsigned long long dst = out_base + (unsigned long long)slot * (2ull * row);
+#pragma unroll
+              for (int at = 0; at < ATOMS; ++at)
+                stg16_global(reinterpret_cast<void *>(dst + 128ull * at + 16ull * lc),
+                             lds16(src + at * kAtomT + pr * 32 * 128));
+            }
           }
         }
       }
@@ -438,6 +497,38 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
   if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
 }
 
+template <bool INPLACE, bool MULTI>
+__device__ __forceinline__ void run_task(const ReuseArgs &a, uint32_t s0, unsigned char *sp,
+                                         const kamera_item &it, int layer, int ch,
+                                         const Tile &tile, int nmem) {
+  if constexpr (MULTI) {
+    if (tile.band == 0) {
+      if (tile.ncols == 128)
+        task_loop<128, 0, false, true>(a, s0, sp, it, layer, ch, tile, nmem);
+      else
+        task_loop<64, 0, false, true>(a, s0, sp, it, layer, ch, tile, nmem);
+    } else if (tile.ncols == 128 && tile.band == 128) {
+      task_loop<128, 128, false, true>(a, s0, sp, it, layer, ch, tile, nmem);
+    } else if (tile.ncols == 128) {
+      task_loop<128, 64, false, true>(a, s0, sp, it, layer, ch, tile, nmem);
+    } else {
+      task_loop<64, 64, false, true>(a, s0, sp, it, layer, ch, tile, nmem);
+    }
+  } else if (INPLACE || tile.band == 0) {
+    if (tile.ncols == 128)
+      task_loop<128, 0, INPLACE, false>(a, s0, sp, it, layer, ch, tile, 1);
+    else
+      task_loop<64, 0, INPLACE, false>(a, s0, sp, it, layer, ch, tile, 1);
+  } else if constexpr (!INPLACE) {
+    if (tile.ncols == 128 && tile.band == 128)
+      task_loop<128, 128, false, false>(a, s0, sp, it, layer, ch, tile, 1);
+    else if (tile.ncols == 128)
+      task_loop<128, 64, false, false>(a, s0, sp, it, layer, ch, tile, 1);
+    else
+      task_loop<64, 64, false, false>(a, s0, sp, it, layer, ch, tile, 1);
+  }
+}
+
 __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_constant__ ReuseArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -447,29 +538,43 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_const
   const int ct = blockIdx.x, item = blockIdx.y;
   const int layer = blockIdx.z / lay.n_ch;
   const int ch = blockIdx.z - layer * lay.n_ch;
+  // canonical pointers of the block's items for the group search, loaded with the item
+  const void *cand = share_candidate(a.items, a.n_items, item, ch, a.smem.run > 1);
   const kamera_item it = a.items ? a.items[item] : a.single;
   // rejected items are reported by the copy kernel; unpatched layers are its work too
   if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) return;
   if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;
   const bool rotate = ch == 0 && item_rotates(it, lay);
   const Tile tile = tile_of(lay, ch, ct, rotate);
-  if (tile.ncols == 128) {
-    if (tile.band == 0)
-      task_loop<128, 0, false>(a, s0, sp, it, layer, ch, tile);
-    else if (tile.band == 128)
-      task_loop<128, 128, false>(a, s0, sp, it, layer, ch, tile);
-    else
-      task_loop<128, 64, false>(a, s0, sp, it, layer, ch, tile);
-  } else {
-    if (tile.band == 0)
-      task_loop<64, 0, false>(a, s0, sp, it, layer, ch, tile);
-    else
-      task_loop<64, 64, false>(a, s0, sp, it, layer, ch, tile);
+  // the tile holds rope columns (all of GQA channel 0, MLA's k_pe tile): group members need
+  // the same offsets as well as the same canonical, length, factors and patched layers
+  const bool has_rope = tile_of(lay, ch, ct, true).band > 0;
+  const void *src = ch == 0 ? it.canon_k : it.canon_v;
+  int nmem = 1;
+  if (a.items && a.smem.run > 1) {
+    // every warp finds the run (the same answer from the same items), so that no barrier is
+    // needed unless the tile has several members; warp 0 records them
+    nmem = share_run(a.items, item, it, src, cand, a.smem.run,
+                     reinterpret_cast<int *>(sp + a.smem.members), threadIdx.x < 32,
+                     [&](const kamera_item &o) {
+                       return o.num_tokens == it.num_tokens && o.patch_u == it.patch_u &&
+                              o.patch_vt == it.patch_vt && o.patch_m == it.patch_m &&
+                              o.patch_l0 == it.patch_l0 && o.patch_l1 == it.patch_l1 &&
+                              (!has_rope || same_offsets(o, it, lay)) &&
+                              item_check(o, lay, a.pool, a.max_tokens, a.max_m) == 0;
+                     });
+    if (nmem == 0) return;       // another CTA writes this tile
+    if (nmem > 1) __syncthreads();  // the members' requests and first tokens are visible
   }
+  // the single-member branch first: the member loops placed ahead of it slowed it by 5 %
+  if (nmem == 1)
+    run_task<false, false>(a, s0, sp, it, layer, ch, tile, 1);
+  else
+    run_task<false, true>(a, s0, sp, it, layer, ch, tile, nmem);
 }
 
 // The patch re-added in place on cached rows: every tile unrotated, rows gathered from and
-// written back to the pool.
+// written back to the pool (no groups: each item's rows are its own).
 __global__ void __launch_bounds__(kThrT, 2) patch_inplace_kernel(const __grid_constant__ ReuseArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -486,10 +591,7 @@ __global__ void __launch_bounds__(kThrT, 2) patch_inplace_kernel(const __grid_co
   }
   if (it.num_tokens <= 0 || !layer_patched(it, layer)) return;
   const Tile tile = tile_of(lay, ch, ct, false);
-  if (tile.ncols == 128)
-    task_loop<128, 0, true>(a, s0, sp, it, layer, ch, tile);
-  else
-    task_loop<64, 0, true>(a, s0, sp, it, layer, ch, tile);
+  run_task<true, false>(a, s0, sp, it, layer, ch, tile, 1);
 }
 
 int align128t(int x) { return (x + 127) & ~127; }
@@ -511,23 +613,24 @@ bool inplace_layout(const DevLayout &l) {
   return l.latent % l.tw == 0 && (l.rope_d == 64 || l.rope_d == 128);
 }
 
-SmemPlan reuse_tile_plan(const DevLayout &l, int max_m) {
+namespace {
+
+// Offsets for runs of up to `run` group members per CTA with `u_bufs` U buffers.
+SmemPlan tile_plan_with(const DevLayout &l, int max_m, int run, int u_bufs) {
   SmemPlan p{};
   int widest = l.tw;
   if (l.kind == KAMERA_MLA && l.rope_d > widest) widest = l.rope_d;
   const int kp = max_m > 0 ? ((max_m + 15) & ~15) : 16;
   p.fast = 1;
+  p.run = run;
+  p.u_bufs = u_bufs;
   p.pitch = widest * 2;
   p.stage = kTileRows * widest * 2;  // a multiple of 1024: the swizzle atoms stay aligned
   p.a_stage = align128t(kTileRows * kp * 2);
   p.b_stage = align128t(widest * kp * 2);
   p.cs_stage = align128t(l.npairs * 12);
-  p.pages_stage = align128t((kTileRows / l.page_size + 2) * 4);
-  const int fixed = 2 * p.stage + p.b_stage + 512 + p.cs_stage + 2 * p.pages_stage +
-                    kTileRows * 8 + 128 + 1024;
-  // two U buffers when two CTAs still fit on an SM (227 KB of shared memory, 1 KB reserved
-  // per CTA), else one
-  p.u_bufs = (fixed + 2 * p.a_stage + 1024) * 2 <= 227 * 1024 ? 2 : 1;
+  p.pg_per_member = kTileRows / l.page_size + 2;
+  p.pages_stage = align128t(run * p.pg_per_member * 4);
   int off = 0;
   p.canon = off;  // two stages of swizzled tiles, first so they stay 1024-aligned
   off += 2 * p.stage;
@@ -541,9 +644,11 @@ SmemPlan reuse_tile_plan(const DevLayout &l, int max_m) {
   off += p.cs_stage;
   p.pages = off;
   off += 2 * p.pages_stage;
-  p.slots = off;  // global addresses of the rows of the tile being stored
-  off += kTileRows * 8;
-  p.misc = off;   // TMEM address, timeout flag, two MMA barriers
+  p.slots = off;  // slot of each row of the tile being stored, per member
+  off += align128t(run * kTileRows * 4 > kTileRows * 8 ? run * kTileRows * 4 : kTileRows * 8);
+  p.members = off;  // members' requests and first tokens
+  off += 2 * kShareBlock * 4;
+  p.misc = off;   // TMEM address, timeout flag, two MMA barriers, member count
   off += 128;
   p.total = off + 1024;  // slack to align the base to 1024 bytes
   int cols = 32;
@@ -551,6 +656,28 @@ SmemPlan reuse_tile_plan(const DevLayout &l, int max_m) {
   p.acc_cols = cols;
   p.tmem_cols = 2 * cols;
   return p;
+}
+
+// CTAs of a plan per SM (227 KB of shared memory, 1 KB reserved per CTA; at most 2).
+int tile_ctas(const SmemPlan &p) {
+  const int n = (227 * 1024) / (p.total + 1024);
+  return n < 2 ? n : 2;
+}
+
+}  // namespace
+
+// Two U buffers when two CTAs still fit on an SM, else one. Runs of group members grow (up to
+// max_run) while the plan keeps its U buffers and CTAs per SM.
+SmemPlan reuse_tile_plan(const DevLayout &l, int max_m, int max_run) {
+  SmemPlan base = tile_plan_with(l, max_m, 1, 2);
+  if (tile_ctas(base) < 2) base = tile_plan_with(l, max_m, 1, 1);
+  SmemPlan best = base;
+  for (int r = 2; r <= max_run && r <= kShareBlock; ++r) {
+    const SmemPlan p = tile_plan_with(l, max_m, r, base.u_bufs);
+    if (tile_ctas(p) < tile_ctas(base)) break;
+    best = p;
+  }
+  return best;
 }
 
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s) {

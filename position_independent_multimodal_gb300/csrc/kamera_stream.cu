@@ -71,20 +71,45 @@ __global__ void __launch_bounds__(kThreads) relocate_kernel(const __grid_constan
 }
 
 constexpr int kCopyRows = 128;
+constexpr int kCopyRun = 8;  // most group members one CTA of the copy kernel writes
 
 // Unpatched layers of reuse items: the canonical rows of (item, layer, channel) stream through
 // registers to their slots, rope columns rotated on the way (R(delta) with no patch term),
-// everything else copied byte for byte. One CTA per 128 rows of an (item, layer, channel);
-// the grid runs items fastest after the row blocks, so placements that share a canonical read
-// it from L2. Patched layers are left to the tensor-core kernel.
-template <bool kFixedUnit>
+// everything else copied byte for byte. One CTA per 128 rows of an (item, layer, channel) that
+// leads a run of group members; each row, rotated once, is stored at every member's slot
+// (rowoff[f][r]: element offset of row r of member f in the layer's pool, -1 skips). The grid
+// runs items fastest after the row blocks, so placements that share a canonical but not a run
+// read it from L2. Patched layers are left to the tensor-core kernel.
+template <bool kFixedUnit, bool kMulti>
 __device__ __forceinline__ void copy_rows(const DevLayout &lay, int ch, bool rotate, int rows,
                                           int row, const __nv_bfloat16 *src0,
-                                          __nv_bfloat16 *pool, const long long *rowoff,
-                                          const float2 *cs) {
+                                          __nv_bfloat16 *pool, const long long (*rowoff)[kCopyRows],
+                                          int nmem, const float2 *cs) {
   const int tid = threadIdx.x;
   const int upr = row >> 4;
   constexpr int B = 2;  // two units (four 16-byte vectors) in flight per thread
+  // one unit of row r (offset off of member 0), rotated if it holds rope pairs, to its slots
+  auto put = [&](const ColUnit &cu, int r, long long off, uint4 va, uint4 vb) {
+    if (cu.rot != 0) {
+      float xa[8], xb[8];
+      unpack8(va, xa);
+      unpack8(vb, xb);
+      rotate_unit(cu, cs, xa, xb);
+      va = pack8_rn(xa);
+      vb = pack8_rn(xb);
+    }
+    if (off >= 0) {
+      st16(pool + off + cu.ca, va);
+      st16(pool + off + cu.cb, vb);
+    }
+    if (kMulti)
+      for (int f = 1; f < nmem; ++f) {
+        const long long o = rowoff[f][r];
+        if (o < 0) continue;
+        st16(pool + o + cu.ca, va);
+        st16(pool + o + cu.cb, vb);
+      }
+  };
   if (kFixedUnit) {
     // upr divides the block: every thread keeps one column unit and walks rows
     const int u = tid % upr, r0 = tid / upr, rstep = kThreads / upr;
@@ -97,7 +122,7 @@ __device__ __forceinline__ void copy_rows(const DevLayout &lay, int ch, bool rot
         const int r = rb + k * rstep;
         off[k] = -1;
         if (r < rows) {
-          off[k] = rowoff[r];
+          off[k] = rowoff[0][r];
           const __nv_bfloat16 *src = src0 + (long long)r * row;
           ra[k] = __ldg(reinterpret_cast<const uint4 *>(src + cu.ca));
           rb_[k] = __ldg(reinterpret_cast<const uint4 *>(src + cu.cb));
@@ -105,19 +130,8 @@ __device__ __forceinline__ void copy_rows(const DevLayout &lay, int ch, bool rot
       }
 #pragma unroll
       for (int k = 0; k < B; ++k) {
-        if (off[k] < 0) continue;
-        __nv_bfloat16 *dst = pool + off[k];
-        if (cu.rot == 0) {
-          st16(dst + cu.ca, ra[k]);
-          st16(dst + cu.cb, rb_[k]);
-        } else {
-          float xa[8], xb[8];
-          unpack8(ra[k], xa);
-          unpack8(rb_[k], xb);
-          rotate_unit(cu, cs, xa, xb);
-          st16(dst + cu.ca, pack8_rn(xa));
-          st16(dst + cu.cb, pack8_rn(xb));
-        }
+        const int r = rb + k * rstep;
+        if (r < rows && (kMulti || off[k] >= 0)) put(cu, r, off[k], ra[k], rb_[k]);
       }
     }
   } else {
@@ -126,47 +140,41 @@ __device__ __forceinline__ void copy_rows(const DevLayout &lay, int ch, bool rot
       uint4 ra[B], rb_[B];
       ColUnit cu[B];
       long long off[B];
+      int rr[B];
 #pragma unroll
       for (int k = 0; k < B; ++k) {
         const int w = base + k * kThreads;
+        rr[k] = -1;
         off[k] = -1;
         if (w < n) {
           const int r = w / upr;
+          rr[k] = r;
           cu[k] = col_unit(lay, ch, w - r * upr, rotate);
-          off[k] = rowoff[r];
+          off[k] = rowoff[0][r];
           const __nv_bfloat16 *src = src0 + (long long)r * row;
           ra[k] = __ldg(reinterpret_cast<const uint4 *>(src + cu[k].ca));
           rb_[k] = __ldg(reinterpret_cast<const uint4 *>(src + cu[k].cb));
         }
       }
 #pragma unroll
-      for (int k = 0; k < B; ++k) {
-        if (off[k] < 0) continue;
-        __nv_bfloat16 *dst = pool + off[k];
-        if (cu[k].rot == 0) {
-          st16(dst + cu[k].ca, ra[k]);
-          st16(dst + cu[k].cb, rb_[k]);
-        } else {
-          float xa[8], xb[8];
-          unpack8(ra[k], xa);
-          unpack8(rb_[k], xb);
-          rotate_unit(cu[k], cs, xa, xb);
-          st16(dst + cu[k].ca, pack8_rn(xa));
-          st16(dst + cu[k].cb, pack8_rn(xb));
-        }
-      }
+      for (int k = 0; k < B; ++k)
+        if (rr[k] >= 0 && (kMulti || off[k] >= 0)) put(cu[k], rr[k], off[k], ra[k], rb_[k]);
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads) reuse_copy_kernel(const __grid_constant__ ReuseArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) reuse_copy_kernel(const __grid_constant__ ReuseArgs a) {
   __shared__ float2 cs[kMaxPairs];
-  __shared__ long long rowoff[kCopyRows];  // element offset of each row in the layer's pool
+  __shared__ long long rowoff[kCopyRun][kCopyRows];  // member f, row r (-1: skipped)
+  __shared__ int members[2 * kShareBlock];  // requests, then first tokens, of the run
+  __shared__ int s_nmem;
   const DevLayout &lay = a.lay;
   const int tid = threadIdx.x;
   const int item = blockIdx.y;
   const int layer = blockIdx.z / lay.n_ch;
   const int ch = blockIdx.z - layer * lay.n_ch;
+  // canonical pointers of the block's items for the group search, loaded with the item
+  const void *cand = share_candidate(a.items, a.n_items, item, ch, a.run_copy > 1 && tid < 32);
   const kamera_item it = a.items ? a.items[item] : a.single;
   if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);
@@ -177,23 +185,58 @@ __global__ void __launch_bounds__(kThreads) reuse_copy_kernel(const __grid_const
   const int rows = min(kCopyRows, it.num_tokens - t0);
   const bool rotate = ch == 0 && item_rotates(it, lay);
   const int row = ch == 0 ? lay.row_k : lay.row_v;
-  if (rotate)
-    for (int i = tid; i < lay.npairs; i += kThreads)
+  const void *src = ch == 0 ? it.canon_k : it.canon_v;
+  if (tid < 32) {
+    // group: valid items of the block with this channel's canonical and length, unpatched on
+    // this layer too, and (channel 0, which holds the rope columns) the same offsets
+    int n = 1;
+    if (a.items && a.run_copy > 1)
+      n = share_run(a.items, item, it, src, cand, a.run_copy, members, true,
+                    [&](const kamera_item &o) {
+                      return o.num_tokens == it.num_tokens && !layer_patched(o, layer) &&
+                             (ch != 0 || same_offsets(o, it, lay)) &&
+                             item_check(o, lay, a.pool, a.max_tokens, a.max_m) == 0;
+                    });
+    if (tid == 0) s_nmem = n;
+  } else if (rotate) {
+    for (int i = tid - 32; i < lay.npairs; i += kThreads - 32)
       cs[i] = rope_phase(a.freq.q[i], pair_delta(it, lay, i));
+  }
+  // member 0 of every run is the CTA's own item: its slots are looked up meanwhile
   for (int r = tid; r < rows; r += kThreads) {
     const long long slot =
         slot_of(a.pool, lay.page_size, it.req, (long long)it.start_tok + t0 + r, a.status);
-    rowoff[r] = slot < 0 ? -1 : slot * row;
+    rowoff[0][r] = slot < 0 ? -1 : slot * row;
   }
   __syncthreads();
-  const __nv_bfloat16 *src0 = static_cast<const __nv_bfloat16 *>(ch == 0 ? it.canon_k
-                                                                          : it.canon_v) +
+  const int nmem = s_nmem;
+  if (nmem == 0) return;  // another CTA writes these rows
+  if (nmem > 1) {
+    for (int e = kCopyRows + tid; e < nmem * kCopyRows; e += kThreads) {
+      const int f = e / kCopyRows, r = e - f * kCopyRows;
+      if (r < rows) {
+        const long long slot = slot_of(a.pool, lay.page_size, members[f],
+                                       (long long)members[kShareBlock + f] + t0 + r, a.status);
+        rowoff[f][r] = slot < 0 ? -1 : slot * row;
+      }
+    }
+    __syncthreads();
+  }
+  const __nv_bfloat16 *src0 = static_cast<const __nv_bfloat16 *>(src) +
                               ((long long)layer * it.num_tokens + t0) * row;
   __nv_bfloat16 *pool = (ch == 0 ? a.pool.k : a.pool.v) + (long long)layer * a.pool.num_slots * row;
-  if (kThreads % (row >> 4) == 0)
-    copy_rows<true>(lay, ch, rotate, rows, row, src0, pool, rowoff, cs);
-  else
-    copy_rows<false>(lay, ch, rotate, rows, row, src0, pool, rowoff, cs);
+  const bool fixed = kThreads % (row >> 4) == 0;
+  if (nmem > 1) {
+    if (fixed)
+      copy_rows<true, true>(lay, ch, rotate, rows, row, src0, pool, rowoff, nmem, cs);
+    else
+      copy_rows<false, true>(lay, ch, rotate, rows, row, src0, pool, rowoff, nmem, cs);
+  } else {
+    if (fixed)
+      copy_rows<true, false>(lay, ch, rotate, rows, row, src0, pool, rowoff, 1, cs);
+    else
+      copy_rows<false, false>(lay, ch, rotate, rows, row, src0, pool, rowoff, 1, cs);
+  }
 }
 
 __global__ void rope_phases_kernel(const __grid_constant__ FreqQ64 f, int npairs,

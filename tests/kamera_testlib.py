@@ -61,10 +61,23 @@ def sentinel_pool(layout: wl.Layout, num_slots: int, device="cuda"):
     return k, v
 
 
-def to_device_items(items, device="cuda"):
+def to_device_items(items, device="cuda", keep_sharing=True):
+    """Items with their tensors on the device. Tensors that several host items share stay
+    shared (one device copy), as a caller's chunk store would be, unless ``keep_sharing`` is
+    False (every item gets its own copies, so no two items name the same rows)."""
     out = []
+    copies = {}
+
+    def mv(t):
+        if t is None:
+            return None
+        if not keep_sharing:
+            return t.to(device)
+        if id(t) not in copies:
+            copies[id(t)] = (t, t.to(device))
+        return copies[id(t)][1]
+
     for it in items:
-        mv = lambda t: None if t is None else t.to(device)
         out.append(dataclasses.replace(it, canon_k=mv(it.canon_k), canon_v=mv(it.canon_v),
                                        patch_u=mv(it.patch_u), patch_vt=mv(it.patch_vt)))
     return out
