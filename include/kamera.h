@@ -196,9 +196,10 @@ kamera_status kamera_reuse(const kamera_handle *handle, const kamera_item *item,
  * Shared chunks (§5 "Reorder": one orbit patch serves every ordering of a chunk): valid items
  * of the same aligned block of 32 consecutive items (items 0-31, 32-63, ...) that name the
  * same canonical rows, length, factors and patched layers (and, for the columns that turn,
- * the same offsets) are read and computed once and written to each item's own slots. The
- * bytes written are those of separate calls; only the reads and arithmetic are shared. On
- * patched layers the block may be smaller (16, 8, ...) when shared memory is short.
+ * the same offsets) form a group. A group's members, in item order, are taken a few at a
+ * time (3 on patched layers, 2 on the others): each such run is read and computed once and
+ * written to each member's own slots. The bytes written are those of separate calls; only
+ * the reads and arithmetic are shared.
  */
 kamera_status kamera_batch_reuse(const kamera_handle *handle, const kamera_item *d_items,
                                  int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
