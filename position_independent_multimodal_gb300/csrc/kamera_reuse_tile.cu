@@ -55,7 +55,7 @@ __device__ __forceinline__ void sts_i32t(uint32_t a, int v) {
 template <int NC>
 __device__ __forceinline__ void epi_fold(uint32_t x, int r, int half, uint32_t trow) {
   constexpr int CH = NC / 16;
-#pragma unroll
+#pragma unroll 1
   for (int q0 = 0; q0 < CH; q0 += 2) {
     const int j0 = half * CH + q0;
     uint32_t acc[16];
@@ -82,7 +82,7 @@ template <int NC, int BAND>
 __device__ __forceinline__ void epi_rot(uint32_t x, int r, int half, uint32_t trow,
                                         const float *rot, int np) {
   constexpr int HB = BAND / 2, PAIRS_HALF = NC / 4, GROUPS = PAIRS_HALF / 8;
-#pragma unroll
+#pragma unroll 1
   for (int q = 0; q < GROUPS; ++q) {
     const int p = half * PAIRS_HALF + q * 8;
     const int head = p / HB, i = p % HB;
