@@ -19,8 +19,11 @@ __device__ __forceinline__ void st16(void *p, const uint4 &v) {
 constexpr int kRelocTile = 32;
 
 // In place: 4 units (8 vectors) are loaded before any is written back, so each thread keeps
-// 128 bytes in flight.
-__global__ void __launch_bounds__(kThreads) relocate_kernel(const __grid_constant__ RelocArgs a) {
+// 128 bytes in flight. kFixed: the row's rope units divide the block, so every thread keeps one
+// column unit and walks rows (at most 85 registers: 3 CTAs per SM); otherwise (row, unit) pairs are
+// dealt out in turn.
+template <bool kFixed>
+__global__ void __launch_bounds__(kThreads, kFixed ? 3 : 1) relocate_kernel(const __grid_constant__ RelocArgs a) {
   __shared__ float2 cs[kMaxPairs];
   __shared__ long long slots[kRelocTile];
   const DevLayout &lay = a.lay;
@@ -36,8 +39,39 @@ __global__ void __launch_bounds__(kThreads) relocate_kernel(const __grid_constan
   const int u_first = lay.kind == KAMERA_GQA ? 0 : (lay.latent >> 4);
   const int n_units = lay.kind == KAMERA_GQA ? (lay.row_k >> 4) : (lay.rope_d >> 4);
   __nv_bfloat16 *pool = a.pool.k + (long long)layer * a.pool.num_slots * lay.row_k;
-  const int n = rows * n_units;
   constexpr int B = 4;
+  if constexpr (kFixed) {
+    // the units divide the block: every thread keeps one column unit and walks rows, B rows
+    // loaded before any is written back
+    const int rstep = kThreads / n_units;
+    const ColUnit cu = col_unit(lay, 0, u_first + tid % n_units, true);
+    for (int rb = tid / n_units; rb < rows; rb += rstep * B) {
+      uint4 ra[B], rb_[B];
+      __nv_bfloat16 *p[B];
+#pragma unroll
+      for (int k = 0; k < B; ++k) {
+        const int r = rb + k * rstep;
+        p[k] = nullptr;
+        if (r < rows && slots[r] >= 0) {
+          p[k] = pool + slots[r] * lay.row_k;
+          ra[k] = *reinterpret_cast<const uint4 *>(p[k] + cu.ca);
+          rb_[k] = *reinterpret_cast<const uint4 *>(p[k] + cu.cb);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < B; ++k) {
+        if (!p[k]) continue;
+        float xa[8], xb[8];
+        unpack8(ra[k], xa);
+        unpack8(rb_[k], xb);
+        rotate_unit(cu, cs, xa, xb);
+        st16(p[k] + cu.ca, pack8_rn(xa));
+        st16(p[k] + cu.cb, pack8_rn(xb));
+      }
+    }
+    return;
+  }
+  const int n = rows * n_units;
   for (int base = tid; base < n; base += kThreads * B) {
     uint4 ra[B], rb[B];
     ColUnit cu[B];
@@ -270,7 +304,11 @@ cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s) {
 
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s) {
   dim3 grid((a.T + kRelocTile - 1) / kRelocTile, a.lay.L);
-  relocate_kernel<<<grid, kThreads, 0, s>>>(a);
+  const int n_units = a.lay.kind == KAMERA_GQA ? (a.lay.row_k >> 4) : (a.lay.rope_d >> 4);
+  if (kThreads % n_units == 0)
+    relocate_kernel<true><<<grid, kThreads, 0, s>>>(a);
+  else
+    relocate_kernel<false><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
