@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--workload", choices=OTHER_WORKLOADS, default=None,
                     help="time only this one of the other workloads and print it (a profiling "
                          "entry point; not the bench line)")
+    ap.add_argument("--survivors-seqs", type=int, default=64,
+                    help="sequences of the sliding-window survival workload (64: the full "
+                         "77 GB K pool; fewer shrink it for profilers that replay the kernel)")
     return ap.parse_args()
 
 
@@ -502,7 +505,7 @@ OTHER_WORKLOADS = ("patch_readd_in_place_18_placements", "decode_attention_reord
                    "form_patch_84_deficits")
 
 
-def other_workloads(dev, only=None):
+def other_workloads(dev, only=None, survivors_seqs=64):
     """Brief timings of the in-place switch, decode attention over the written pool, M-RoPE
     reorder, re-anchoring, MLA recall, sliding-window survival, recall-sweep and
     patch-forming workloads (each a parity-tested configuration of its own); reported beside
@@ -667,7 +670,7 @@ def other_workloads(dev, only=None):
         torch.cuda.empty_cache()
 
     if want("mha_sliding_window_448_survivors"):
-        w = wl.config4(device=dev)
+        w = wl.config4(device=dev, n_seq=survivors_seqs)
         h = km.create(w.layout)
         vd = torch.zeros(1, 1, 8, dtype=torch.bfloat16, device=dev)
         pool = km.Pool(w.k_pool, vd, w.page_table.to(dev), w.num_slots)
@@ -678,12 +681,14 @@ def other_workloads(dev, only=None):
                 km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, st)
         ms = time_calls(reloc, 3)
         moved = sum(sp.num_tokens for sp in w.spans) * w.layout.num_layers * w.layout.row_k * 2 * 2
+        n_seq = len(w.spans)
+        pool_gb = w.k_pool.numel() * 2 / 1e9
         out["mha_sliding_window_448_survivors"] = {
-            "workload": "MHA 32 layers x 32 heads x 128, 64 sequences x 7 survivor chunks of 576 "
-                        "tokens re-rotated in place by delta=-576 (K pool 77 GB)",
+            "workload": f"MHA 32 layers x 32 heads x 128, {n_seq} sequences x 7 survivor chunks of "
+                        f"576 tokens re-rotated in place by delta=-576 (K pool {pool_gb:.0f} GB)",
             "ms_per_step": ms, "gb_s_written": moved / 2 / ms / 1e6,
             "frac_hbm_peak": moved / ms / 1e6 / peak,
-            "chunks_per_s": 448 / ms * 1e3}
+            "chunks_per_s": 7 * n_seq / ms * 1e3}
         del w, pool
         torch.cuda.empty_cache()
 
@@ -836,7 +841,8 @@ def main():
         return
     if args.workload is not None:
         import torch
-        print(json.dumps(other_workloads(torch.device("cuda", local_rank), only=args.workload)))
+        print(json.dumps(other_workloads(torch.device("cuda", local_rank), only=args.workload,
+                                         survivors_seqs=args.survivors_seqs)))
         return
     if world > 1:
         import torch

@@ -160,3 +160,19 @@ def test_out_of_range_page_in_one_member():
         tl.check_rows(lay, oi, layer, 0, None, kb[layer, sl])
     changed = np.any(kb != wl.POOL_SENTINEL_BITS, axis=(0, 2))
     assert changed.sum() == 200 + 200 - 16
+
+
+@pytest.mark.parametrize("m", [0, 16])
+def test_interleaved_pairing_groups_in_the_copy_kernel(m):
+    # interleaved pairs take the general patched-layer kernel (no groups there); unpatched
+    # layers still go through the grouped copy kernel
+    lay = dataclasses.replace(gqa(H=2, hd=64), rope_style=wl.INTERLEAVED)
+    check_grouped(orderings(lay, m, f"shareil{m}"), n_shared_min=4)
+
+
+@pytest.mark.parametrize("kind", ["gqa", "mla"])
+def test_cuda_core_engine_with_shared_chunks(kind, monkeypatch):
+    # the CUDA-core patch engine (general kernel) beside the grouped copy kernel
+    monkeypatch.setenv("KAMERA_PATCH_ENGINE", "fma")
+    lay = gqa(H=4, hd=128) if kind == "gqa" else mla()
+    check_grouped(orderings(lay, 16, f"sharefma{kind}"), n_shared_min=4)
