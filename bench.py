@@ -278,6 +278,92 @@ def cpu_baseline(target_s: float):
                       f"per core, {wall:.1f} s wall"}
 
 
+def _oracle_per_chunk(threads: int):
+    """µs per chunk of the float64 oracle on the tiny GQA workload (in full) and on timed units
+    of the MLA recall, sliding-window and recall-sweep workloads (extrapolated linearly to a
+    whole chunk). Runs in a fresh process whose BLAS / OpenMP thread count is `threads`."""
+    import workloads as wl
+    from oracle import kamera_oracle as ora
+
+    def oitem(it):
+        b = lambda t: None if t is None else wl.bf16_bits(t)
+        return ora.as_item(canon_k=b(it.canon_k), canon_v=b(it.canon_v), patch_u=b(it.patch_u),
+                           patch_vt=b(it.patch_vt), delta=it.delta, num_tokens=it.num_tokens,
+                           req=it.req, start_tok=it.start_tok, patch_m=it.patch_m,
+                           patch_l0=it.patch_l0, patch_l1=it.patch_l1, delta_h=it.delta_h,
+                           delta_w=it.delta_w)
+
+    def timed(fn):  # best of two runs
+        best = None
+        for _ in range(2):
+            t = time.perf_counter()
+            fn()
+            dt = time.perf_counter() - t
+            best = dt if best is None else min(best, dt)
+        return best
+
+    out = {}
+    # tiny GQA: the whole chunk, every layer and channel
+    w = wl.config1(strong=True)
+    it = oitem(w.items[0])
+    units = [(l, c) for l in range(w.layout.num_layers) for c in range(2)]
+    dt = timed(lambda: [ora.reuse_layer_bits(w.layout, it, l, c) for l, c in units])
+    out["tiny_gqa"] = {"us_per_chunk": dt * 1e6, "sample": "the whole chunk (2 layers x K, V)"}
+    # MLA recall: one unpatched and one patched layer of one chunk, x13 and x14
+    w = wl.config3(n_chunks=1)
+    it = oitem(w.items[0])
+    t0 = timed(lambda: ora.reuse_layer_bits(w.layout, it, 0, 0))
+    t1 = timed(lambda: ora.reuse_layer_bits(w.layout, it, 13, 0))
+    out["mla_recall"] = {"us_per_chunk": (13 * t0 + 14 * t1) * 1e6,
+                         "sample": "layers 0 and 13 of one chunk, extrapolated to 13 unpatched "
+                                   "and 14 patched layers"}
+    # sliding window: 64 survivor tokens of one layer, extrapolated to 576 tokens x 32 layers
+    w = wl.config4(n_seq=1, layers=1)
+    pool = wl.bf16_bits(w.k_pool).copy()
+    pt = w.page_table.numpy()
+    sp = w.spans[0]
+    t2 = timed(lambda: ora.relocate(w.layout, pool, pt, sp.req, sp.start_tok, 64, sp.delta))
+    out["mha_sliding_window"] = {"us_per_chunk": t2 * (576 / 64) * 32 * 1e6,
+                                 "sample": "64 survivor tokens of one layer, extrapolated to "
+                                           "576 tokens x 32 layers"}
+    # recall sweep: K and V of one unpatched and one patched layer, x32 each
+    w = wl.config5(n_req=1, recalls=1)
+    unp = oitem(wl.config5_launch_items(w, 0)[0])
+    pat = oitem(wl.config5_launch_items(w, 4)[0])
+    t3 = timed(lambda: [ora.reuse_layer_bits(w.layout, unp, 0, c) for c in range(2)])
+    t4 = timed(lambda: [ora.reuse_layer_bits(w.layout, pat, 0, c) for c in range(2)])
+    out["gqa_recall_sweep"] = {"us_per_chunk": 32 * (t3 + t4) * 1e6,
+                               "sample": "K and V of one unpatched and one patched layer, "
+                                         "extrapolated to 32 of each"}
+    return out
+
+
+def _oracle_per_chunk_in(threads: int):
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = str(threads)
+    import torch
+    torch.set_num_threads(threads)
+    return _oracle_per_chunk(threads)
+
+
+def oracle_per_chunk():
+    """The oracle per chunk of the other reference workloads, at 1 thread and at all threads
+    (each in its own spawned process, so the thread count applies before NumPy loads)."""
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    res = {}
+    for threads in (1, cores):
+        with ctx.Pool(1) as pool:
+            res[threads] = pool.apply(_oracle_per_chunk_in, (threads,))
+    out = {"kind": "oracle", "cores": cores, "extrapolated": True,
+           "unit": "us per chunk (a chunk across all its layers)"}
+    for name in res[1]:
+        out[name] = {"us_1_thread": res[1][name]["us_per_chunk"],
+                     f"us_{cores}_threads": res[cores][name]["us_per_chunk"],
+                     "sample": res[1][name]["sample"]}
+    return out
+
+
 def reference_arm(args, rank):
     if rank != 0:
         return
@@ -434,9 +520,10 @@ def kamera_arm(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_other_workloads:
         others = other_workloads(dev)
 
-    cpu = None
+    cpu = cpu_chunks = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
+        cpu_chunks = oracle_per_chunk()
 
     if rank != 0:
         return
@@ -482,6 +569,8 @@ def kamera_arm(args, rank, world, local_rank):
         line["other_workloads"] = others
     if cpu:
         line["cpu_baseline"] = cpu
+    if cpu_chunks:
+        line["cpu_baseline_per_chunk"] = cpu_chunks
     print(json.dumps(line), flush=True)
 
 
