@@ -588,7 +588,8 @@ def time_calls(fn, steps, warmup=1):
     return e0.elapsed_time(e1) / steps
 
 
-OTHER_WORKLOADS = ("patch_readd_in_place_18_placements", "decode_attention_reorder_pool",
+OTHER_WORKLOADS = ("tiny_gqa_one_chunk", "patch_readd_in_place_18_placements",
+                   "decode_attention_reorder_pool",
                    "mrope_reorder_18_placements", "reanchor_18_placements", "mla_recall_64_chunks",
                    "mha_sliding_window_448_survivors", "gqa_recall_sweep_1024_items",
                    "form_patch_84_deficits")
@@ -743,6 +744,30 @@ def other_workloads(dev, only=None, survivors_seqs=64):
             "ms_per_call": ms, "gb_s_written": written / ms / 1e6,
             "frac_hbm_peak": (written + read) / ms / 1e6 / peak}
         del w, k, v, pool, d_items
+        torch.cuda.empty_cache()
+
+    if want("tiny_gqa_one_chunk"):
+        # the correctness-sized workload: one 256-token chunk, 2 layers, one kamera_reuse call
+        # (launch- and latency-bound at this size)
+        w = wl.config1(device=dev, strong=True)
+        acc = accounting(w)
+        lay = w.layout
+        h = km.create(lay)
+        k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+        pool = km.Pool(k, torch.empty_like(k), w.page_table.to(dev), w.num_slots)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        it = w.items[0]
+        ms = time_calls(lambda: km.kamera_reuse(h, it, pool, st), 500, warmup=20)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        out["tiny_gqa_one_chunk"] = {
+            "workload": "GQA 2 layers, H_kv=2 x 64, one chunk T=256 relocated by delta=1000, "
+                        "m=8 patch on both layers (one kamera_reuse call)",
+            "us_per_call": ms * 1e3, "gb_s_written": acc["written"] / ms / 1e6,
+            "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
+            "chunks_per_s": 1 / ms * 1e3}
+        del w, k, pool
         torch.cuda.empty_cache()
 
     if want("mla_recall_64_chunks"):
