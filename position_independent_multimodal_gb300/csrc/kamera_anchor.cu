@@ -80,29 +80,54 @@ __global__ void __launch_bounds__(kThr) reanchor_kernel(const __grid_constant__ 
   __nv_bfloat16 *pool0 = ch == 0 ? a.pool.k : a.pool.v;
   const int upr = row >> 4;  // 16-column units per row
   if (kThr % upr == 0 && kRows % (kThr / upr) == 0) {
-    // every thread keeps one column unit and walks the rows r0, r0 + rstep, ... of each layer
+    // every thread keeps one column unit and walks the rows r0, r0 + rstep, ...; a row's
+    // phases are read once into registers and turn the row in all of the CTA's layers, whose
+    // loads are all in flight before the first store
     const int u = tid % upr, r0 = tid / upr, rstep = kThr / upr;
-    const int per = kRows / rstep;
     const ColUnit cu = col_unit(lay, ch, u, rotate);
-    for (int layer = l0; layer < l1; ++layer) {
-      const __nv_bfloat16 *src0 = canon + ((long long)layer * it.num_tokens + t0) * row;
-      __nv_bfloat16 *pool = pool0 + (long long)layer * a.pool.num_slots * row;
-      for (int b = 0; b < per; b += 4) {  // four rows in flight
-        uint4 ra[4], rb[4];
+    const int nl = l1 - l0;
+    for (int r = r0; r < rows; r += rstep) {
+      const long long off = rowoff[r];
+      if (off < 0) continue;
+      uint4 ra[kLayers], rb[kLayers];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int r = r0 + (b + k) * rstep;
-          if (b + k < per && r < rows) {
-            const __nv_bfloat16 *src = src0 + (long long)r * row;
-            ra[k] = __ldg(reinterpret_cast<const uint4 *>(src + cu.ca));
-            rb[k] = __ldg(reinterpret_cast<const uint4 *>(src + cu.cb));
-          }
+      for (int l = 0; l < kLayers; ++l) {
+        if (l < nl) {
+          const __nv_bfloat16 *src = canon + ((long long)(l0 + l) * it.num_tokens + t0 + r) * row;
+          ra[l] = __ldg(reinterpret_cast<const uint4 *>(src + cu.ca));
+          rb[l] = __ldg(reinterpret_cast<const uint4 *>(src + cu.cb));
         }
+      }
+      float2 c[8];  // NeoX: pairs fa..fa+7; interleaved: fa..fa+3 then fb..fb+3
+      if (cu.rot != 0) {
+        const float2 *row_cs = cs + r * np;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int r = r0 + (b + k) * rstep;
-          if (b + k < per && r < rows && rowoff[r] >= 0)
-            store_unit(pool + rowoff[r], cu, ra[k], rb[k], cs + r * np);
+        for (int e = 0; e < 8; ++e)
+          c[e] = cu.rot == 1 ? row_cs[cu.fa + e] : row_cs[(e < 4 ? cu.fa : cu.fb - 4) + e];
+      }
+#pragma unroll
+      for (int l = 0; l < kLayers; ++l) {
+        if (l >= nl) break;
+        __nv_bfloat16 *dst = pool0 + (long long)(l0 + l) * a.pool.num_slots * row + off;
+        if (cu.rot == 0) {
+          st16(dst + cu.ca, ra[l]);
+          st16(dst + cu.cb, rb[l]);
+        } else {
+          float xa[8], xb[8];
+          unpack8(ra[l], xa);
+          unpack8(rb[l], xb);
+          if (cu.rot == 1) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rot_pair(xa[e], xb[e], c[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              rot_pair(xa[e], xa[e + 1], c[e >> 1]);
+              rot_pair(xb[e], xb[e + 1], c[4 + (e >> 1)]);
+            }
+          }
+          st16(dst + cu.ca, pack8_rn(xa));
+          st16(dst + cu.cb, pack8_rn(xb));
         }
       }
     }

@@ -167,8 +167,13 @@ SideStream *side_stream() {
 
 // Patched layers on the caller's stream, unpatched layers on the side stream at the same time
 // (layouts served by the tile kernel); otherwise the two kernels in order on the caller's
-// stream.
-cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, cudaStream_t s) {
+// stream. `unpatched` false (a single item patched on every layer, checked on the host): the
+// copy kernel would have nothing to do, so only the patched-layer kernel is launched.
+cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, cudaStream_t s,
+                        bool unpatched = true) {
+  if (patched && !unpatched)
+    return a.smem.fast ? kamera::launch_reuse_tile(a, n_items, s)
+                       : kamera::launch_reuse(a, n_items, s);
   SideStream *ss = (a.smem.fast && patched) ? side_stream() : nullptr;
   if (!ss) {
     cudaError_t e = kamera::launch_reuse_copy(a, s);
@@ -295,8 +300,9 @@ kamera_status kamera_reuse(const kamera_handle *h, const kamera_item *item,
   a.freq = h->freq;
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
   // unpatched layers stream through registers; patched layers take the tensor-core pipeline
-  return from_cuda(
-      launch_both(a, 1, item->patch_m > 0 && item->patch_l1 > item->patch_l0, strm));
+  const bool patched = item->patch_m > 0 && item->patch_l1 > item->patch_l0;
+  const bool all_patched = patched && item->patch_l0 == 0 && item->patch_l1 == h->lay.L;
+  return from_cuda(launch_both(a, 1, patched, strm, !all_patched));
 }
 
 namespace {
