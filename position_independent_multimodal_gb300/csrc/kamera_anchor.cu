@@ -98,13 +98,8 @@ __global__ void __launch_bounds__(kThr) reanchor_kernel(const __grid_constant__ 
           rb[l] = __ldg(reinterpret_cast<const uint4 *>(src + cu.cb));
         }
       }
-      float2 c[8];  // NeoX: pairs fa..fa+7; interleaved: fa..fa+3 then fb..fb+3
-      if (cu.rot != 0) {
-        const float2 *row_cs = cs + r * np;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          c[e] = cu.rot == 1 ? row_cs[cu.fa + e] : row_cs[(e < 4 ? cu.fa : cu.fb - 4) + e];
-      }
+      float2 c[8];
+      if (cu.rot != 0) unit_phases(cu, cs + r * np, c);
 #pragma unroll
       for (int l = 0; l < kLayers; ++l) {
         if (l >= nl) break;
@@ -116,16 +111,7 @@ __global__ void __launch_bounds__(kThr) reanchor_kernel(const __grid_constant__ 
           float xa[8], xb[8];
           unpack8(ra[l], xa);
           unpack8(rb[l], xb);
-          if (cu.rot == 1) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) rot_pair(xa[e], xb[e], c[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              rot_pair(xa[e], xa[e + 1], c[e >> 1]);
-              rot_pair(xb[e], xb[e + 1], c[4 + (e >> 1)]);
-            }
-          }
+          rotate_unit_with(cu, c, xa, xb);
           st16(dst + cu.ca, pack8_rn(xa));
           st16(dst + cu.cb, pack8_rn(xb));
         }

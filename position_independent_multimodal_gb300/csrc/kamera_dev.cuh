@@ -487,6 +487,29 @@ __device__ __forceinline__ void rotate_unit(const ColUnit &c, const float2 *cs, 
   }
 }
 
+// The eight (cos, sin) a unit's rotation reads, for keeping in registers while a thread turns
+// the same unit of many rows: NeoX pairs fa..fa+7; interleaved fa..fa+3, then fb..fb+3.
+__device__ __forceinline__ void unit_phases(const ColUnit &c, const float2 *cs, float2 *p) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    p[e] = c.rot == 1 ? cs[c.fa + e] : cs[(e < 4 ? c.fa : c.fb - 4) + e];
+}
+
+// rotate_unit with the phases of unit_phases.
+__device__ __forceinline__ void rotate_unit_with(const ColUnit &c, const float2 *p, float *xa,
+                                                 float *xb) {
+  if (c.rot == 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rot_pair(xa[e], xb[e], p[e]);
+  } else if (c.rot == 2) {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      rot_pair(xa[e], xa[e + 1], p[e >> 1]);
+      rot_pair(xb[e], xb[e + 1], p[4 + (e >> 1)]);
+    }
+  }
+}
+
 // Patch forming (kamera_form.cu): one problem is a float32 deficit [T x W].
 constexpr int kMaxSketch = 96;            // sketch width k
 constexpr int kMaxFormSmem = 232448;      // shared memory per block (opt-in limit of sm_103a)
