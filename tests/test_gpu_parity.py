@@ -281,17 +281,49 @@ def test_rope_phases_range_reduction(theta, d):
     km.kamera_rope_phases(h, torch.from_numpy(deltas).cuda(), out)
     torch.cuda.synchronize()
     got = out.cpu().numpy().astype(np.float64)
-    # reference angles reduced exactly with Python integers and fractions of a turn
-    from fractions import Fraction
-    inv = ora.inv_freq(theta, d)
+    want = phase_reference(theta, d, deltas)
+    bad = np.argwhere(np.abs(got - want) > 2.0 ** -22)
+    assert bad.size == 0, [(int(deltas[a]), int(i), got[a, i], want[a, i]) for a, i, _ in bad[:5]]
+
+
+def phase_reference(theta, d, deltas):
+    """(cos, sin) of δ·inv_freq_i with the angle reduced exactly: δ times the float64 inv_freq_i
+    as a rational number of turns of the float64 2π, the fractional turn taken exactly."""
     import math
+    from fractions import Fraction
+    inv = [Fraction(float(x)) for x in ora.inv_freq(theta, d)]
+    two_pi = Fraction(2 * math.pi)
+    out = np.empty((len(deltas), d // 2, 2))
     for a, dl in enumerate(deltas):
-        for i in range(d // 2):
-            turns = Fraction(int(dl)) * Fraction(float(inv[i])) / Fraction(2 * math.pi)
+        for i, f in enumerate(inv):
+            turns = Fraction(int(dl)) * f / two_pi
             frac = float(turns - math.floor(turns))
-            c, s = math.cos(2 * math.pi * frac), math.sin(2 * math.pi * frac)
-            assert abs(got[a, i, 0] - c) <= 2.0 ** -22, (dl, i, got[a, i], c, s)
-            assert abs(got[a, i, 1] - s) <= 2.0 ** -22, (dl, i, got[a, i], c, s)
+            out[a, i] = (math.cos(2 * math.pi * frac), math.sin(2 * math.pi * frac))
+    return out
+
+
+@pytest.mark.parametrize("workload", ["tiny", "reorder", "mla_recall", "sliding_window",
+                                      "recall_sweep"])
+def test_rope_phases_every_offset_of_the_reference_workloads(workload):
+    # every (δ, pair) the five reference workloads use, with their θ and rotary width, against
+    # the exactly reduced angle; 2^-22 absolute: one float32 ulp near 1 of the sincospi result
+    # plus the Q0.64 table's |δ|·2^-65 turns
+    theta, d, deltas = {
+        "tiny": (1e4, 64, [1000]),
+        "reorder": (1e6, 128, [0, 1024, 2048]),
+        "mla_recall": (1e4, 64, wl.config3_deltas()),
+        "sliding_window": (1e4, 128, [-576]),
+        "recall_sweep": (1e6, 128, wl.config5_deltas()),
+    }[workload]
+    h = km.create(gqa_layout(H=1, hd=d, theta=theta))
+    dl = np.asarray(deltas, dtype=np.int64)
+    out = torch.empty(len(dl), d // 2, 2, dtype=torch.float32, device="cuda")
+    km.kamera_rope_phases(h, torch.from_numpy(dl).cuda(), out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    want = phase_reference(theta, d, dl)
+    bad = np.argwhere(np.abs(got - want) > 2.0 ** -22)
+    assert bad.size == 0, [(int(dl[a]), int(i), got[a, i], want[a, i]) for a, i, _ in bad[:5]]
 
 
 def test_empty_inputs_launch_nothing():

@@ -344,14 +344,25 @@ def config_reanchor(seed: int = 0, device="cpu") -> Workload:
                            seed=seed, device=device)
 
 
+def config3_deltas(seed: int = 0, n_chunks: int = 64) -> list:
+    """The MLA recall workload's offsets: δ ~ U[-32768, 32768] per chunk."""
+    g = _gen("cpu", seed, "cfg3", "delta")
+    return torch.randint(-32768, 32769, (n_chunks,), generator=g).tolist()
+
+
+def config5_deltas(seed: int = 0, n_items: int = 1024) -> list:
+    """The recall sweep's offsets: δ ~ U[0, 131072) per item."""
+    g = _gen("cpu", seed, "cfg5", "delta")
+    return torch.randint(0, 131072, (n_items,), generator=g).tolist()
+
+
 def config3(seed: int = 0, device="cpu", n_chunks: int = 64) -> Workload:
     """MLA (DeepSeek-V2-Lite-shaped): 27 layers, c_KV 512 ‖ k_pe 64, θ=1e4, T=1024 chunks each
     recalled into its own request at δ ~ U[-32768, 32768], m=32 on both groups for layers
     13–26. The paper's setting is one chunk; ``n_chunks`` of them form the batch."""
     lay = Layout(kind=MLA, num_layers=27, page_size=16, latent_dim=512, rope_dim=64,
                  rope_style=NEOX_HALF, rope_theta=1e4)
-    g = _gen("cpu", seed, "cfg3", "delta")
-    deltas = torch.randint(-32768, 32769, (n_chunks,), generator=g).tolist()
+    deltas = config3_deltas(seed, n_chunks)
     placements = [(c, c, 0, deltas[c]) for c in range(n_chunks)]
     return reuse_workload("cfg3", lay, n_chunks=n_chunks, T=1024, placements=placements,
                           m=32, l0=13, l1=27, seed=seed, device=device)
@@ -393,8 +404,7 @@ def config5(seed: int = 0, device="cpu", n_req: int = 256, recalls: int = 4,
                       rope_dim=128, rope_style=NEOX_HALF, rope_theta=1e6)
     lay = dataclasses.replace(lay_full, num_layers=Ls)
     n_items = n_req * recalls
-    g = _gen("cpu", seed, "cfg5", "delta")
-    deltas = torch.randint(0, 131072, (n_items,), generator=g).tolist()
+    deltas = config5_deltas(seed, n_items)
     ppr = recalls * T // lay.page_size
     pt = shuffled_page_table(n_req, ppr, _gen("cpu", seed, "cfg5", "pages"))
     W = lay.row_k
