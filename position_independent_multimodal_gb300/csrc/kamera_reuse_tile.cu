@@ -536,8 +536,11 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_const
   unsigned char *sp = smem_raw + (s0 - raw);
   const DevLayout &lay = a.lay;
   const int ct = blockIdx.x, item = blockIdx.y;
-  const int layer = blockIdx.z / lay.n_ch;
-  const int ch = blockIdx.z - layer * lay.n_ch;
+  // top layers first: the reference models patch the upper layers, so the CTAs of unpatched
+  // layers (which return at once) come last, into the slots the tail leaves idle, instead of
+  // filling the machine before any work starts (9 us of the reorder step's 162)
+  const int layer = lay.L - 1 - (int)blockIdx.z / lay.n_ch;
+  const int ch = (int)blockIdx.z % lay.n_ch;
   // canonical pointers of the block's items for the group search, loaded with the item
   const void *cand = share_candidate(a.items, a.n_items, item, ch, a.smem.run > 1);
   const kamera_item it = a.items ? a.items[item] : a.single;
@@ -582,8 +585,8 @@ __global__ void __launch_bounds__(kThrT, 2) patch_inplace_kernel(const __grid_co
   unsigned char *sp = smem_raw + (s0 - raw);
   const DevLayout &lay = a.lay;
   const int ct = blockIdx.x, item = blockIdx.y;
-  const int layer = blockIdx.z / lay.n_ch;
-  const int ch = blockIdx.z - layer * lay.n_ch;
+  const int layer = lay.L - 1 - (int)blockIdx.z / lay.n_ch;  // top layers first, as above
+  const int ch = (int)blockIdx.z % lay.n_ch;
   const kamera_item it = a.items ? a.items[item] : a.single;
   if (a.items && inplace_item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
     if (ct == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);
