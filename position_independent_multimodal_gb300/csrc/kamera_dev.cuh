@@ -277,41 +277,37 @@ __device__ __forceinline__ bool same_offsets(const kamera_item &a, const kamera_
   return a.delta == b.delta && (!l.mrope || (a.delta_h == b.delta_h && a.delta_w == b.delta_w));
 }
 
-// Lane j of a warp loads the channel-ch canonical pointer of item (self's aligned block of
-// kShareBlock items) + j for the group search (null when there is none, or `on` is false).
-__device__ __forceinline__ const void *share_candidate(const kamera_item *items, int n_items,
-                                                       int self, int ch, bool on) {
+// Lane j of a warp loads item (self's aligned block of kShareBlock items) + j for the group
+// search, with the CTA's own item: the whole item, so that the search needs one round trip.
+// Returns false (and leaves *o alone) when there is no such item or `on` is false.
+__device__ __forceinline__ bool share_candidate(const kamera_item *items, int n_items, int self,
+                                                bool on, kamera_item *o) {
   const int j = (self & ~(kShareBlock - 1)) + (int)(threadIdx.x & 31);
-  if (!on || !items || j >= n_items || j == self) return nullptr;
-  return ch == 0 ? items[j].canon_k : items[j].canon_v;
+  if (!on || !items || j >= n_items || j == self) return false;
+  *o = items[j];
+  return true;
 }
 
 // Called by whole warps for item `self` (its item `me`, its channel's canonical `src`, and
-// each lane's share_candidate `cand`) of a batch: the group of self is every valid item of
-// self's aligned block of kShareBlock items with the same canonical for which `same` holds;
-// its members, in item order, are split into runs of `run` items, and the CTA of each run's
-// first item takes the run. Every lane returns the size of self's run (0: self belongs to a
-// run that another CTA takes). When `record`, the run's requests and first tokens are written
-// to members[f] and members[kShareBlock + f] (f = 0 is self). Other items are read in full
-// only when their canonical pointer equals src.
+// each lane's share_candidate item `cand` when `has_cand`) of a batch: the group of self is
+// every valid item of self's aligned block of kShareBlock items with the same canonical for
+// which `same` holds; its members, in item order, are split into runs of `run` items, and the
+// CTA of each run's first item takes the run. Every lane returns the size of self's run (0:
+// self belongs to a run that another CTA takes). When `record`, the run's requests and first
+// tokens are written to members[f] and members[kShareBlock + f] (f = 0 is self).
 template <class Same>
-__device__ __forceinline__ int share_run(const kamera_item *items, int self,
-                                         const kamera_item &me, const void *src,
-                                         const void *cand, int run, int *members, bool record,
-                                         Same same) {
+__device__ __forceinline__ int share_run(int self, const kamera_item &me, const void *src, int ch,
+                                         bool has_cand, const kamera_item &cand, int run,
+                                         int *members, bool record, Same same) {
   const int lane = threadIdx.x & 31;
   const int b0 = self & ~(kShareBlock - 1);
   const int j = b0 + lane;
-  const bool is_cand = cand != nullptr && cand == src;
   bool mem = j == self;
   int req = me.req, start = me.start_tok;
-  if (__ballot_sync(0xffffffffu, is_cand)) {
-    if (is_cand) {
-      const kamera_item o = items[j];
-      mem = same(o);
-      req = o.req;
-      start = o.start_tok;
-    }
+  if (has_cand && (ch == 0 ? cand.canon_k : cand.canon_v) == src && same(cand)) {
+    mem = true;
+    req = cand.req;
+    start = cand.start_tok;
   }
   const unsigned mask = __ballot_sync(0xffffffffu, mem);
   const int f_self = __popc(mask & ((1u << (self - b0)) - 1u));

@@ -467,8 +467,8 @@ __global__ void __launch_bounds__(kThr, 2) reuse_kernel(const __grid_constant__ 
   const DevLayout &lay = a.lay;
   // this CTA's task: column tile, item, (layer, channel)
   const int ct = blockIdx.x, item = blockIdx.y;
-  const int layer = blockIdx.z / lay.n_ch;
-  const int ch = blockIdx.z - layer * lay.n_ch;
+  const int layer = lay.L - 1 - (int)blockIdx.z / lay.n_ch;  // top layers first (see the tile kernel)
+  const int ch = (int)blockIdx.z % lay.n_ch;
   const kamera_item it = a.items ? a.items[item] : a.single;
   if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
     if (ct == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);

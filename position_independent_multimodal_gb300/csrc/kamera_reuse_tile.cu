@@ -542,7 +542,8 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_const
   const int layer = lay.L - 1 - (int)blockIdx.z / lay.n_ch;
   const int ch = (int)blockIdx.z % lay.n_ch;
   // canonical pointers of the block's items for the group search, loaded with the item
-  const void *cand = share_candidate(a.items, a.n_items, item, ch, a.smem.run > 1);
+  kamera_item cand;
+  const bool has_cand = share_candidate(a.items, a.n_items, item, a.smem.run > 1, &cand);
   const kamera_item it = a.items ? a.items[item] : a.single;
   // rejected items are reported by the copy kernel; unpatched layers are its work too
   if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) return;
@@ -557,7 +558,7 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_tile_kernel(const __grid_const
   if (a.items && a.smem.run > 1) {
     // every warp finds the run (the same answer from the same items), so that no barrier is
     // needed unless the tile has several members; warp 0 records them
-    nmem = share_run(a.items, item, it, src, cand, a.smem.run,
+    nmem = share_run(item, it, src, ch, has_cand, cand, a.smem.run,
                      reinterpret_cast<int *>(sp + a.smem.members), threadIdx.x < 32,
                      [&](const kamera_item &o) {
                        return o.num_tokens == it.num_tokens && o.patch_u == it.patch_u &&

@@ -208,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 4) reuse_copy_kernel(const __grid_co
   const int layer = blockIdx.z / lay.n_ch;
   const int ch = blockIdx.z - layer * lay.n_ch;
   // canonical pointers of the block's items for the group search, loaded with the item
-  const void *cand = share_candidate(a.items, a.n_items, item, ch, a.run_copy > 1 && tid < 32);
+  kamera_item cand;
+  const bool has_cand = share_candidate(a.items, a.n_items, item, a.run_copy > 1 && tid < 32,
+                                        &cand);
   const kamera_item it = a.items ? a.items[item] : a.single;
   if (a.items && item_check(it, lay, a.pool, a.max_tokens, a.max_m) != 0) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) atomicOr(a.status, KAMERA_DEVICE_BAD_ITEM);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 4) reuse_copy_kernel(const __grid_co
     // this layer too, and (channel 0, which holds the rope columns) the same offsets
     int n = 1;
     if (a.items && a.run_copy > 1)
-      n = share_run(a.items, item, it, src, cand, a.run_copy, members, true,
+      n = share_run(item, it, src, ch, has_cand, cand, a.run_copy, members, true,
                     [&](const kamera_item &o) {
                       return o.num_tokens == it.num_tokens && !layer_patched(o, layer) &&
                              (ch != 0 || same_offsets(o, it, lay)) &&
