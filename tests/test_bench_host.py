@@ -11,3 +11,18 @@ def test_oracle_per_chunk_covers_the_reference_workloads():
         assert rec["sample"], name
     # extrapolation: a whole MLA chunk (27 layers) costs more than the 2-layer tiny chunk
     assert out["mla_recall"]["us_per_chunk"] > out["tiny_gqa"]["us_per_chunk"]
+
+
+def test_reorder_accounting_matches_the_byte_counts_of_the_workload():
+    # the roofline's numerator: 18 placements x 28 layers x 1024 tokens x (K + V rows of 512)
+    # bf16 written; each of the 3 canonicals read once; each chunk's orbit patch (14 layers of
+    # U [2][1024][32] and V_m^T [32][512 + 512]) read once
+    import workloads as wl
+    w = wl.config2(device="cpu")
+    acc = bench.accounting(w)
+    assert acc["written"] == 18 * 28 * 1024 * 1024 * 2 == 1_056_964_608
+    assert acc["written"] // 18 == 58_720_256
+    assert acc["canon_distinct"] == 3 * 28 * 1024 * 1024 * 2 == 176_160_768
+    assert acc["patch"] == 3 * 14 * (2 * 1024 * 32 + 32 * 1024) * 2 == 8_257_536
+    assert acc["per_kernel"]["reuse_copy_kernel"] + acc["per_kernel"]["reuse_tile_kernel"] == \
+        acc["algorithmic"] + acc["meta"]
