@@ -15,15 +15,13 @@
 // chunk j of row r at chunk j ^ (r % 8)), so copies in and out move 4 rows x 128 bytes per
 // warp instruction and a thread that owns a row reads and writes its chunks without bank
 // conflicts. U rows (A operand) and V_m^T columns (B operand, staged once per task) are
-// no-swizzle core matrices. Per tile one thread issues tcgen05.mma into one of two TMEM
-// accumulators [128 lanes = tokens][tile columns]: the patch U V_m^T and, when the tile does
-// not rotate, the canonical tile itself as X I per 16-column block (I a 16 x 16 identity:
-// exact products, float32 accumulation); the MMA of tile t+1 runs while tile t is stored. In
-// the epilogue each token row belongs to two threads (TMEM lane quarter warp % 4, half warp / 4
-// of the columns): a folded tile only rounds the accumulator; a rotating tile rotates the
-// staged row on the CUDA cores (packed f32x2) and adds the patch; one rounding to bf16, written
-// back in place. Ranks that are not a multiple of 8 form the patch on the CUDA cores from the
-// staged operands.
+// no-swizzle core matrices. Per tile one thread issues tcgen05.mma of the patch U V_m^T into
+// one of two TMEM accumulators [128 lanes = tokens][tile columns] (float32); the MMA of tile t+1
+// runs while tile t is stored. In the epilogue each token row belongs to two threads (TMEM lane
+// quarter warp % 4, half warp / 4 of the columns): the staged row, rotated on the CUDA cores
+// where it turns, plus the patch in packed f32x2 arithmetic, one rounding to bf16, written back
+// in place. Ranks that are not a multiple of 8 form the patch on the CUDA cores from the staged
+// operands.
 #include "kamera_dev.cuh"
 #include "kamera_ptx.cuh"
 #include "kamera_smem.cuh"
@@ -50,27 +48,29 @@ __device__ __forceinline__ void sts_i32t(uint32_t a, int v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
-// Canonical folded into the accumulator: round and write back. Half h owns the contiguous
-// chunks [h*NC/16, (h+1)*NC/16).
+// Unrotated tile: the staged row plus the patch from TMEM in packed f32x2 arithmetic, one
+// rounding, written back in place. Half h owns the contiguous chunks [h*NC/16, (h+1)*NC/16).
+// Each element is its own sum, so a non-finite value stays in its own column.
 template <int NC>
-__device__ __forceinline__ void epi_fold(uint32_t x, int r, int half, uint32_t trow) {
+__device__ __forceinline__ void epi_add(uint32_t x, int r, int half, uint32_t trow) {
   constexpr int CH = NC / 16;
 #pragma unroll 1
   for (int q0 = 0; q0 < CH; q0 += 2) {
     const int j0 = half * CH + q0;
     uint32_t acc[16];
     ptx::tmem_ld16(trow + j0 * 8, acc);
+    const uint32_t a0 = swz(x, r, j0), a1 = swz(x, r, j0 + 1);
+    const uint4 x0 = lds16(a0), x1 = lds16(a1);
     ptx::tmem_ld_wait(acc);
     ptx::tmem_ld_wait(acc + 8);
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t o[8];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        o[e] = pack2_rn(__uint_as_float(acc[8 * q + 2 * e]),
-                        __uint_as_float(acc[8 * q + 2 * e + 1]));
-      sts16(swz(x, r, j0 + q), make_uint4(o[0], o[1], o[2], o[3]));
-    }
+    for (int e = 0; e < 8; ++e)
+      o[e] = f2_to_bf2(add2(bf2_to_f2(w[e]), f2(__uint_as_float(acc[2 * e]),
+                                                 __uint_as_float(acc[2 * e + 1]))));
+    sts16(a0, make_uint4(o[0], o[1], o[2], o[3]));
+    sts16(a1, make_uint4(o[4], o[5], o[6], o[7]));
   }
 }
 
@@ -122,7 +122,7 @@ __device__ __forceinline__ void epi_rot(uint32_t x, int r, int half, uint32_t tr
 
 // CUDA-core contraction (ranks that are not a multiple of 8): the patch of row r from the
 // staged operands, added to the staged row (rotated first when band > 0), one rounding. Each
-// half owns the chunks of epi_fold / epi_rot.
+// half owns the chunks of epi_add / epi_rot.
 __device__ __noinline__ void epi_fma(uint32_t x, int r, int half, int nc, int band,
                                      uint32_t a_op, uint32_t b_op, int m, const float *rot,
                                      int np) {
@@ -177,12 +177,11 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
   const int T = it.num_tokens, m = it.patch_m, Kp = (m + 15) & ~15, m8 = m >> 3;
   const int row = ch == 0 ? lay.row_k : lay.row_v;
   const bool tensor = (m & 7) == 0 && aligned16(it.patch_u);
-  const bool fold = tensor && BAND == 0;
   const bool u2 = P.u_bufs == 2;  // U of tile t+2 staged with its rows (else one buffer)
   const int ps = lay.page_size;
   const int ntt = (T + kTileRows - 1) / kTileRows;
   const uint32_t x_op = s0 + P.canon, v_op = s0 + P.b_op;
-  const uint32_t id_op = s0 + P.desc, pg_op = s0 + P.pages;
+  const uint32_t pg_op = s0 + P.pages;
   const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
   volatile int *flag = reinterpret_cast<volatile int *>(sp + P.misc + 4);
   // MULTI: int slot [member][row] (-1 skips); else the global address of each row (0 skips)
@@ -294,15 +293,6 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
       ptx::mma_bf16(d, ptx::smem_desc(ub + ks * 2 * 2048, 2048, 128),
                     ptx::smem_desc(v_op + ks * 2 * NCORE * 128, NCORE * 128, 128), idesc,
                     ks > 0 ? 1u : 0u);
-    if (fold) {  // D[:, 16j..16j+15] += X[:, 16j..16j+15] * I
-      const uint32_t idesc16 = ptx::idesc_bf16_f32(kTileRows, 16) | (1u << 16);
-      const uint64_t bd = ptx::smem_desc(id_op, 256, 128);
-      const uint32_t xs = x_op + (t & 1) * P.stage;
-#pragma unroll
-      for (int j = 0; j < NC / 16; ++j)
-        ptx::mma_bf16(d + 16 * j, ptx::smem_desc_sw128(xs + (j >> 2) * kAtomT + (j & 3) * 32),
-                      bd, idesc16, 1u);
-    }
     ptx::mma_commit(s_bar + 8 * (t & 1));
   };
 
@@ -329,11 +319,6 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
       sts16(s0 + P.a_op + b * P.a_stage + ((m8 * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4),
             make_uint4(0u, 0u, 0u, 0u));
     }
-  if (fold) {  // 16 x 16 identity, MN-major core matrices (element (n, k))
-    const int n = tid & 15, k = tid >> 4;
-    sts_u16(id_op + ((k >> 3) * 2 + (n >> 3)) * 128 + (k & 7) * 16 + (n & 7) * 2,
-            n == k ? 0x3F80u : 0u);
-  }
   {  // V_m^T of the tile, once: MN-major core matrices, ranks past m zero
     const int wg = tile.group == 0 ? lay.w0 : lay.w1;
     const __nv_bfloat16 *vt = static_cast<const __nv_bfloat16 *>(it.patch_vt) +
@@ -365,7 +350,7 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
     }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
-  __syncthreads();  // TMEM address, barriers, identity, table, tile 0 visible
+  __syncthreads();  // TMEM address, barriers, table, tile 0 visible
   ptx::tc_fence_after();
   tmem = *reinterpret_cast<volatile uint32_t *>(sp + P.misc);
   bool timed_out = false;
@@ -399,7 +384,7 @@ __device__ __forceinline__ void task_loop(const ReuseArgs &a, uint32_t s0, unsig
     if (write) {
       if (use_tc) {
         if constexpr (BAND == 0)
-          epi_fold<NC>(xs, r, half, trow0 + s * P.acc_cols);
+          epi_add<NC>(xs, r, half, trow0 + s * P.acc_cols);
         else
           epi_rot<NC, BAND>(xs, r, half, trow0 + s * P.acc_cols, rot, lay.npairs);
       } else if (!tensor && r < rows) {
@@ -642,8 +627,6 @@ SmemPlan tile_plan_with(const DevLayout &l, int max_m, int run, int u_bufs) {
   off += p.b_stage;
   p.a_op = off;
   off += p.u_bufs * p.a_stage;
-  p.desc = off;  // the 16 x 16 identity operand
-  off += 512;
   p.cs = off;
   off += p.cs_stage;
   p.pages = off;
