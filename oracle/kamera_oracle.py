@@ -13,8 +13,8 @@ Reuse, Eq. 1 in §1 and §3; App. A "Forming and applying the patch"):
   * R(δ) re-rotates the RoPE phase of the stored keys by the integer offset δ = p1 - p0
     (§3 "Relocate"); RoPE composes, R(δ)R(p0) = R(p1), so this is exact algebra. Values and
     the MLA latent c_KV are never rotated (§3 "One mechanism for MLA, GQA, and MHA"; Fig. 2).
-  * U_m V_mᵀ is the rank-m patch: U holds U·Σ [T×m], the stored V_m is kept transposed as
-    Vt [m×W] (App. A, ``form_patch`` returns ``U[:, :m] * S[:m], Vt[:m]``); the patch is added
+  * U_m V_mᵀ is the rank-m patch: the left factor carries the singular values (U·Σ, [T×m]) and
+    the stored V_m is kept transposed as Vt [m×W] (App. A ``form_patch``); the patch is added
     after the rotation, in the target frame (App. A ``apply_reuse``: rotate, then add).
   * The result is written into a paged KV pool at the chunk's new slots (§6 "Recompute-free
     on a live engine": SGLang's paged KV pool).
@@ -530,10 +530,13 @@ def decode_attention(layout, k_pool, v_pool, page_table, req: int, ctx_len: int,
 # ----------------------------------------------------------------------------------------
 
 def form_patch(kv_cond, kv_solo_relocated, m: int):
-    """Δ = KV(B|A) - R(δ)KV(B|∅); keep the top-m SVD factors (U·Σ [T×m], Vt [m×W])."""
-    delta_kv = np.asarray(kv_cond, np.float64) - np.asarray(kv_solo_relocated, np.float64)
-    u, s, vt = np.linalg.svd(delta_kv, full_matrices=False)
-    return u[:, :m] * s[:m], vt[:m]
+    """The compile step of App. A from its two prefills: the deficit between the conditioned KV
+    and the relocated context-free KV, replaced by its best rank-m approximation (Eckart–Young:
+    the m leading singular triplets), with the singular values carried by the left factor.
+    Returns (U·Σ [T×m], V_mᵀ [m×W]); see ``form_patch_svd`` for the sign convention."""
+    deficit = np.asarray(kv_cond, np.float64) - np.asarray(kv_solo_relocated, np.float64)
+    us, vt, _ = form_patch_svd(deficit, m)
+    return us, vt
 
 
 def _sign_rows(us, vt):

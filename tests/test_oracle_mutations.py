@@ -5,7 +5,8 @@ pin in tests/test_oracle_pins.py then fails. The variants: a flipped sign, a dro
 transposed pairing, a patch that is rotated too, a double rounding, an off-by-one slot, M-RoPE
 offsets or sections taken wrongly, a re-anchoring position of the wrong sign or with its
 coordinates reversed, attention without its scale, an unnormalised split merge, singular
-values in ascending order, and the opposite sign convention.
+values in ascending order, the opposite sign convention, an error scale built from the product
+of the factor sums or counting a turned pair twice, and a re-anchoring that skips the values.
 """
 import numpy as np
 import pytest
@@ -116,7 +117,37 @@ def sign_rows_flipped(us, vt):
     return -us, -vt                   # the largest entry of each row made negative
 
 
+def magnitude_product_of_sums(layout, item, layer, channel, tokens=None):
+    # Σ_j|U_tj| · Σ_j|Vt_jc| in place of Σ_j |U_tj · Vt_jc| for the patch term
+    mag = ora_magnitude_orig(layout, ora.as_item(**{**vars(item), "patch_m": 0}), layer, channel,
+                             tokens)
+    if ora.layer_patched(item, layer):
+        li = layer - item.patch_l0
+        for c0, w, g in ora.channel_groups(layout, channel):
+            u = np.abs(ora.factor_f64(item.patch_u[li][g]))
+            vt = np.abs(ora.factor_f64(ora.vt_of_group(layout, item.patch_vt[li], item.patch_m, g)))
+            mag[:, c0:c0 + w] += u.sum(axis=1, keepdims=True) * vt.sum(axis=0, keepdims=True)
+    return mag
+
+
+def magnitude_pair_twice(layout, item, layer, channel, tokens=None):
+    # |x| kept and |a| + |b| added on top for turned pairs (the element counted twice)
+    mag = ora_magnitude_orig(layout, item, layer, channel, tokens)
+    if channel == 0 and ora.item_rotates(layout, item):
+        canon = np.asarray(item.canon_k[layer])
+        x = np.abs(ora.bf16_to_f64(canon if tokens is None else canon[np.asarray(tokens)]))
+        for c0, d in ora.rope_bands(layout):
+            mag[:, c0:c0 + d] += x[:, c0:c0 + d]
+    return mag
+
+
+def reanchor_skips_values(layout, item, k_pool, v_pool, page_table):
+    ora_apply_reanchor_orig(layout, item, k_pool, None, page_table)
+
+
 ora_rotate_orig = ora.rotate_band
+ora_magnitude_orig = ora.magnitude_layer
+ora_apply_reanchor_orig = ora.apply_reanchor
 ora_f64_to_bf16_orig = ora.f64_to_bf16
 ora_axes_orig = ora.mrope_pair_axes
 ora_token_offsets_orig = ora.token_offsets
@@ -150,6 +181,13 @@ CASES = [
       pins.test_randomized_patch_residual_near_the_eckart_young_optimum]),
     ("_sign_rows", sign_rows_flipped,
      [pins.test_randomized_patch_recovers_an_exactly_low_rank_deficit]),
+    ("magnitude_layer", magnitude_product_of_sums,
+     [lambda: pins.test_magnitude_scale_by_explicit_loops("gqa", ora.NEOX_HALF, 0),
+      lambda: pins.test_magnitude_scale_by_explicit_loops("mla", ora.NEOX_HALF, 31)]),
+    ("magnitude_layer", magnitude_pair_twice,
+     [lambda: pins.test_magnitude_scale_by_explicit_loops("gqa", ora.NEOX_HALF, 777)]),
+    ("apply_reanchor", reanchor_skips_values, [pins.test_reanchored_items_land_at_their_slots]),
+    ("slot_of", off_by_one_slot, [pins.test_reanchored_items_land_at_their_slots]),
 ]
 
 

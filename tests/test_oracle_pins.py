@@ -761,6 +761,106 @@ def test_reanchor_mla_rotates_only_k_pe():
     assert not np.array_equal(bits[:, 32:], it.canon_k[0][:, 32:])
 
 
+def test_reanchored_items_land_at_their_slots():
+    # every token's re-anchored row is written at slot_of(req, start_tok + j) of each layer and
+    # channel (an independent page expansion), and no other slot changes
+    ps, L = 4, 2
+    lay = ns_layout(num_layers=L, page_size=ps, num_kv_heads=2, head_dim=8, rope_dim=8)
+    W = 16
+    pt = RNG.permutation(12).reshape(2, 6).astype(np.int32)
+    flat = (pt[:, :, None].astype(np.int64) * ps + np.arange(ps)).reshape(2, -1)
+    k_pool = np.full((L, 48, W), 0x5A5A, np.uint16)
+    v_pool = k_pool.copy()
+    want_k, want_v = k_pool.copy(), v_pool.copy()
+    from types import SimpleNamespace
+    for i, (req, start, T) in enumerate([(0, 1, 7), (1, 5, 9)]):
+        rng = np.random.default_rng(40 + i)
+        k = ora.f64_to_bf16(rng.standard_normal((L, T, W)))
+        v = ora.f64_to_bf16(rng.standard_normal((L, T, W)))
+        it = SimpleNamespace(canon_k=k, canon_v=v, positions=rng.integers(-50, 50, T),
+                             num_tokens=T, req=req, start_tok=start)
+        ora.apply_reanchor(lay, it, k_pool, v_pool, pt)
+        for layer in range(L):
+            kb = ora.reanchor_layer_bits(lay, it, layer, 0)
+            vb = ora.reanchor_layer_bits(lay, it, layer, 1)
+            for j in range(T):
+                want_k[layer, flat[req, start + j]] = kb[j]
+                want_v[layer, flat[req, start + j]] = vb[j]
+    np.testing.assert_array_equal(k_pool, want_k)
+    np.testing.assert_array_equal(v_pool, want_v)
+    # MLA: one pool, only the k_pe band turns
+    mla = ns_layout(kind=ora.MLA, num_layers=1, page_size=ps, num_kv_heads=0, head_dim=0,
+                    latent_dim=16, rope_dim=8)
+    pool = np.full((1, 48, 24), 0x5A5A, np.uint16)
+    want = pool.copy()
+    it = SimpleNamespace(canon_k=ora.f64_to_bf16(RNG.standard_normal((1, 5, 24))), canon_v=None,
+                         positions=np.array([3, -1, 0, 7, 100]), num_tokens=5, req=1, start_tok=2)
+    ora.apply_reanchor(mla, it, pool, None, pt)
+    bits = ora.reanchor_layer_bits(mla, it, 0, 0)
+    for j in range(5):
+        want[0, flat[1, 2 + j]] = bits[j]
+    np.testing.assert_array_equal(pool, want)
+
+
+# ------------------------------------------------------------------------------------------
+# the error scale the GPU tolerance multiplies (§6 "within one bf16 ULP")
+# ------------------------------------------------------------------------------------------
+
+def _magnitude_by_hand(lay, it, layer, ch):
+    """The scale of the terms of every result element, by explicit loops: |x| of the element,
+    or |a| + |b| of its rope pair when the pair turns, plus the sum over j of |U_tj * Vt_jc|."""
+    canon = (it.canon_k if ch == 0 else it.canon_v)[layer]
+    T, row = canon.shape
+    x = [[float(ora.bf16_to_f64(canon[t, c])) for c in range(row)] for t in range(T)]
+    out = [[abs(x[t][c]) for c in range(row)] for t in range(T)]
+    if ch == 0 and it.delta != 0:
+        if lay.kind == ora.GQA:
+            bands = [(h * lay.head_dim, lay.head_dim) for h in range(lay.num_kv_heads)]
+        else:
+            bands = [(lay.latent_dim, lay.rope_dim)]
+        for c0, d in bands:
+            for k in range(d // 2):
+                a, b = (c0 + k, c0 + k + d // 2) if lay.rope_style == ora.NEOX_HALF else \
+                    (c0 + 2 * k, c0 + 2 * k + 1)
+                for t in range(T):
+                    out[t][a] = out[t][b] = abs(x[t][a]) + abs(x[t][b])
+    if it.patch_m and it.patch_l0 <= layer < it.patch_l1:
+        li, m = layer - it.patch_l0, it.patch_m
+        if lay.kind == ora.GQA:
+            groups = [(0, row, ch)]
+        else:
+            groups = [(0, lay.latent_dim, 0), (lay.latent_dim, lay.rope_dim, 1)]
+        w0 = lay.num_kv_heads * lay.head_dim if lay.kind == ora.GQA else lay.latent_dim
+        for c0, w, g in groups:
+            off = 0 if g == 0 else m * w0
+            for t in range(T):
+                for c in range(w):
+                    for j in range(m):
+                        u = float(ora.bf16_to_f64(it.patch_u[li][g][t][j]))
+                        v = float(ora.bf16_to_f64(it.patch_vt[li][off + j * w + c]))
+                        out[t][c0 + c] += abs(u * v)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("kind,style,delta", [("gqa", ora.NEOX_HALF, 777), ("gqa", ora.NEOX_HALF, 0),
+                                              ("gqa", ora.INTERLEAVED, -5), ("mla", ora.NEOX_HALF, 31),
+                                              ("mla", ora.INTERLEAVED, 0)])
+def test_magnitude_scale_by_explicit_loops(kind, style, delta):
+    if kind == "gqa":
+        lay, it = gqa_item(L=3, T=4, H=2, hd=8, m=3, l0=1, l1=3, delta=delta)
+        lay.rope_style = style
+    else:
+        lay, it = mla_item(L=3, T=4, latent=16, rope=8, m=2, l0=1, l1=2, delta=delta)
+        lay.rope_style = style
+    # signs on both sides of zero in the factors: a product of sums would not match
+    n_ch = 2 if kind == "gqa" else 1
+    for layer in range(3):
+        for ch in range(n_ch):
+            got = ora.magnitude_layer(lay, it, layer, ch)
+            np.testing.assert_allclose(got, _magnitude_by_hand(lay, it, layer, ch), rtol=1e-12,
+                                       atol=0)
+
+
 # ------------------------------------------------------------------------------------------
 # consumer check: decode attention and the log-sum-exp merge (§1)
 # ------------------------------------------------------------------------------------------
