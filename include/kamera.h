@@ -169,6 +169,29 @@ kamera_status kamera_destroy(kamera_handle *handle);
 const char *kamera_status_string(kamera_status status);
 
 /*
+ * Options of a handle, for ablations and tuning; a new handle has the defaults, and every call
+ * made with the handle after kamera_set_option uses the new value. Not thread-safe against
+ * calls that use the same handle at the same time. The pages have no counterpart: these select
+ * between implementations of the same operation.
+ *   KAMERA_OPT_PATCH_ENGINE: KAMERA_ENGINE_TENSOR (default) forms the rank-m patch on the tensor
+ *     cores where the rank is a multiple of 8; KAMERA_ENGINE_CUDA_CORES forms every patch with
+ *     float32 FMAs on the CUDA cores (the ablation of the tensor-core path).
+ *   KAMERA_OPT_SHARE_RUN_PATCHED: in kamera_batch_reuse, the most members of a group of
+ *     placements of one chunk (see kamera_batch_reuse) written from one computed tile on
+ *     patched layers, 1..32 (default 3; 1 groups nothing).
+ *   KAMERA_OPT_SHARE_RUN_UNPATCHED: the same on layers without a patch, 1..8 (default 2).
+ * The bytes written do not depend on any option beyond the rounding of float32 sums. An unknown
+ * option or a value out of range returns KAMERA_ERR_INVALID_ARG and changes nothing.
+ */
+#define KAMERA_OPT_PATCH_ENGINE 1
+#define KAMERA_OPT_SHARE_RUN_PATCHED 2
+#define KAMERA_OPT_SHARE_RUN_UNPATCHED 3
+#define KAMERA_ENGINE_TENSOR 0
+#define KAMERA_ENGINE_CUDA_CORES 1
+
+kamera_status kamera_set_option(kamera_handle *handle, int32_t option, int32_t value);
+
+/*
  * Survivor relocation, in place (§5 "Sliding-window survival": keep the survivor's KV as-is
  * and apply R(delta); Fig. 2: rotate_k_pe_inplace). Rotates the rope columns of K (GQA/MHA:
  * every head; MLA: the k_pe band only) of logical tokens [start_tok, start_tok+num_tokens)
@@ -379,16 +402,20 @@ kamera_status kamera_form_patch(const float *d_delta, int64_t ld, int64_t delta_
  * its paged KV pool at start-up (so an allocation at patch-forming time would fail or evict
  * cache), or host code with no device allocator of its own. The Kamera paper has no
  * counterpart to this call; it is kamera_form_patch with the workspace taken from a fixed
- * array of KAMERA_FORM_PATCH_SCRATCH_BYTES in this library's device memory, reserved with the
- * library's device code.
+ * array of KAMERA_FORM_PATCH_SCRATCH_BYTES in this library's device memory.
  *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library routine.
- *   - Arguments, outputs, results and errors are those of kamera_form_patch. In addition, a
- *     call whose kamera_form_patch_workspace(num_problems, T, W, k) exceeds
- *     KAMERA_FORM_PATCH_SCRATCH_BYTES (32 MiB: e.g. 96 deficits of 1024 x 512 at k = 40)
- *     returns KAMERA_ERR_UNSUPPORTED and launches nothing.
- *   - Set-up: the first call with num_problems > 0 on a device looks up the array's device
- *     address (once per device, with that device current) and keeps it; a failed lookup
- *     returns KAMERA_ERR_CUDA. Make that first call before any stream capture.
+ *   - Arguments, outputs and results are those of kamera_form_patch, and so are its argument
+ *     errors, which are checked first. Then a call whose kamera_form_patch_workspace(
+ *     num_problems, T, W, k) exceeds KAMERA_FORM_PATCH_SCRATCH_BYTES (32 MiB: e.g. 96 deficits
+ *     of 1024 x 512 at k = 40) returns KAMERA_ERR_UNSUPPORTED and launches nothing.
+ *   - Set-up: the first call on a device, with that device current, looks up the array's
+ *     device address and loads and configures the kernel; a failure returns KAMERA_ERR_CUDA.
+ *     CUDA reserves the array when it loads this library's device code, which by default
+ *     (lazy module loading) happens at that set-up, not earlier. A call with num_problems = 0
+ *     and otherwise valid arguments does the set-up alone: make one on each device before
+ *     handing that device's free memory to a pool, and before any stream capture. After the
+ *     set-up, calls take no device memory. A device reset (cudaDeviceReset) discards the
+ *     set-up's address: do not use this call on a device after resetting it.
  *   - Nothing has to start at zero: the array's contents on entry are ignored and left
  *     undefined.
  *   - One array per device: calls on the same device that overlap in time (different

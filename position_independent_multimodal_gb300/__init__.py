@@ -8,6 +8,8 @@ from ._binding import (  # noqa: F401
     ITEM_BYTES, KAMERA_DEVICE_BAD_ITEM, KAMERA_DEVICE_SLOT_OOB, KAMERA_ERR_CUDA,
     KAMERA_FORM_PATCH_SCRATCH_BYTES,
     KAMERA_ERR_INVALID_ARG, KAMERA_ERR_UNSUPPORTED, KAMERA_GQA, KAMERA_MLA,
+    KAMERA_ENGINE_CUDA_CORES, KAMERA_ENGINE_TENSOR, KAMERA_OPT_PATCH_ENGINE,
+    KAMERA_OPT_SHARE_RUN_PATCHED, KAMERA_OPT_SHARE_RUN_UNPATCHED, kamera_set_option,
     KAMERA_MROPE_CONTIGUOUS, KAMERA_MROPE_INTERLEAVED, KAMERA_OK,
     KAMERA_ROPE_INTERLEAVED, KAMERA_ROPE_NEOX_HALF, LIB_PATH, Handle, KameraError, Pool,
     create, kamera_batch_patch_inplace, kamera_batch_reuse, kamera_batch_reuse_timed,

@@ -29,6 +29,11 @@ KAMERA_ROPE_INTERLEAVED = 1
 KAMERA_MROPE_CONTIGUOUS = 0
 KAMERA_MROPE_INTERLEAVED = 1
 KAMERA_FORM_PATCH_SCRATCH_BYTES = 32 << 20
+KAMERA_OPT_PATCH_ENGINE = 1
+KAMERA_OPT_SHARE_RUN_PATCHED = 2
+KAMERA_OPT_SHARE_RUN_UNPATCHED = 3
+KAMERA_ENGINE_TENSOR = 0
+KAMERA_ENGINE_CUDA_CORES = 1
 
 
 class KameraError(RuntimeError):
@@ -86,6 +91,7 @@ def lib() -> ctypes.CDLL:
         L.kamera_destroy.argtypes = [vp]
         L.kamera_status_string.argtypes = [ctypes.c_int]
         L.kamera_status_string.restype = ctypes.c_char_p
+        L.kamera_set_option.argtypes = [vp, i32, i32]
         L.kamera_relocate.argtypes = [vp, ctypes.POINTER(kamera_pool), i32, i32, i32, i64, vp, vp]
         L.kamera_reuse.argtypes = [vp, ctypes.POINTER(kamera_item), ctypes.POINTER(kamera_pool),
                                    vp, vp]
@@ -171,8 +177,24 @@ class Handle:
             pass
 
 
-def create(layout) -> Handle:
-    return Handle(layout)
+def create(layout, **options) -> Handle:
+    """kamera_create, then kamera_set_option for each keyword: patch_engine,
+    share_run_patched, share_run_unpatched."""
+    h = Handle(layout)
+    for name, value in options.items():
+        kamera_set_option(h, name, value)
+    return h
+
+
+_OPTIONS = {"patch_engine": KAMERA_OPT_PATCH_ENGINE,
+            "share_run_patched": KAMERA_OPT_SHARE_RUN_PATCHED,
+            "share_run_unpatched": KAMERA_OPT_SHARE_RUN_UNPATCHED}
+
+
+def kamera_set_option(handle: Handle, option, value: int) -> None:
+    """kamera_set_option; `option` is a KAMERA_OPT_* value or its keyword name."""
+    opt = _OPTIONS[option] if isinstance(option, str) else int(option)
+    _check(lib().kamera_set_option(handle.ptr, opt, int(value)), "kamera_set_option")
 
 
 class Pool:

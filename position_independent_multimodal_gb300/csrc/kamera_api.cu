@@ -12,7 +12,9 @@ struct kamera_handle {
   kamera_layout desc;
   kamera::DevLayout lay;
   kamera::FreqQ64 freq;
-  int engine;  // engine of patched tiles (KAMERA_PATCH_ENGINE=fma selects the CUDA-core one)
+  int engine;     // engine of patched tiles (KAMERA_OPT_PATCH_ENGINE)
+  int run_tile;   // most members of a group written from one computed tile, patched layers
+  int run_copy;   // the same on unpatched layers
 };
 
 namespace {
@@ -202,22 +204,11 @@ kamera::SmemPlan reuse_plan(const kamera_handle *h, int max_m, int max_run) {
 }
 
 
-
-int env_int(const char *name, int dflt) {
-  const char *e = std::getenv(name);
-  return e ? std::atoi(e) : dflt;
-}
-
-// Most members of a group of shared rows that one CTA writes: the patched-layer kernel and
-// the copy kernel.
-int share_run_tile() {
-  static const int r = env_int("KAMERA_SHARE_RUN_TILE", 3);
-  return r < 1 ? 1 : (r > kamera::kShareBlock ? kamera::kShareBlock : r);
-}
-int share_run_copy() {
-  static const int r = env_int("KAMERA_SHARE_RUN_COPY", 2);
-  return r < 1 ? 1 : (r > 8 ? 8 : r);
-}
+// Defaults of the handle options (measured on the reorder workload: runs of 3 on patched layers,
+// 2 on unpatched ones give the fastest kernels).
+constexpr int kDefaultRunTile = 3;
+constexpr int kDefaultRunCopy = 2;
+constexpr int kMaxRunCopy = 8;
 
 }  // namespace
 
@@ -234,10 +225,31 @@ kamera_status kamera_create(const kamera_layout *layout, kamera_handle **out) {
   h->desc = *layout;
   h->lay = l;
   fill_freq(*layout, l, &h->freq);
-  const char *eng = std::getenv("KAMERA_PATCH_ENGINE");
-  h->engine = (eng && std::strcmp(eng, "fma") == 0) ? kamera::kEngineFma : kamera::kEngineTensor;
+  h->engine = kamera::kEngineTensor;
+  h->run_tile = kDefaultRunTile;
+  h->run_copy = kDefaultRunCopy;
   *out = h;
   return KAMERA_OK;
+}
+
+kamera_status kamera_set_option(kamera_handle *h, int32_t option, int32_t value) {
+  if (!h) return KAMERA_ERR_INVALID_ARG;
+  switch (option) {
+    case KAMERA_OPT_PATCH_ENGINE:
+      if (value != KAMERA_ENGINE_TENSOR && value != KAMERA_ENGINE_CUDA_CORES)
+        return KAMERA_ERR_INVALID_ARG;
+      h->engine = value == KAMERA_ENGINE_TENSOR ? kamera::kEngineTensor : kamera::kEngineFma;
+      return KAMERA_OK;
+    case KAMERA_OPT_SHARE_RUN_PATCHED:
+      if (value < 1 || value > kamera::kShareBlock) return KAMERA_ERR_INVALID_ARG;
+      h->run_tile = value;
+      return KAMERA_OK;
+    case KAMERA_OPT_SHARE_RUN_UNPATCHED:
+      if (value < 1 || value > kMaxRunCopy) return KAMERA_ERR_INVALID_ARG;
+      h->run_copy = value;
+      return KAMERA_OK;
+  }
+  return KAMERA_ERR_INVALID_ARG;
 }
 
 kamera_status kamera_destroy(kamera_handle *handle) {
@@ -326,8 +338,8 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
   a.max_tokens = max_tokens;
   a.max_m = max_patch_m;
   a.engine = h->engine;
-  a.smem = reuse_plan(h, a.max_m, share_run_tile());
-  a.run_copy = share_run_copy();
+  a.smem = reuse_plan(h, a.max_m, h->run_tile);
+  a.run_copy = h->run_copy;
   a.status = d_status;
   a.freq = h->freq;
   if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
@@ -531,6 +543,36 @@ kamera_status kamera_rope_phases(const kamera_handle *h, const int64_t *d_deltas
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace kamera {
+
+kamera_status form_patch_args(const float *d_delta, int64_t ld, int64_t delta_stride,
+                              int32_t num_problems, int32_t T, int32_t W, const float *d_omega,
+                              int64_t omega_stride, int32_t k, int32_t q, int32_t m,
+                              const void *d_u, int64_t u_stride, const void *d_vt,
+                              int64_t vt_stride, const float *d_sigma) {
+  if (num_problems < 0 || T < 1 || W < 1) return KAMERA_ERR_INVALID_ARG;
+  if (k < 1 || m < 1 || m > k || q < 0) return KAMERA_ERR_INVALID_ARG;
+  if (k > kMaxSketch || k > T || k > W || q > 16) return KAMERA_ERR_UNSUPPORTED;
+  if (form_patch_smem(W, k) > (size_t)kMaxFormSmem) return KAMERA_ERR_UNSUPPORTED;
+  if (ld < W || delta_stride < 0 || omega_stride < 0 || u_stride < 0 || vt_stride < 0)
+    return KAMERA_ERR_INVALID_ARG;
+  if (num_problems > 1 && (u_stride < (int64_t)T * m || vt_stride < (int64_t)m * W))
+    return KAMERA_ERR_INVALID_ARG;
+  if (num_problems == 0) return KAMERA_OK;
+  auto mis = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (!d_delta || !d_omega || !d_u || !d_vt) return KAMERA_ERR_INVALID_ARG;
+  if (mis(d_delta, 4) || mis(d_omega, 4) || mis(d_u, 2) || mis(d_vt, 2) ||
+      (d_sigma && mis(d_sigma, 4)))
+    return KAMERA_ERR_INVALID_ARG;
+  return KAMERA_OK;
+}
+
+}  // namespace kamera
+
+extern "C" {
+
 size_t kamera_form_patch_workspace(int32_t num_problems, int32_t T, int32_t W, int32_t k) {
   if (num_problems < 0 || T < 0 || W < 0 || k < 0) return 0;
   return kamera::form_patch_workspace(num_problems, T, W, k);
@@ -542,20 +584,11 @@ kamera_status kamera_form_patch(const float *d_delta, int64_t ld, int64_t delta_
                                 int64_t u_stride, void *d_vt, int64_t vt_stride, float *d_sigma,
                                 void *d_workspace, size_t workspace_bytes,
                                 kamera_stream_t stream) {
-  if (num_problems < 0 || T < 1 || W < 1) return KAMERA_ERR_INVALID_ARG;
-  if (k < 1 || m < 1 || m > k || q < 0) return KAMERA_ERR_INVALID_ARG;
-  if (k > kamera::kMaxSketch || k > T || k > W || q > 16) return KAMERA_ERR_UNSUPPORTED;
-  if (kamera::form_patch_smem(W, k) > (size_t)kamera::kMaxFormSmem) return KAMERA_ERR_UNSUPPORTED;
-  if (ld < W || delta_stride < 0 || omega_stride < 0 || u_stride < 0 || vt_stride < 0)
-    return KAMERA_ERR_INVALID_ARG;
-  if (num_problems > 1 && (u_stride < (int64_t)T * m || vt_stride < (int64_t)m * W))
-    return KAMERA_ERR_INVALID_ARG;
-  if (num_problems == 0) return KAMERA_OK;
-  auto mis = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
-  if (!d_delta || !d_omega || !d_u || !d_vt || !d_workspace) return KAMERA_ERR_INVALID_ARG;
-  if (mis(d_delta, 4) || mis(d_omega, 4) || mis(d_u, 2) || mis(d_vt, 2) ||
-      mis(d_workspace, 4) || (d_sigma && mis(d_sigma, 4)))
-    return KAMERA_ERR_INVALID_ARG;
+  const kamera_status st =
+      kamera::form_patch_args(d_delta, ld, delta_stride, num_problems, T, W, d_omega,
+                              omega_stride, k, q, m, d_u, u_stride, d_vt, vt_stride, d_sigma);
+  if (st != KAMERA_OK || num_problems == 0) return st;
+  if (!d_workspace || (reinterpret_cast<uintptr_t>(d_workspace) & 3u)) return KAMERA_ERR_INVALID_ARG;
   if (workspace_bytes < kamera::form_patch_workspace(num_problems, T, W, k))
     return KAMERA_ERR_INVALID_ARG;
   kamera::FormArgs a;

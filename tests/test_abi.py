@@ -345,3 +345,19 @@ def test_library_is_required(monkeypatch, tmp_path):
     monkeypatch.setattr(kb, "_lib", None)
     with pytest.raises(ImportError):
         kb.lib()
+
+
+def test_set_option_checks_its_arguments():
+    h = km.create(gqa())
+    km.kamera_set_option(h, "patch_engine", km.KAMERA_ENGINE_CUDA_CORES)
+    km.kamera_set_option(h, km.KAMERA_OPT_PATCH_ENGINE, km.KAMERA_ENGINE_TENSOR)
+    km.kamera_set_option(h, "share_run_patched", 32)
+    km.kamera_set_option(h, "share_run_unpatched", 1)
+    for opt, val in ((km.KAMERA_OPT_PATCH_ENGINE, 2), (km.KAMERA_OPT_SHARE_RUN_PATCHED, 0),
+                     (km.KAMERA_OPT_SHARE_RUN_PATCHED, 33), (km.KAMERA_OPT_SHARE_RUN_UNPATCHED, 9),
+                     (99, 1)):
+        with pytest.raises(km.KameraError) as e:
+            km.kamera_set_option(h, opt, val)
+        assert e.value.status == km.KAMERA_ERR_INVALID_ARG
+    assert km.lib().kamera_set_option(None, km.KAMERA_OPT_PATCH_ENGINE, 0) == \
+        km.KAMERA_ERR_INVALID_ARG

@@ -44,8 +44,8 @@ def ragged(layout, m, name, seed=0, strong=True):
                              patch_per_item=True, extra_pages=3)
 
 
-def run_and_check(w, batch=True):
-    h = km.create(w.layout)
+def run_and_check(w, batch=True, **options):
+    h = km.create(w.layout, **options)
     items = tl.to_device_items(w.items)
     if batch:
         k, v, status, _ = tl.run_batch(h, w.layout, items, w.page_table, w.num_slots)
@@ -70,11 +70,10 @@ def test_gqa_ragged_batch(m, style):
 
 
 @pytest.mark.parametrize("kind", ["gqa", "mla"])
-def test_fma_engine_matches_oracle(kind, monkeypatch):
+def test_fma_engine_matches_oracle(kind):
     # the CUDA-core engine for every patched tile (the ablation of the tensor-core path)
-    monkeypatch.setenv("KAMERA_PATCH_ENGINE", "fma")
     lay = gqa_layout(L=2, H=4, hd=128) if kind == "gqa" else mla_layout(L=2)
-    run_and_check(ragged(lay, 32, f"fma{kind}"))
+    run_and_check(ragged(lay, 32, f"fma{kind}"), patch_engine=km.KAMERA_ENGINE_CUDA_CORES)
 
 
 @pytest.mark.parametrize("m", [0, 8, 32, 128])

@@ -52,13 +52,13 @@ def orderings(layout, m, name, Ts=(130, 256, 77), prefix=5, patch_per_item=False
                              patch_per_item=patch_per_item, extra_pages=2)
 
 
-def batch_pools(w, items, **kw):
-    h = km.create(w.layout)
+def batch_pools(w, items, options=None, **kw):
+    h = km.create(w.layout, **(options or {}))
     return tl.run_batch(h, w.layout, items, w.page_table, w.num_slots, **kw)
 
 
-def single_pools(w, items):
-    h = km.create(w.layout)
+def single_pools(w, items, options=None):
+    h = km.create(w.layout, **(options or {}))
     return tl.run_single(h, w.layout, items, w.page_table, w.num_slots)
 
 
@@ -66,20 +66,20 @@ def same_bytes(a, b):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def check_grouped(w, n_shared_min=1):
+def check_grouped(w, n_shared_min=1, options=None):
     items = tl.to_device_items(w.items)
     ptrs = {(it.canon_k.data_ptr(), it.delta) for it in items}
     assert len(ptrs) <= len(items) - n_shared_min, "the workload has no shared rows"
-    k, v, status, _ = batch_pools(w, items)
+    k, v, status, _ = batch_pools(w, items, options)
     assert status == 0
     tl.check_full(w.layout, w.items, w.page_table, k, v)
-    k1, v1, s1 = single_pools(w, items)
+    k1, v1, s1 = single_pools(w, items, options)
     assert s1 == 0
     same_bytes(k, k1)
     if v is not None:
         same_bytes(v, v1)
     # the same batch with every item on its own copies (no group forms) writes the same bytes
-    k2, v2, s2, _ = batch_pools(w, tl.to_device_items(w.items, keep_sharing=False))
+    k2, v2, s2, _ = batch_pools(w, tl.to_device_items(w.items, keep_sharing=False), options)
     assert s2 == 0
     same_bytes(k, k2)
     if v is not None:
@@ -171,8 +171,16 @@ def test_interleaved_pairing_groups_in_the_copy_kernel(m):
 
 
 @pytest.mark.parametrize("kind", ["gqa", "mla"])
-def test_cuda_core_engine_with_shared_chunks(kind, monkeypatch):
+def test_cuda_core_engine_with_shared_chunks(kind):
     # the CUDA-core patch engine (general kernel) beside the grouped copy kernel
-    monkeypatch.setenv("KAMERA_PATCH_ENGINE", "fma")
     lay = gqa(H=4, hd=128) if kind == "gqa" else mla()
-    check_grouped(orderings(lay, 16, f"sharefma{kind}"), n_shared_min=4)
+    check_grouped(orderings(lay, 16, f"sharefma{kind}"), n_shared_min=4,
+                  options=dict(patch_engine=km.KAMERA_ENGINE_CUDA_CORES))
+
+
+@pytest.mark.parametrize("runs", [(1, 1), (6, 8), (32, 3)])
+def test_run_sizes_write_the_same_bytes(runs):
+    # any run size (1: no groups) writes what separate calls write
+    patched, unpatched = runs
+    check_grouped(orderings(gqa(H=4, hd=128), 16, f"runs{patched}"), n_shared_min=4,
+                  options=dict(share_run_patched=patched, share_run_unpatched=unpatched))
