@@ -528,6 +528,13 @@ struct FormArgs {
 size_t form_patch_workspace(long long n, int T, int W, int k);  // kamera_form.cu
 size_t form_patch_smem(int W, int k);
 cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s);
+cudaError_t prepare_form_patch();  // loads the kernel and sets its shared-memory limit
+// The argument checks of kamera_form_patch other than those of the workspace.
+kamera_status form_patch_args(const float *d_delta, int64_t ld, int64_t delta_stride,
+                              int32_t num_problems, int32_t T, int32_t W, const float *d_omega,
+                              int64_t omega_stride, int32_t k, int32_t q, int32_t m,
+                              const void *d_u, int64_t u_stride, const void *d_vt,
+                              int64_t vt_stride, const float *d_sigma);
 SmemPlan reuse_smem_plan(const DevLayout &l, int max_m);           // kamera_reuse.cu
 cudaError_t launch_reuse(const ReuseArgs &a, int n_items, cudaStream_t s);
 bool fast_layout(const DevLayout &l);                               // kamera_reuse_tile.cu

@@ -483,27 +483,46 @@ size_t form_patch_workspace(long long n, int T, int W, int k) {
 
 size_t form_patch_smem(int W, int k) { return (size_t)form_plan(W, k).total * sizeof(float); }
 
+namespace {
+
+int g_form_configured[64] = {0};  // per device: the kernel's dynamic shared-memory limit
+std::mutex g_form_mu;
+
+// Once per device: the kernel is loaded and may use the device's opt-in shared memory.
+cudaError_t configure_form(int dev) {
+  std::lock_guard<std::mutex> lock(g_form_mu);
+  if (g_form_configured[dev]) return cudaSuccess;
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, form_patch_kernel);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(form_patch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
+  g_form_configured[dev] = optin;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t prepare_form_patch() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  return configure_form(dev);
+}
+
 cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s) {
-  static int configured[64] = {0};
-  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const size_t smem = form_patch_smem(a.W, a.k);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!configured[dev]) {
-      int optin = 0;
-      e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(form_patch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               optin);
-      if (e != cudaSuccess) return e;
-      configured[dev] = optin;
-    }
-    if ((size_t)configured[dev] < smem) return cudaErrorInvalidValue;
-  }
+  e = configure_form(dev);
+  if (e != cudaSuccess) return e;
+  if ((size_t)g_form_configured[dev] < smem) return cudaErrorInvalidValue;
   if (a.n == 0) return cudaSuccess;
   form_patch_kernel<<<a.n, kThr, smem, s>>>(a);
   return cudaGetLastError();
@@ -513,9 +532,8 @@ cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s) {
 
 // ---------------------------------------------------------------------------------------
 // kamera_form_patch_static_scratch: kamera_form_patch with its workspace in a fixed array of
-// this library's device memory, for callers that cannot allocate device memory at the call
-// site (see include/kamera.h). The array is reserved with the library's device code, so the
-// call allocates nothing; one array per device, shared by every call on that device.
+// this library's device memory, for callers that cannot allocate device memory where they call
+// it (see include/kamera.h). One array per device, shared by every call on that device.
 // ---------------------------------------------------------------------------------------
 
 namespace {
@@ -523,8 +541,9 @@ namespace {
 static __device__ __align__(256) float g_form_scratch[KAMERA_FORM_PATCH_SCRATCH_BYTES /
                                                       sizeof(float)];
 
-// Device address of g_form_scratch on the current device, looked up once per device (with that
-// device current) and kept; the lookup is the set-up that the first call on a device does.
+// Set-up, once per device with that device current: the array's device address (the lookup
+// also makes CUDA load this file's device code, which reserves the array) and the kernel,
+// loaded and configured. Later calls on the device reuse the address.
 cudaError_t form_scratch(void **out) {
   static void *ptrs[64] = {nullptr};
   static std::mutex mu;
@@ -538,6 +557,8 @@ cudaError_t form_scratch(void **out) {
     e = cudaGetSymbolAddress(&p, g_form_scratch);
     if (e != cudaSuccess) return e;
     if (!p) return cudaErrorInvalidSymbol;
+    e = kamera::prepare_form_patch();
+    if (e != cudaSuccess) return e;
     ptrs[dev] = p;
   }
   *out = ptrs[dev];
@@ -551,14 +572,15 @@ extern "C" kamera_status kamera_form_patch_static_scratch(
     int32_t W, const float *d_omega, int64_t omega_stride, int32_t k, int32_t q, int32_t m,
     void *d_u, int64_t u_stride, void *d_vt, int64_t vt_stride, float *d_sigma,
     kamera_stream_t stream) {
-  if (num_problems < 0 || T < 1 || W < 1 || k < 1) return KAMERA_ERR_INVALID_ARG;
+  const kamera_status st =
+      kamera::form_patch_args(d_delta, ld, delta_stride, num_problems, T, W, d_omega,
+                              omega_stride, k, q, m, d_u, u_stride, d_vt, vt_stride, d_sigma);
+  if (st != KAMERA_OK) return st;
   if (kamera::form_patch_workspace(num_problems, T, W, k) > KAMERA_FORM_PATCH_SCRATCH_BYTES)
     return KAMERA_ERR_UNSUPPORTED;
-  if (num_problems == 0)  // argument checks only; nothing to set up or launch
-    return kamera_form_patch(d_delta, ld, delta_stride, 0, T, W, d_omega, omega_stride, k, q, m,
-                             d_u, u_stride, d_vt, vt_stride, d_sigma, nullptr, 0, stream);
   void *scratch = nullptr;
-  if (form_scratch(&scratch) != cudaSuccess) return KAMERA_ERR_CUDA;
+  if (form_scratch(&scratch) != cudaSuccess) return KAMERA_ERR_CUDA;  // set-up on a first call
+  if (num_problems == 0) return KAMERA_OK;
   return kamera_form_patch(d_delta, ld, delta_stride, num_problems, T, W, d_omega, omega_stride,
                            k, q, m, d_u, u_stride, d_vt, vt_stride, d_sigma, scratch,
                            KAMERA_FORM_PATCH_SCRATCH_BYTES, stream);
