@@ -45,6 +45,11 @@ def parse():
     ap.add_argument("--workload", choices=OTHER_WORKLOADS, default=None,
                     help="time only this one of the other workloads and print it (a profiling "
                          "entry point; not the bench line)")
+    ap.add_argument("--mla-chunks", type=int, default=64,
+                    help="chunks of the MLA recall batch (64; fewer shrink it for profilers)")
+    ap.add_argument("--sweep-requests", type=int, default=256,
+                    help="requests of the recall sweep, 4 recalls each (256: 1024 items; fewer "
+                         "shrink it for profilers)")
     ap.add_argument("--survivors-seqs", type=int, default=64,
                     help="sequences of the sliding-window survival workload (64: the full "
                          "77 GB K pool; fewer shrink it for profilers that replay the kernel)")
@@ -93,11 +98,11 @@ def accounting(w, items=None):
                             "reuse_tile_kernel": out["tensor"]["algorithmic"]})
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when there is
-    no record or the kernel's sources changed since it was taken."""
+def recorded_traffic(kernel: str, workload: str = "gqa_reorder"):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, or None
+    when there is no record or the kernel's sources changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.txt")
     try:
         rec = {}
         for line in open(path):
@@ -437,6 +442,109 @@ def whole_job_gbs(written_per_rank: int, world: int, job_ms: float) -> float:
 
 
 # ----------------------------------------------------------------------------------------
+# timing: individually event-timed runs, an L2 flush between them, median and spread
+# ----------------------------------------------------------------------------------------
+
+class L2Flush:
+    """A write of a buffer well above L2's 129 MB, issued between timed runs so that each
+    starts with nothing of its own inputs in L2."""
+    NBYTES = 512 << 20
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(self.NBYTES, dtype=torch.uint8, device=dev)
+        self.n = 0
+
+    def __call__(self, stream):
+        import torch
+        self.n += 1
+        with torch.cuda.stream(stream):
+            self.buf.fill_(self.n & 0xFF)
+
+
+def event_pairs(n, stream):
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        a.record(stream)  # creates the event handles
+        b.record(stream)
+    return ev
+
+
+def spread(ms):
+    """Median, 10th and 90th percentile (nearest rank) and mean of per-run times in ms."""
+    s = sorted(ms)
+
+    def rank(p):
+        return s[min(len(s) - 1, max(0, math.ceil(p / 100 * len(s)) - 1))]
+    return {"median_ms": statistics.median(s), "p10_ms": rank(10), "p90_ms": rank(90),
+            "mean_ms": statistics.fmean(s), "runs": len(s)}
+
+
+def kernel_fracs(kern_stats, per_kernel_bytes, peak, traffic_of=None, launches=1):
+    """Per kernel: its timing spread, algorithmic bytes per step, and achieved GB/s and
+    fraction of peak from the median. ``traffic_of`` maps a kernel to the workload tag of its
+    recorded DRAM traffic per launch; a step of ``launches`` launches carries that many."""
+    out = {}
+    for name, st in kern_stats.items():
+        kb = per_kernel_bytes[name]
+        kms = st["median_ms"]
+        gbs = kb / (kms / 1e3) / 1e9 if kms > 0 else None
+        out[name] = dict(st, ms=kms, algorithmic_bytes=kb, achieved_gbs=gbs,
+                         frac=gbs / peak if gbs is not None else None)
+        if traffic_of and name in traffic_of:
+            t = recorded_traffic(name, traffic_of[name])
+            out[name]["traffic_per_launch"] = t
+            out[name]["launches_per_step"] = launches
+    return out
+
+
+def time_split(h, launches, pool, st, runs, flush, stream):
+    """``runs`` passes of a reuse step (one kamera_batch_reuse per launch), each after an L2
+    flush, with event marks between every call's two kernels (which then run one after the
+    other). Returns the spread of the per-pass time of each kernel, summed over the launches,
+    and of the whole pass."""
+    import torch
+    import position_independent_multimodal_gb300 as km
+    marks = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in launches]
+             for _ in range(runs)]
+    for per in marks:
+        for trio in per:
+            for e in trio:
+                e.record(stream)
+    torch.cuda.synchronize()
+    for d, n, mt, mm in launches:  # warm-up pass
+        km.kamera_batch_reuse(h, d, n, mt, mm, pool, st, stream)
+    for per in marks:
+        flush(stream)
+        for (d, n, mt, mm), trio in zip(launches, per):
+            km.kamera_batch_reuse_timed(h, d, n, mt, mm, pool, st, trio, stream)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    copy = [sum(t[0].elapsed_time(t[1]) for t in per) for per in marks]
+    tile = [sum(t[1].elapsed_time(t[2]) for t in per) for per in marks]
+    return {"reuse_copy_kernel": spread(copy), "reuse_tile_kernel": spread(tile)}
+
+
+def time_steps(fn, runs, flush, stream, warmup=1):
+    """Spread of ``runs`` individually event-timed calls of ``fn``, an L2 flush before each."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    ev = event_pairs(runs, stream)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush(stream)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return spread([a.elapsed_time(b) for a, b in ev])
+
+
+# ----------------------------------------------------------------------------------------
 # the CUDA arm
 # ----------------------------------------------------------------------------------------
 
@@ -460,9 +568,11 @@ def kamera_arm(args, rank, world, local_rank):
     n_items = len(w.items)
     max_m = max(it.patch_m for it in w.items)
     stream = torch.cuda.current_stream()
+    n_split = max(20, min(args.steps, 1000))
+    flush = L2Flush(dev)
+    step_ev = event_pairs(args.steps, stream)
     # three events per split step: before, between and after the call's two kernels
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-             for _ in range(min(args.steps, 1000))]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_split)]
     for trio in marks:
         for e in trio:
             e.record(stream)  # creates the event handles
@@ -490,26 +600,38 @@ def kamera_arm(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     # the step as a user runs it: the two kernels side by side (copy kernel on the library's
-    # side stream, joined back before the next step)
+    # side stream, joined back before the next step); every step timed on its own, after an
+    # L2 flush that the events leave out
+    for a, b in step_ev:
+        flush(stream)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    # second figure: the same number of steps back to back, no flush between them
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
         step()
     e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
     # per-kernel split for the roofline: the same call with event marks between its kernels,
-    # which runs them one after the other on the stream
-    for i in range(len(marks)):
-        step(marks[i])
+    # which runs them one after the other on the stream, each step after an L2 flush
+    for trio in marks:
+        flush(stream)
+        step(trio)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    kern_ms = {"reuse_copy_kernel": statistics.fmean(t[0].elapsed_time(t[1]) for t in marks),
-               "reuse_tile_kernel": statistics.fmean(t[1].elapsed_time(t[2]) for t in marks)}
-    ms = job_time_ms(ms, world, dev)
+    step_stats = spread([a.elapsed_time(b) for a, b in step_ev])
+    b2b_ms = e0.elapsed_time(e1) / args.steps
+    kern_stats = {"reuse_copy_kernel": spread([t[0].elapsed_time(t[1]) for t in marks]),
+                  "reuse_tile_kernel": spread([t[1].elapsed_time(t[2]) for t in marks])}
+    kern_ms = {k: v["median_ms"] for k, v in kern_stats.items()}
+    ms = job_time_ms(step_stats["median_ms"], world, dev)
+    b2b_ms = job_time_ms(b2b_ms, world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    del flush
 
     e2e = None
     if not args.no_e2e:
@@ -531,18 +653,20 @@ def kamera_arm(args, rank, world, local_rank):
     s = ms / 1e3
     achieved = acc["algorithmic"] / s / 1e9
     dom = max(kern_ms, key=kern_ms.get)
-    kernels = {}
-    for name, kms in kern_ms.items():
-        kb = acc["per_kernel"][name]
-        kernels[name] = {"ms": kms, "algorithmic_bytes": kb,
-                         "achieved_gbs": kb / (kms / 1e3) / 1e9 if kms > 0 else None,
-                         "frac": kb / (kms / 1e3) / 1e9 / peak if kms > 0 else None}
+    kernels = kernel_fracs(kern_stats, acc["per_kernel"], peak)
     line = {
         "metric": METRIC,
         "value": whole_job_gbs(acc["written"], world, ms),
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "step_timing": dict(step_stats, back_to_back_mean_ms=b2b_ms,
+                            protocol=(f"{args.steps} steps each timed by its own pair of events, "
+                                      f"an L2 flush (a {L2Flush.NBYTES >> 20} MB write) before "
+                                      f"each and outside the events; ms_per_step and value are "
+                                      f"the median; back_to_back_mean_ms is the mean of "
+                                      f"{args.steps} further steps run back to back with no "
+                                      f"flush")),
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_desc(acc),
         "chunks_per_s": n_items * world / s,
@@ -558,9 +682,10 @@ def kamera_arm(args, rank, world, local_rank):
                                      else "fallback 6.8 TB/s")},
         "kernels": kernels,
         "gpu_launches": 2 * args.steps,
-        "kernel_split": (f"per-kernel times from {len(marks)} further steps with event marks "
-                         f"between the two kernels (run one after the other); the headline "
-                         f"step runs them side by side"),
+        "kernel_split": (f"per-kernel medians (p10, p90) of {len(marks)} further steps, each "
+                         f"after an L2 flush, with event marks between the two kernels (run one "
+                         f"after the other); the headline step runs them side by side; frac "
+                         f"from the median"),
         "clocks": clk,
     }
     if e2e:
@@ -574,28 +699,15 @@ def kamera_arm(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def time_calls(fn, steps, warmup=1):
-    import torch
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        fn()
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
-
-
 OTHER_WORKLOADS = ("tiny_gqa_one_chunk", "patch_readd_in_place_18_placements",
                    "decode_attention_reorder_pool",
                    "mrope_reorder_18_placements", "reanchor_18_placements", "mla_recall_64_chunks",
+                   "mla_recall_one_chunk",
                    "mha_sliding_window_448_survivors", "gqa_recall_sweep_1024_items",
                    "form_patch_84_deficits")
 
 
-def other_workloads(dev, only=None, survivors_seqs=64):
+def other_workloads(dev, only=None, survivors_seqs=64, mla_chunks=64, sweep_requests=256):
     """Brief timings of the in-place switch, decode attention over the written pool, M-RoPE
     reorder, re-anchoring, MLA recall, sliding-window survival, recall-sweep and
     patch-forming workloads (each a parity-tested configuration of its own); reported beside
@@ -610,7 +722,12 @@ def other_workloads(dev, only=None, survivors_seqs=64):
     def want(name):
         return only is None or only == name
 
-    def reuse_calls(w, launches):
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def reuse_calls(w, launches, runs=20, split=False):
+        """Median (spread) of ``runs`` individually timed steps, one kamera_batch_reuse per
+        launch, an L2 flush before each; with ``split``, also the per-kernel spread."""
         lay = w.layout
         h = km.create(lay)
         k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
@@ -624,12 +741,12 @@ def other_workloads(dev, only=None, survivors_seqs=64):
 
         def call():
             for d, n, mt, mm in packed:
-                km.kamera_batch_reuse(h, d, n, mt, mm, pool, st)
-        ms = time_calls(call, 5)
-        torch.cuda.synchronize()
+                km.kamera_batch_reuse(h, d, n, mt, mm, pool, st, stream)
+        step = time_steps(call, runs, flush, stream)
+        kern = time_split(h, packed, pool, st, runs, flush, stream) if split else None
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())}")
-        return ms
+        return step, kern
 
     if want("patch_readd_in_place_18_placements") or want("decode_attention_reorder_pool"):
         # reversible switch: the patch re-added in place on the cached rows of the 18 reorder
@@ -648,9 +765,10 @@ def other_workloads(dev, only=None, survivors_seqs=64):
         def readd():
             sign = flips[0]
             flips[0] = -sign
-            km.kamera_batch_patch_inplace(h, d_items, len(w.items), 1024, 32, pool, sign, st)
-        ms = time_calls(readd, 20, warmup=4)
-        torch.cuda.synchronize()
+            km.kamera_batch_patch_inplace(h, d_items, len(w.items), 1024, 32, pool, sign, st,
+                                          stream)
+        step = time_steps(readd, 20, flush, stream, warmup=4)
+        ms = step["median_ms"]
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())}")
         rows = sum(it.num_tokens * (it.patch_l1 - it.patch_l0) for it in w.items)
@@ -660,7 +778,7 @@ def other_workloads(dev, only=None, survivors_seqs=64):
             "workload": "GQA reorder pool (28 layers, H_kv=4 x 128): rank-32 patch re-added in place "
                         "on layers 14-27 of all 18 placements (one batched call), alternately +1 "
                         "and -1",
-            "ms_per_step": ms, "gb_s_moved": moved / ms / 1e6,
+            "ms_per_step": ms, "timing": step, "gb_s_moved": moved / ms / 1e6,
             "frac_hbm_peak": moved / ms / 1e6 / peak}
 
         # consumer check: decode attention of one query token per head (Qwen2-VL-7B: 28 query
@@ -691,8 +809,8 @@ def other_workloads(dev, only=None, survivors_seqs=64):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             attend_all_layers()
-        ms = time_calls(graph.replay, 20, warmup=3)
-        torch.cuda.synchronize()
+        step = time_steps(graph.replay, 20, flush, stream, warmup=3)
+        ms = step["median_ms"]
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())}")
         kv_bytes = reqs * ctx * lay.num_layers * (lay.row_k + lay.row_v) * 2
@@ -700,7 +818,7 @@ def other_workloads(dev, only=None, survivors_seqs=64):
             "workload": "decode attention over the reorder pool: 6 requests x 3072 tokens, 28 query "
                         "heads over 4 KV heads x 128, all 28 layers (one call per layer, replayed "
                         "from a CUDA graph)",
-            "ms_per_step": ms, "gb_s_read": kv_bytes / ms / 1e6,
+            "ms_per_step": ms, "timing": step, "gb_s_read": kv_bytes / ms / 1e6,
             "frac_hbm_peak": kv_bytes / ms / 1e6 / peak}
         del w, k, v, pool, q, ws, o_buf, graph
         torch.cuda.empty_cache()
@@ -708,11 +826,12 @@ def other_workloads(dev, only=None, survivors_seqs=64):
     if want("mrope_reorder_18_placements"):
         w = wl.config2_mrope(device=dev)
         acc = accounting(w)
-        ms = reuse_calls(w, [w.items])
+        step, _ = reuse_calls(w, [w.items])
+        ms = step["median_ms"]
         out["mrope_reorder_18_placements"] = {
             "workload": "the GQA reorder step with Qwen2.5-VL M-RoPE (16|24|24 pairs over t, h, w; "
                         "t moved by j*1024, h and w by j*16 at ordering position j)",
-            "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
+            "ms_per_call": ms, "timing": step, "gb_s_written": acc["written"] / ms / 1e6,
             "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak}
         del w
         torch.cuda.empty_cache()
@@ -728,9 +847,9 @@ def other_workloads(dev, only=None, survivors_seqs=64):
         pool = km.Pool(k, v, w.page_table.to(dev), w.num_slots)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         d_items = km.pack_anchor_items(w.items).to(dev)
-        ms = time_calls(lambda: km.kamera_reanchor(h, d_items, len(w.items), 1024, pool, st), 20,
-                        warmup=3)
-        torch.cuda.synchronize()
+        step = time_steps(lambda: km.kamera_reanchor(h, d_items, len(w.items), 1024, pool, st,
+                                                     stream), 20, flush, stream, warmup=3)
+        ms = step["median_ms"]
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())}")
         written = sum(it.num_tokens for it in w.items) * lay.num_layers * (lay.row_k + lay.row_v) * 2
@@ -741,7 +860,7 @@ def other_workloads(dev, only=None, survivors_seqs=64):
             "workload": "QV-PIC-style re-anchoring: three 32 x 32-token images stored before rotation "
                         "(Qwen2.5-VL layout, 28 layers, H_kv=4 x 128, M-RoPE 16|24|24) placed in all "
                         "6 orderings, every layer, per-token (t, h, w) positions",
-            "ms_per_call": ms, "gb_s_written": written / ms / 1e6,
+            "ms_per_call": ms, "timing": step, "gb_s_written": written / ms / 1e6,
             "frac_hbm_peak": (written + read) / ms / 1e6 / peak}
         del w, k, v, pool, d_items
         torch.cuda.empty_cache()
@@ -757,30 +876,63 @@ def other_workloads(dev, only=None, survivors_seqs=64):
         pool = km.Pool(k, torch.empty_like(k), w.page_table.to(dev), w.num_slots)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         it = w.items[0]
-        ms = time_calls(lambda: km.kamera_reuse(h, it, pool, st), 500, warmup=20)
-        torch.cuda.synchronize()
+        step = time_steps(lambda: km.kamera_reuse(h, it, pool, st, stream), 200, flush, stream,
+                          warmup=20)
+        ms = step["median_ms"]
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())}")
         out["tiny_gqa_one_chunk"] = {
             "workload": "GQA 2 layers, H_kv=2 x 64, one chunk T=256 relocated by delta=1000, "
                         "m=8 patch on both layers (one kamera_reuse call)",
-            "us_per_call": ms * 1e3, "gb_s_written": acc["written"] / ms / 1e6,
+            "us_per_call": ms * 1e3, "timing": step, "gb_s_written": acc["written"] / ms / 1e6,
             "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
             "chunks_per_s": 1 / ms * 1e3}
         del w, k, pool
         torch.cuda.empty_cache()
 
     if want("mla_recall_64_chunks"):
-        w = wl.config3(device=dev)
+        w = wl.config3(device=dev, n_chunks=mla_chunks)
         acc = accounting(w)
-        ms = reuse_calls(w, [w.items])
+        step, kern = reuse_calls(w, [w.items], split=True)
+        ms = step["median_ms"]
         out["mla_recall_64_chunks"] = {
-            "workload": "MLA (DeepSeek-V2-Lite-shaped) 27 layers, c_KV 512 + k_pe 64, 64 chunks "
-                        "T=1024, delta in [-32768, 32768], m=32 on layers 13-26",
-            "ms_per_call": ms, "gb_s_written": acc["written"] / ms / 1e6,
+            "workload": f"MLA (DeepSeek-V2-Lite-shaped) 27 layers, c_KV 512 + k_pe 64, "
+                        f"{mla_chunks} chunks T=1024, delta in [-32768, 32768], m=32 on layers "
+                        f"13-26",
+            "ms_per_call": ms, "timing": step, "gb_s_written": acc["written"] / ms / 1e6,
             "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
-            "chunks_per_s": len(w.items) / ms * 1e3}
+            "chunks_per_s": len(w.items) / ms * 1e3,
+            "kernels": kernel_fracs(kern, acc["per_kernel"], peak,
+                                    {"reuse_tile_kernel": "mla_recall"} if mla_chunks == 64
+                                    else None)}
         del w
+        torch.cuda.empty_cache()
+
+    if want("mla_recall_one_chunk"):
+        # the recall as the paper states it: one T=1024 chunk at a random offset, one
+        # kamera_reuse call (batch 1; the two kernels side by side)
+        w = wl.config3(device=dev, n_chunks=1)
+        acc = accounting(w)
+        lay = w.layout
+        h = km.create(lay)
+        k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
+        pool = km.Pool(k, None, w.page_table.to(dev), w.num_slots)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        it = w.items[0]
+        step = time_steps(lambda: km.kamera_reuse(h, it, pool, st, stream), 200, flush, stream,
+                          warmup=20)
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        ms = step["median_ms"]
+        out["mla_recall_one_chunk"] = {
+            "workload": f"MLA (DeepSeek-V2-Lite-shaped) 27 layers, c_KV 512 + k_pe 64, one chunk "
+                        f"T=1024 at delta={it.delta}, m=32 on layers 13-26, one kamera_reuse "
+                        f"call",
+            "us_per_call": ms * 1e3, "timing": step,
+            "gb_s_written": acc["written"] / ms / 1e6,
+            "frac_hbm_peak": acc["algorithmic"] / ms / 1e6 / peak,
+            "chunks_per_s": 1 / ms * 1e3}
+        del w, k, pool
         torch.cuda.empty_cache()
 
     if want("mha_sliding_window_448_survivors"):
@@ -792,31 +944,42 @@ def other_workloads(dev, only=None, survivors_seqs=64):
 
         def reloc():
             for sp in w.spans:
-                km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, st)
-        ms = time_calls(reloc, 3)
+                km.kamera_relocate(h, pool, sp.req, sp.start_tok, sp.num_tokens, sp.delta, st,
+                                   stream)
+        step = time_steps(reloc, 20, flush, stream)
+        ms = step["median_ms"]
         moved = sum(sp.num_tokens for sp in w.spans) * w.layout.num_layers * w.layout.row_k * 2 * 2
         n_seq = len(w.spans)
         pool_gb = w.k_pool.numel() * 2 / 1e9
         out["mha_sliding_window_448_survivors"] = {
             "workload": f"MHA 32 layers x 32 heads x 128, {n_seq} sequences x 7 survivor chunks of "
                         f"576 tokens re-rotated in place by delta=-576 (K pool {pool_gb:.0f} GB)",
-            "ms_per_step": ms, "gb_s_written": moved / 2 / ms / 1e6,
+            "ms_per_step": ms, "timing": step, "gb_s_written": moved / 2 / ms / 1e6,
             "frac_hbm_peak": moved / ms / 1e6 / peak,
             "chunks_per_s": 7 * n_seq / ms * 1e3}
         del w, pool
         torch.cuda.empty_cache()
 
     if want("gqa_recall_sweep_1024_items"):
-        w = wl.config5(device=dev)
+        w = wl.config5(device=dev, n_req=sweep_requests)
+        n_items = len(w.items)
         launches = [wl.config5_launch_items(w, g) for g in range(8)]
-        ms = reuse_calls(w, launches)
-        written = sum(accounting(w, items)["written"] for items in launches)
-        alg = sum(accounting(w, items)["algorithmic"] for items in launches)
+        step, kern = reuse_calls(w, launches, split=True)
+        ms = step["median_ms"]
+        accs = [accounting(w, items) for items in launches]
+        written = sum(a["written"] for a in accs)
+        alg = sum(a["algorithmic"] for a in accs)
+        per_kernel = {name: sum(a["per_kernel"][name] for a in accs)
+                      for name in accs[0]["per_kernel"]}
         out["gqa_recall_sweep_1024_items"] = {
-            "workload": "GQA 64 layers (8 launches of 8-layer slices), H_kv=8 x 128, 256 requests x "
-                        "4 recalls T=1024, delta in [0, 131072), m=64 on layers 32-63",
-            "ms_per_step": ms, "gb_s_written": written / ms / 1e6,
-            "frac_hbm_peak": alg / ms / 1e6 / peak, "chunks_per_s": 1024 / ms * 1e3}
+            "workload": f"GQA 64 layers (8 launches of 8-layer slices), H_kv=8 x 128, "
+                        f"{sweep_requests} requests x 4 recalls T=1024, delta in [0, 131072), "
+                        f"m=64 on layers 32-63",
+            "ms_per_step": ms, "timing": step, "gb_s_written": written / ms / 1e6,
+            "frac_hbm_peak": alg / ms / 1e6 / peak, "chunks_per_s": n_items / ms * 1e3,
+            "kernels": kernel_fracs(kern, per_kernel, peak,
+                                    {"reuse_tile_kernel": "recall_sweep"}
+                                    if sweep_requests == 256 else None, launches=4)}
         del w, launches
         torch.cuda.empty_cache()
 
@@ -836,7 +999,8 @@ def other_workloads(dev, only=None, survivors_seqs=64):
             km.kamera_form_patch(delta, omega, k, q, m, u, vt, sig, ws, num_problems=n, T=T, W=W,
                                  ld=W, delta_stride=T * W, omega_stride=0, u_stride=T * m,
                                  vt_stride=m * W)
-        ms = time_calls(form, 5, warmup=2)
+        step = time_steps(form, 20, flush, stream, warmup=2)
+        ms = step["median_ms"]
         # algorithmic float32 flops: the (2 + 2q) products with Δ, 12·M·k² per CholeskyQR3 on M
         # rows, and U·Σ = Q·Ũ_m (the Jacobi sweeps are not counted)
         flops = n * ((2 + 2 * q) * 2 * T * W * k + 12 * k * k * ((1 + q) * T + q * W) +
@@ -844,7 +1008,7 @@ def other_workloads(dev, only=None, survivors_seqs=64):
         out["form_patch_84_deficits"] = {
             "workload": "patch forming: 84 float32 deficits 1024 x 512 (the reorder workload's "
                         "patched layers), top 32 of a 40-column sketch, 1 power iteration",
-            "ms_per_call": ms, "deficits_per_s": n / ms * 1e3,
+            "ms_per_call": ms, "timing": step, "deficits_per_s": n / ms * 1e3,
             "gflop_s": flops / ms / 1e6,
             "delta_gb_s": (2 + 2 * q) * n * T * W * 4 / ms / 1e6}
         del delta, omega, u, vt, sig, ws
@@ -956,7 +1120,9 @@ def main():
     if args.workload is not None:
         import torch
         print(json.dumps(other_workloads(torch.device("cuda", local_rank), only=args.workload,
-                                         survivors_seqs=args.survivors_seqs)))
+                                         survivors_seqs=args.survivors_seqs,
+                                         mla_chunks=args.mla_chunks,
+                                         sweep_requests=args.sweep_requests)))
         return
     if world > 1:
         import torch

@@ -96,10 +96,11 @@ def factor_f64(a) -> np.ndarray:
 
 
 def bf16_ulp(y) -> np.ndarray:
-    """Spacing of bf16 numbers at |y| (the unit in the last place of a bf16 value)."""
+    """Spacing of bf16 numbers at |y| (the unit in the last place of a bf16 value): 2^(e-7)
+    for |y| in [2^e, 2^(e+1)), and the subnormal spacing 2^-133 below 2^-126 and at zero."""
     ay = np.abs(np.asarray(y, dtype=np.float64))
     _, E = np.frexp(ay)
-    e = np.maximum(E - 1, -126)
+    e = np.where(ay == 0, -126, np.maximum(E - 1, -126))
     return np.ldexp(1.0, e - 7)
 
 

@@ -26,3 +26,11 @@ def test_reorder_accounting_matches_the_byte_counts_of_the_workload():
     assert acc["patch"] == 3 * 14 * (2 * 1024 * 32 + 32 * 1024) * 2 == 8_257_536
     assert acc["per_kernel"]["reuse_copy_kernel"] + acc["per_kernel"]["reuse_tile_kernel"] == \
         acc["algorithmic"] + acc["meta"]
+
+
+def test_spread_gives_the_median_and_nearest_rank_percentiles():
+    s = bench.spread([float(x) for x in range(20, 0, -1)])  # 20 runs, 1..20 ms in any order
+    assert s["median_ms"] == 10.5 and s["p10_ms"] == 2.0 and s["p90_ms"] == 18.0
+    assert s["mean_ms"] == 10.5 and s["runs"] == 20
+    one = bench.spread([3.0])
+    assert one["median_ms"] == one["p10_ms"] == one["p90_ms"] == 3.0

@@ -6,7 +6,8 @@ transposed pairing, a patch that is rotated too, a double rounding, an off-by-on
 offsets or sections taken wrongly, a re-anchoring position of the wrong sign or with its
 coordinates reversed, attention without its scale, an unnormalised split merge, singular
 values in ascending order, the opposite sign convention, an error scale built from the product
-of the factor sums or counting a turned pair twice, and a re-anchoring that skips the values.
+of the factor sums or counting a turned pair twice, a re-anchoring that skips the values, and
+a bf16 spacing that is wrong at zero or one bit short.
 """
 import numpy as np
 import pytest
@@ -141,6 +142,16 @@ def magnitude_pair_twice(layout, item, layer, channel, tokens=None):
     return mag
 
 
+def ulp_from_frexp_alone(y):
+    ay = np.abs(np.asarray(y, dtype=np.float64))
+    _, E = np.frexp(ay)                      # zero is taken as if it were in [0.5, 1)
+    return np.ldexp(1.0, np.maximum(E - 1, -126) - 7)
+
+
+def ulp_one_bit_short(y):
+    return 2.0 * ora_ulp_orig(y)             # the spacing of a 7-bit significand
+
+
 def reanchor_skips_values(layout, item, k_pool, v_pool, page_table):
     ora_apply_reanchor_orig(layout, item, k_pool, None, page_table)
 
@@ -153,6 +164,7 @@ ora_axes_orig = ora.mrope_pair_axes
 ora_token_offsets_orig = ora.token_offsets
 ora_attend_orig = ora.attend
 ora_sign_rows_orig = ora._sign_rows
+ora_ulp_orig = ora.bf16_ulp
 
 
 CASES = [
@@ -188,6 +200,8 @@ CASES = [
      [lambda: pins.test_magnitude_scale_by_explicit_loops("gqa", ora.NEOX_HALF, 777)]),
     ("apply_reanchor", reanchor_skips_values, [pins.test_reanchored_items_land_at_their_slots]),
     ("slot_of", off_by_one_slot, [pins.test_reanchored_items_land_at_their_slots]),
+    ("bf16_ulp", ulp_from_frexp_alone, [pins.test_bf16_ulp_is_the_gap_to_the_next_pattern]),
+    ("bf16_ulp", ulp_one_bit_short, [pins.test_bf16_ulp_is_the_gap_to_the_next_pattern]),
 ]
 
 

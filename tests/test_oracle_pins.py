@@ -86,6 +86,18 @@ def test_bf16_nearest_by_brute_force_neighbours():
     assert np.all(err <= 0.5 * ora.bf16_ulp(got) * (1 + 1e-12))
 
 
+def test_bf16_ulp_is_the_gap_to_the_next_pattern():
+    """bf16_ulp(y) is the distance from y to the next larger bf16 value, found by stepping
+    the bit pattern, for every finite non-negative bf16 value including zero and the
+    subnormals; negative values take their magnitude's spacing."""
+    bits = np.arange(0x0000, 0x7F7F, dtype=np.uint32).astype(np.uint16)
+    y = ora.bf16_to_f64(bits)
+    nxt = ora.bf16_to_f64((bits + 1).astype(np.uint16))
+    np.testing.assert_array_equal(ora.bf16_ulp(y), nxt - y)
+    np.testing.assert_array_equal(ora.bf16_ulp(-y), nxt - y)
+    assert ora.bf16_ulp(0.0) == 2.0 ** -133 and ora.bf16_ulp(1.0) == 2.0 ** -7
+
+
 def test_bf16_decode_encode_roundtrip_all_patterns():
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     vals = ora.bf16_to_f64(bits)
