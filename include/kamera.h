@@ -367,13 +367,15 @@ kamera_status kamera_decode_attention(const kamera_handle *handle, const kamera_
  *   Y = Delta Omega; Q = orth(Y); q times: Z = orth(Delta^T Q), Q = orth(Delta Z);
  *   B^T = Delta^T Q = V_B Sigma Ut^T; U*Sigma = Q Ut_m Sigma_m; V_m^T = (B^T Ut_m)^T / Sigma_m,
  * sigma descending, each row of V_m^T signed so that its largest-magnitude entry (the first on
- * a tie) is positive, the matching column of U*Sigma flipped with it. float32 arithmetic.
+ * a tie) is positive, the matching column of U*Sigma flipped with it. float32 arithmetic; the
+ * products with Delta run on the tensor cores with float32 operands split into two tf32 terms,
+ * which keeps them float32-accurate. A chain of kernels is launched on `stream`; the call
+ * returns once they are queued.
  *   d_delta     : float32; problem i is the [T][W] matrix at d_delta + i*delta_stride with row
  *                 stride ld >= W (elements).
  *   d_omega     : float32 [W][k] random test matrix of problem i at d_omega + i*omega_stride
  *                 (omega_stride 0: one matrix for all problems), drawn by the caller.
- *   k           : sketch width, m <= k <= min(T, W, 96), with
- *                 4 * (14400 + 3k^2 + kW + 3k) <= 232448 (shared memory of the kernel).
+ *   k           : sketch width, m <= k <= min(T, W, 96).
  *   q           : power iterations, 0..16.   m : rank kept, 1..k.
  *   d_u, d_vt   : bf16 outputs, problem i's U*Sigma [T][m] at d_u + i*u_stride and V_m^T
  *                 [m][W] at d_vt + i*vt_stride (elements). The strides place the results
@@ -383,9 +385,13 @@ kamera_status kamera_decode_attention(const kamera_handle *handle, const kamera_
  *   d_sigma     : float32 [num_problems][m] singular values, or NULL.
  *   d_workspace : device scratch of at least kamera_form_patch_workspace(num_problems, T, W, k)
  *                 bytes, 4-byte aligned; contents on entry are ignored and left undefined.
+ *                 That is num_problems * 4 bytes * ((T + W) * k + nt * (k^2 + 3k) + 9k^2 + k
+ *                 + 4) with nt = ceil(max(T, W) / 128), the float count per problem rounded up
+ *                 to a multiple of 4.
  * Columns past the numerical rank of Delta come out with sigma near zero (zero factors for an
  * exactly zero deficit). Host checks return INVALID_ARG (bad pointer, size, stride, too small
- * a workspace) or UNSUPPORTED (k or the shared memory above the limits) and launch nothing.
+ * a workspace) or UNSUPPORTED (k above the limit) and launch nothing. A device-side wait that
+ * runs out of time (2 s) leaves NaN in the problem's outputs.
  */
 size_t kamera_form_patch_workspace(int32_t num_problems, int32_t T, int32_t W, int32_t k);
 
@@ -406,10 +412,10 @@ kamera_status kamera_form_patch(const float *d_delta, int64_t ld, int64_t delta_
  *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library routine.
  *   - Arguments, outputs and results are those of kamera_form_patch, and so are its argument
  *     errors, which are checked first. Then a call whose kamera_form_patch_workspace(
- *     num_problems, T, W, k) exceeds KAMERA_FORM_PATCH_SCRATCH_BYTES (32 MiB: e.g. 96 deficits
- *     of 1024 x 512 at k = 40) returns KAMERA_ERR_UNSUPPORTED and launches nothing.
+ *     num_problems, T, W, k) exceeds KAMERA_FORM_PATCH_SCRATCH_BYTES (32 MiB: e.g. more than 93
+ *     deficits of 1024 x 512 at k = 40) returns KAMERA_ERR_UNSUPPORTED and launches nothing.
  *   - Set-up: the first call on a device, with that device current, looks up the array's
- *     device address and loads and configures the kernel; a failure returns KAMERA_ERR_CUDA.
+ *     device address and loads and configures the kernels; a failure returns KAMERA_ERR_CUDA.
  *     CUDA reserves the array when it loads this library's device code, which by default
  *     (lazy module loading) happens at that set-up, not earlier. A call with num_problems = 0
  *     and otherwise valid arguments does the set-up alone: make one on each device before

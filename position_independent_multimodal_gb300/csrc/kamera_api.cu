@@ -555,7 +555,7 @@ kamera_status form_patch_args(const float *d_delta, int64_t ld, int64_t delta_st
   if (num_problems < 0 || T < 1 || W < 1) return KAMERA_ERR_INVALID_ARG;
   if (k < 1 || m < 1 || m > k || q < 0) return KAMERA_ERR_INVALID_ARG;
   if (k > kMaxSketch || k > T || k > W || q > 16) return KAMERA_ERR_UNSUPPORTED;
-  if (form_patch_smem(W, k) > (size_t)kMaxFormSmem) return KAMERA_ERR_UNSUPPORTED;
+  if (form_patch_smem(k) > (size_t)kMaxFormSmem) return KAMERA_ERR_UNSUPPORTED;
   if (ld < W || delta_stride < 0 || omega_stride < 0 || u_stride < 0 || vt_stride < 0)
     return KAMERA_ERR_INVALID_ARG;
   if (num_problems > 1 && (u_stride < (int64_t)T * m || vt_stride < (int64_t)m * W))

@@ -526,7 +526,7 @@ struct FormArgs {
 
 // Kernel launchers.
 size_t form_patch_workspace(long long n, int T, int W, int k);  // kamera_form.cu
-size_t form_patch_smem(int W, int k);
+size_t form_patch_smem(int k);  // the largest of the patch-forming kernels
 cudaError_t launch_form_patch(const FormArgs &a, cudaStream_t s);
 cudaError_t prepare_form_patch();  // loads the kernel and sets its shared-memory limit
 // The argument checks of kamera_form_patch other than those of the workspace.

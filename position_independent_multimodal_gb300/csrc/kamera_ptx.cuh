@@ -178,6 +178,36 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
   return d;
 }
 
+// Instruction descriptor of kind::tf32: tf32 A and B (format 2), float32 D, both K-major.
+__host__ __device__ __forceinline__ uint32_t idesc_tf32_f32(int M, int N) {
+  uint32_t d = 0;
+  d |= 1u << 4;                                   // D format: f32
+  d |= 2u << 7;                                   // A format: tf32
+  d |= 2u << 10;                                  // B format: tf32
+  d |= (static_cast<uint32_t>(N >> 3) & 0x3Fu) << 17;
+  d |= (static_cast<uint32_t>(M >> 4) & 0x1Fu) << 24;
+  return d;
+}
+
+// D[tmem] (+)= A[smem] * B[smem] with tf32 operands (K = 8 per instruction), one thread.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// x rounded to the nearest tf32 value (ties away from zero), as a float32 bit pattern whose
+// low 13 bits are zero.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
 // D[tmem] (+)= A[smem] * B[smem], issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {

@@ -244,8 +244,14 @@ class FakeWorkspace(FakeTensor):
 def test_form_patch_host_checks(lib):
     n, T, W, k, q, m = 3, 100, 64, 16, 1, 8
     need = km.kamera_form_patch_workspace(n, T, W, k)
-    assert need == n * 2 * max(T, W) * k * 4
-    assert km.kamera_form_patch_workspace(n, 40, 300, k) == n * 2 * 300 * k * 4
+
+    def documented(n, T, W, k):  # floats per problem, rounded up to a multiple of 4
+        nt = -(-max(T, W) // 128)
+        per = (T + W) * k + nt * (k * k + 3 * k) + 9 * k * k + k + 4
+        return n * (-(-per // 4) * 4) * 4
+    assert need == documented(n, T, W, k) == 63024
+    assert km.kamera_form_patch_workspace(n, 40, 300, k) == documented(n, 40, 300, k) == 104112
+    assert km.kamera_form_patch_workspace(1, 1024, 512, 40) == 358576
     assert km.kamera_form_patch_workspace(-1, T, W, k) == 0
     d, o = FakeTensor(0x100000), FakeTensor(0x200000)
     u, vt, sig = FakeTensor(0x300000), FakeTensor(0x400000), FakeTensor(0x500000)
@@ -275,9 +281,9 @@ def test_form_patch_host_checks(lib):
         with pytest.raises(km.KameraError) as e:
             call(**kw)
         assert e.value.status == km.KAMERA_ERR_INVALID_ARG, kw
-    # k above 96, above T or W, too many power iterations, or too much shared memory
+    # k above 96, above T or W, or too many power iterations (W itself is not bounded)
     unsupported = [dict(k=97, m=8, T=200, W=200), dict(k=64, T=63), dict(k=65, W=64),
-                   dict(q=17), dict(k=96, W=600, T=600)]
+                   dict(q=17)]
     for kw in unsupported:
         with pytest.raises(km.KameraError) as e:
             call(**kw)

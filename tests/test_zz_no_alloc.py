@@ -71,7 +71,7 @@ def _assert_close(ref, got):
 
 @pytest.mark.gpu
 def test_static_scratch_matches_workspace_entry_on_two_calls_in_a_row(cuda_ok):
-    # the 84 deficits of the reorder workload (27.5 MB of scratch), then a smaller problem set
+    # the 84 deficits of the reorder workload (30.1 MB of scratch), then a smaller problem set
     # with per-problem test matrices and two power iterations, issued back to back
     a = _case(84, 1024, 512, 40, 32, 1, True, seed=21)
     b = _case(5, 300, 256, 24, 16, 2, False, seed=22)
@@ -136,7 +136,7 @@ def test_static_scratch_takes_no_memory_after_its_set_up_in_a_fresh_process(cuda
 
 
 def test_static_scratch_checks_arguments_before_its_limit():
-    # 200 deficits of 1024 x 512 at k = 40 need 65.5 MB of workspace, above the 32 MiB array:
+    # 200 deficits of 1024 x 512 at k = 40 need 71.7 MB of workspace, above the 32 MiB array:
     # with valid arguments that is UNSUPPORTED; a bad argument is reported first, as
     # kamera_form_patch reports it. Nothing is launched or set up, so no GPU is needed.
     n, T, W, k, m = 200, 1024, 512, 40, 32
