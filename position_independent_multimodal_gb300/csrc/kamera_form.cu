@@ -682,54 +682,76 @@ __device__ __forceinline__ void rr_pair(int n, int round, int i, int &p, int &q)
 }
 
 // One-sided Jacobi on the columns of a [k × k] (column-major), rotations accumulated into
-// v [k × k] (column-major, set to I here). Eight lanes own one pair for its whole rotation, so
-// a warp turns four pairs at once.
-__device__ void jacobi_small(float *a, float *v, int k) {
+// v [k × k] (column-major, set to I here); pairs: (k + 1)² / 4 int2 of shared scratch for the
+// round-robin schedule, computed once. Eight lanes own one pair for its whole rotation, so a
+// warp turns four pairs at once; the pair's columns stay in registers from the dot products to
+// the rotation. The rotation's parameters use the hardware reciprocal and reciprocal square
+// root (a few ulp): any rotation with cs² + sn² = 1 to that accuracy serves, as the columns are
+// orthogonalised, not the angles reproduced.
+__device__ void jacobi_small(float *a, float *v, int k, int2 *pairs) {
+  constexpr int G = 8, PW = 32 / G, E = (kMaxSketch + G - 1) / G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sub = lane & 7;
+  const int sub = lane % G, slot = lane / G;
+  const int n = k + (k & 1), h = n / 2;  // an odd k plays a dummy column
+  for (int e = tid; e < (n - 1) * h; e += kThr) {
+    const int round = e / h, i = e - round * h;
+    int p, q;
+    rr_pair(n, round, i, p, q);
+    pairs[e] = (p < k && q < k) ? make_int2(p, q) : make_int2(-1, -1);
+  }
   for (int e = tid; e < k * k; e += kThr) v[e] = (e / k == e % k) ? 1.f : 0.f;
   __syncthreads();
-  const int n = k + (k & 1);  // an odd k plays a dummy column
-  const float tol = sqrtf((float)k) * 1.1920929e-7f;
+  const float tol2 = (float)k * 1.1920929e-7f * 1.1920929e-7f;  // (√k·2⁻²³)²
   for (int sweep = 0; sweep < 30; ++sweep) {
     int rotated = 0;
     for (int round = 0; round < n - 1; ++round) {
-      for (int i0 = 4 * warp; i0 < n / 2; i0 += 4 * kWarps) {  // warp-uniform
-        const int i = i0 + (lane >> 3);
-        int pc = 0, qc = 0;
-        bool live = i < n / 2;
-        if (live) {
-          rr_pair(n, round, i, pc, qc);
-          live = pc < k && qc < k;
+      for (int i0 = PW * warp; i0 < h; i0 += PW * kWarps) {  // warp-uniform
+        const int i = i0 + slot;
+        const int2 pq = i < h ? pairs[round * h + i] : make_int2(-1, -1);
+        const bool live = pq.x >= 0;
+        float *x = a + (long long)(live ? pq.x : 0) * k, *y = a + (long long)(live ? pq.y : 0) * k;
+        float xr[E], yr[E], al = 0.f, be = 0.f, ga = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int w = sub + G * e;
+          xr[e] = (live && w < k) ? x[w] : 0.f;
+          yr[e] = (live && w < k) ? y[w] : 0.f;
         }
-        float *x = a + (long long)pc * k, *y = a + (long long)qc * k;
-        float al = 0.f, be = 0.f, ga = 0.f;
-        if (live)
-          for (int w = sub; w < k; w += 8) {
-            const float xv = x[w], yv = y[w];
-            al = fmaf(xv, xv, al);
-            be = fmaf(yv, yv, be);
-            ga = fmaf(xv, yv, ga);
-          }
-        for (int o = 4; o > 0; o >>= 1) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          al = fmaf(xr[e], xr[e], al);
+          be = fmaf(yr[e], yr[e], be);
+          ga = fmaf(xr[e], yr[e], ga);
+        }
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) {
           al += __shfl_xor_sync(0xffffffffu, al, o);
           be += __shfl_xor_sync(0xffffffffu, be, o);
           ga += __shfl_xor_sync(0xffffffffu, ga, o);
         }
-        if (live && fabsf(ga) > tol * sqrtf(al) * sqrtf(be)) {
-          const float zeta = (be - al) / (2.f * ga);
-          const float t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.f)));
-          const float cs = 1.f / sqrtf(fmaf(t, t, 1.f)), sn = cs * t;
-          for (int w = sub; w < k; w += 8) {
-            const float xv = x[w], yv = y[w];
-            x[w] = cs * xv - sn * yv;
-            y[w] = sn * xv + cs * yv;
+        // |γ| > tol·√(αβ): not yet orthogonal (a zero column never is rotated)
+        if (live && ga * ga > tol2 * al * be) {
+          const float zeta = (be - al) * __frcp_rn(2.f * ga);
+          const float t =
+              copysignf(1.f, zeta) * __frcp_rn(fabsf(zeta) + sqrtf(fmaf(zeta, zeta, 1.f)));
+          const float cs = rsqrtf(fmaf(t, t, 1.f)), sn = cs * t;
+          float *vx = v + (long long)pq.x * k, *vy = v + (long long)pq.y * k;
+          float vxr[E], vyr[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int w = sub + G * e;
+            vxr[e] = w < k ? vx[w] : 0.f;
+            vyr[e] = w < k ? vy[w] : 0.f;
           }
-          float *vx = v + (long long)pc * k, *vy = v + (long long)qc * k;
-          for (int w = sub; w < k; w += 8) {
-            const float xv = vx[w], yv = vy[w];
-            vx[w] = cs * xv - sn * yv;
-            vy[w] = sn * xv + cs * yv;
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int w = sub + G * e;
+            if (w < k) {
+              x[w] = cs * xr[e] - sn * yr[e];
+              y[w] = sn * xr[e] + cs * yr[e];
+              vx[w] = cs * vxr[e] - sn * vyr[e];
+              vy[w] = sn * vxr[e] + cs * vyr[e];
+            }
           }
           rotated = 1;
         }
@@ -751,7 +773,7 @@ struct SvdArgs {
 };
 
 __host__ __device__ inline size_t svd_smem(int k) {
-  return 4 * ((size_t)4 * k * k + 2 * k + 8);
+  return 4 * ((size_t)4 * k * k + 2 * k + 8) + 8 * (size_t)((k + 1) / 2) * (k + 1);
 }
 
 __global__ void __launch_bounds__(kThr, 1) form_svd_kernel(const __grid_constant__ SvdArgs a) {
@@ -762,6 +784,7 @@ __global__ void __launch_bounds__(kThr, 1) form_svd_kernel(const __grid_constant
   float *r = fsm, *v = r + k * k, *t1 = v + k * k, *l3 = t1 + k * k;
   float *nrm = l3 + k * k;
   int *order = reinterpret_cast<int *>(nrm + k);
+  int2 *pairs = reinterpret_cast<int2 *>(fsm + ((4 * k * k + 2 * k + 8 + 1) & ~1));
   const float *L1 = r, *L2 = v;  // staged where R_B and Ṽ go later
   load_vec(a.lb1 + wo, k * k, r);
   load_vec(a.lb2 + wo, k * k, v);
@@ -784,7 +807,7 @@ __global__ void __launch_bounds__(kThr, 1) form_svd_kernel(const __grid_constant
     r[e] = s;
   }
   __syncthreads();
-  jacobi_small(r, v, k);
+  jacobi_small(r, v, k, pairs);
 
   // σ_j = ‖column j‖, then the columns by σ (descending, ties by column index)
   for (int j = warp; j < k; j += kWarps) {
