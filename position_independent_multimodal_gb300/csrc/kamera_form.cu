@@ -312,34 +312,52 @@ __device__ void store_tile(const float *y, int P, int rows, int k, float *dst) {
 }
 
 // dst tile = src tile · L⁻ᵀ (li[l·k + j] = L⁻¹[j][l]), all 128 rows. Thread (lane, warp) owns
-// rows lane + 32i (i < 4) and columns warp + 8c (c < 12): each step over l reads four tile
-// values and up to twelve L⁻ᵀ values (the same for the whole warp) for up to 48 products.
-__device__ void apply_linv(const float *src, float *dst, int P, int k, const float *li) {
-  const int rg = threadIdx.x & 31, cg = threadIdx.x >> 5;
-  const int nc = (k - cg + 7) >> 3;  // columns of this warp
-  float acc[4][12];
+// rows lane + 32i (i < 4) and the NC columns warp + 8c of its warp (NC = ⌈(k − warp) / 8⌉, a
+// compile-time count so that no product slot is idle): each step over l reads four tile values
+// and NC L⁻ᵀ values (the same for the whole warp) for 4·NC products.
+template <int NC>
+__device__ void apply_linv_cols(const float *src, float *dst, int P, int k, const float *li,
+                                int rg, int cg) {
+  float acc[4][NC];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int c = 0; c < 12; ++c) acc[i][c] = 0.f;
+    for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
   for (int l = 0; l < k; ++l) {
     float x[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] = src[(rg + 32 * i) * P + l];
     const float *w = li + l * k + cg;
 #pragma unroll
-    for (int c = 0; c < 12; ++c)
-      if (c < nc) {
-        const float wc = w[8 * c];
+    for (int c = 0; c < NC; ++c) {
+      const float wc = w[8 * c];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][c] = fmaf(x[i], wc, acc[i][c]);
-      }
+      for (int i = 0; i < 4; ++i) acc[i][c] = fmaf(x[i], wc, acc[i][c]);
+    }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int c = 0; c < 12; ++c)
-      if (c < nc) dst[(rg + 32 * i) * P + cg + 8 * c] = acc[i][c];
+    for (int c = 0; c < NC; ++c) dst[(rg + 32 * i) * P + cg + 8 * c] = acc[i][c];
+}
+
+__device__ void apply_linv(const float *src, float *dst, int P, int k, const float *li) {
+  const int rg = threadIdx.x & 31, cg = threadIdx.x >> 5;
+  switch ((k - cg + 7) >> 3) {  // warp-uniform
+    case 1: apply_linv_cols<1>(src, dst, P, k, li, rg, cg); break;
+    case 2: apply_linv_cols<2>(src, dst, P, k, li, rg, cg); break;
+    case 3: apply_linv_cols<3>(src, dst, P, k, li, rg, cg); break;
+    case 4: apply_linv_cols<4>(src, dst, P, k, li, rg, cg); break;
+    case 5: apply_linv_cols<5>(src, dst, P, k, li, rg, cg); break;
+    case 6: apply_linv_cols<6>(src, dst, P, k, li, rg, cg); break;
+    case 7: apply_linv_cols<7>(src, dst, P, k, li, rg, cg); break;
+    case 8: apply_linv_cols<8>(src, dst, P, k, li, rg, cg); break;
+    case 9: apply_linv_cols<9>(src, dst, P, k, li, rg, cg); break;
+    case 10: apply_linv_cols<10>(src, dst, P, k, li, rg, cg); break;
+    case 11: apply_linv_cols<11>(src, dst, P, k, li, rg, cg); break;
+    case 12: apply_linv_cols<12>(src, dst, P, k, li, rg, cg); break;
+    default: break;  // k − warp ≤ 0: no columns
+  }
 }
 
 // ---------------------------------------------------------------------------------------
