@@ -548,6 +548,17 @@ def time_steps(fn, runs, flush, stream, warmup=1):
 # the CUDA arm
 # ----------------------------------------------------------------------------------------
 
+def batch_handle(km, lay, n_items, dev):
+    """A handle with a batch workspace for batches of up to n_items items: the library plans
+    such batches on the device and runs their patched layers as a persistent kernel (it keeps
+    its per-tile grid kernel for batches that do not fit that path)."""
+    import torch
+    h = km.create(lay)
+    ws = torch.empty(km.kamera_batch_workspace_bytes(h, n_items), dtype=torch.uint8, device=dev)
+    km.kamera_set_batch_workspace(h, ws)
+    return h
+
+
 def kamera_arm(args, rank, world, local_rank):
     import torch
     import position_independent_multimodal_gb300 as km
@@ -558,7 +569,7 @@ def kamera_arm(args, rank, world, local_rank):
     w = wl.config2(seed=rank_seed(rank), device=dev)
     lay = w.layout
     acc = accounting(w)
-    h = km.create(lay)
+    h = batch_handle(km, lay, len(w.items), dev)
     k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
     v = torch.empty(lay.num_layers, w.num_slots, lay.row_v, dtype=torch.bfloat16, device=dev)
     pt = w.page_table.to(dev)
@@ -729,7 +740,7 @@ def other_workloads(dev, only=None, survivors_seqs=64, mla_chunks=64, sweep_requ
         """Median (spread) of ``runs`` individually timed steps, one kamera_batch_reuse per
         launch, an L2 flush before each; with ``split``, also the per-kernel spread."""
         lay = w.layout
-        h = km.create(lay)
+        h = batch_handle(km, lay, max(len(items) for items in launches), dev)
         k = torch.empty(lay.num_layers, w.num_slots, lay.row_k, dtype=torch.bfloat16, device=dev)
         v = (torch.empty(lay.num_layers, w.num_slots, lay.row_v, dtype=torch.bfloat16,
                          device=dev) if lay.kind == wl.GQA else None)

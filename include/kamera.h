@@ -192,6 +192,34 @@ const char *kamera_status_string(kamera_status status);
 kamera_status kamera_set_option(kamera_handle *handle, int32_t option, int32_t value);
 
 /*
+ * Batch workspace of a handle (the pages have no counterpart: it selects how the patched layers
+ * of kamera_batch_reuse are scheduled, not what they compute). With a workspace of at least
+ * kamera_batch_workspace_bytes(handle, num_items) bytes, a kamera_batch_reuse call of the
+ * handle first plans the batch on the device (its groups and a list of its patched rows,
+ * written into the workspace) and then runs the patched layers as a persistent kernel: sets of
+ * CTAs, one per column tile, each set walking an equal share of the rows' token tiles. Without
+ * a workspace, or when the batch does not fit this path, the call runs them as one CTA per
+ * (item, layer, channel, column tile) as before. The bytes written to the pool are the same
+ * either way.
+ * Batches that take the persistent path: GQA/MHA layouts whose patched layers run on the
+ * tensor-core tile kernel (NeoX-half pairing, column tiles of 64 or 128 whole-head columns),
+ * d_items 16-byte aligned, at most 2048 items and num_items x num_layers x 2 <= 16384,
+ * KAMERA_OPT_SHARE_RUN_PATCHED at most 4, and a rank small enough for two V_m^T buffers and
+ * two CTAs per SM in shared memory (max_patch_m <= 48 where a column tile is 128 wide).
+ * kamera_batch_workspace_bytes: bytes for batches of up to num_items items (0 for a NULL
+ * handle or num_items < 0).
+ * kamera_set_batch_workspace: d_workspace is device memory owned by the caller, 256-byte
+ * aligned, of `bytes` bytes (at least kamera_batch_workspace_bytes(handle, 1)); the handle
+ * keeps the pointer until it is set again or the handle is destroyed. NULL with bytes 0
+ * removes it. Calls that use the same handle's workspace must not run at the same time on
+ * the device: order them on one stream (a later call overwrites the plan of an earlier one).
+ * Returns KAMERA_ERR_INVALID_ARG (and changes nothing) for a NULL handle, a misaligned or too
+ * small workspace, or NULL with bytes != 0.
+ */
+size_t kamera_batch_workspace_bytes(const kamera_handle *handle, int32_t num_items);
+kamera_status kamera_set_batch_workspace(kamera_handle *handle, void *d_workspace, size_t bytes);
+
+/*
  * Survivor relocation, in place (§5 "Sliding-window survival": keep the survivor's KV as-is
  * and apply R(delta); Fig. 2: rotate_k_pe_inplace). Rotates the rope columns of K (GQA/MHA:
  * every head; MLA: the k_pe band only) of logical tokens [start_tok, start_tok+num_tokens)

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     KAMERA_MROPE_CONTIGUOUS, KAMERA_MROPE_INTERLEAVED, KAMERA_OK,
     KAMERA_ROPE_INTERLEAVED, KAMERA_ROPE_NEOX_HALF, LIB_PATH, Handle, KameraError, Pool,
     create, kamera_batch_patch_inplace, kamera_batch_reuse, kamera_batch_reuse_timed,
+    kamera_batch_workspace_bytes, kamera_set_batch_workspace,
     kamera_form_patch, kamera_form_patch_static_scratch, kamera_form_patch_workspace,
     kamera_decode_attention, kamera_decode_attention_workspace, kamera_patch_inplace,
     kamera_reanchor, pack_anchor_items, kamera_relocate,

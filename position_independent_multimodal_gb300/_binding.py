@@ -92,6 +92,9 @@ def lib() -> ctypes.CDLL:
         L.kamera_status_string.argtypes = [ctypes.c_int]
         L.kamera_status_string.restype = ctypes.c_char_p
         L.kamera_set_option.argtypes = [vp, i32, i32]
+        L.kamera_batch_workspace_bytes.argtypes = [vp, i32]
+        L.kamera_batch_workspace_bytes.restype = ctypes.c_size_t
+        L.kamera_set_batch_workspace.argtypes = [vp, vp, ctypes.c_size_t]
         L.kamera_relocate.argtypes = [vp, ctypes.POINTER(kamera_pool), i32, i32, i32, i64, vp, vp]
         L.kamera_reuse.argtypes = [vp, ctypes.POINTER(kamera_item), ctypes.POINTER(kamera_pool),
                                    vp, vp]
@@ -118,6 +121,7 @@ def lib() -> ctypes.CDLL:
         L.kamera_form_patch_static_scratch.argtypes = [vp, i64, i64, i32, i32, i32, vp, i64,
                                                        i32, i32, i32, vp, i64, vp, i64, vp, vp]
         for f in ("kamera_create", "kamera_destroy", "kamera_relocate", "kamera_reuse",
+                  "kamera_set_option", "kamera_set_batch_workspace",
                   "kamera_batch_reuse", "kamera_rope_phases", "kamera_batch_reuse_timed",
                   "kamera_patch_inplace", "kamera_batch_patch_inplace", "kamera_form_patch",
                   "kamera_form_patch_static_scratch", "kamera_reanchor",
@@ -195,6 +199,23 @@ def kamera_set_option(handle: Handle, option, value: int) -> None:
     """kamera_set_option; `option` is a KAMERA_OPT_* value or its keyword name."""
     opt = _OPTIONS[option] if isinstance(option, str) else int(option)
     _check(lib().kamera_set_option(handle.ptr, opt, int(value)), "kamera_set_option")
+
+
+def kamera_batch_workspace_bytes(handle: Handle, num_items: int) -> int:
+    """kamera_batch_workspace_bytes: workspace bytes for batches of up to num_items items."""
+    return int(lib().kamera_batch_workspace_bytes(handle.ptr, int(num_items)))
+
+
+def kamera_set_batch_workspace(handle: Handle, workspace: Optional[torch.Tensor]) -> None:
+    """kamera_set_batch_workspace with a device tensor (its bytes), or None to remove it. The
+    handle object keeps a reference to the tensor while the library holds its pointer."""
+    if workspace is None:
+        _check(lib().kamera_set_batch_workspace(handle.ptr, None, 0), "kamera_set_batch_workspace")
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+        _check(lib().kamera_set_batch_workspace(handle.ptr, workspace.data_ptr(), nbytes),
+               "kamera_set_batch_workspace")
+    handle.batch_workspace = workspace
 
 
 class Pool:

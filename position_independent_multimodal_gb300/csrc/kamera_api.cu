@@ -15,6 +15,8 @@ struct kamera_handle {
   int engine;     // engine of patched tiles (KAMERA_OPT_PATCH_ENGINE)
   int run_tile;   // most members of a group written from one computed tile, patched layers
   int run_copy;   // the same on unpatched layers
+  void *ws = nullptr;     // batch workspace (kamera_set_batch_workspace), device memory
+  size_t ws_bytes = 0;
 };
 
 namespace {
@@ -171,23 +173,27 @@ SideStream *side_stream() {
 // (layouts served by the tile kernel); otherwise the two kernels in order on the caller's
 // stream. `unpatched` false (a single item patched on every layer, checked on the host): the
 // copy kernel would have nothing to do, so only the patched-layer kernel is launched.
+// Patched layers: the persistent kernel when the batch has a workspace, else the grid kernel
+// on the layouts it serves, else the general pipeline.
+cudaError_t launch_patched(const kamera::ReuseArgs &a, int n_items, cudaStream_t s) {
+  if (!a.smem.fast) return kamera::launch_reuse(a, n_items, s);
+  return a.plan_ws ? kamera::launch_reuse_persist(a, s)
+                   : kamera::launch_reuse_tile(a, n_items, s);
+}
+
 cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, cudaStream_t s,
                         bool unpatched = true) {
-  if (patched && !unpatched)
-    return a.smem.fast ? kamera::launch_reuse_tile(a, n_items, s)
-                       : kamera::launch_reuse(a, n_items, s);
+  if (patched && !unpatched) return launch_patched(a, n_items, s);
   SideStream *ss = (a.smem.fast && patched) ? side_stream() : nullptr;
   if (!ss) {
     cudaError_t e = kamera::launch_reuse_copy(a, s);
-    if (e == cudaSuccess && patched)
-      e = a.smem.fast ? kamera::launch_reuse_tile(a, n_items, s)
-                      : kamera::launch_reuse(a, n_items, s);
+    if (e == cudaSuccess && patched) e = launch_patched(a, n_items, s);
     return e;
   }
   std::lock_guard<std::mutex> lock(ss->mu);  // one fork/join at a time per device
   cudaError_t e = cudaEventRecord(ss->fork, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
-  if (e == cudaSuccess) e = kamera::launch_reuse_tile(a, n_items, s);
+  if (e == cudaSuccess) e = launch_patched(a, n_items, s);
   if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, ss->stream);
   if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ss->join, 0);
@@ -250,6 +256,27 @@ kamera_status kamera_set_option(kamera_handle *h, int32_t option, int32_t value)
       return KAMERA_OK;
   }
   return KAMERA_ERR_INVALID_ARG;
+}
+
+size_t kamera_batch_workspace_bytes(const kamera_handle *h, int32_t num_items) {
+  if (!h || num_items < 0) return 0;
+  return kamera::persist_workspace_bytes(h->lay, num_items);
+}
+
+kamera_status kamera_set_batch_workspace(kamera_handle *h, void *d_workspace, size_t bytes) {
+  if (!h) return KAMERA_ERR_INVALID_ARG;
+  if (!d_workspace) {
+    if (bytes != 0) return KAMERA_ERR_INVALID_ARG;
+    h->ws = nullptr;
+    h->ws_bytes = 0;
+    return KAMERA_OK;
+  }
+  if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0 ||
+      bytes < kamera::persist_workspace_bytes(h->lay, 1))
+    return KAMERA_ERR_INVALID_ARG;
+  h->ws = d_workspace;
+  h->ws_bytes = bytes;
+  return KAMERA_OK;
 }
 
 kamera_status kamera_destroy(kamera_handle *handle) {
@@ -344,6 +371,15 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
   a.freq = h->freq;
   if ((long long)h->lay.ntile * num_items * h->lay.L * h->lay.n_ch > 0x7FFFFFFFll)
     return KAMERA_ERR_UNSUPPORTED;
+  if (h->ws && a.smem.fast && max_patch_m > 0 &&
+      (reinterpret_cast<uintptr_t>(d_items) & 15u) == 0 &&
+      h->ws_bytes >= kamera::persist_workspace_bytes(h->lay, num_items)) {
+    const kamera::SmemPlan pp = kamera::reuse_persist_plan(h->lay, a.max_m, h->run_tile);
+    if (kamera::persist_batch_ok(h->lay, pp, num_items, max_tokens)) {
+      a.smem = pp;
+      a.plan_ws = h->ws;
+    }
+  }
   const cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
   auto mark = [&](int i) -> cudaError_t {
     if (!events || !events[i]) return cudaSuccess;
@@ -354,9 +390,7 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess && max_patch_m > 0)
-    e = a.smem.fast ? kamera::launch_reuse_tile(a, num_items, strm)
-                    : kamera::launch_reuse(a, num_items, strm);
+  if (e == cudaSuccess && max_patch_m > 0) e = launch_patched(a, num_items, strm);
   if (e == cudaSuccess) e = mark(2);
   return from_cuda(e);
 }

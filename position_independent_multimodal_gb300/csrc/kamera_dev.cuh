@@ -56,7 +56,8 @@ struct SmemPlan {
   int tmem_cols;         // TMEM columns to allocate (0: no patched tiles possible)
   int acc_cols;          // TMEM columns of one accumulator
   int u_bufs;            // U buffers (2: staged two tiles ahead; 1: after each MMA)
-  int fast;              // 1: plan of reuse_tile_kernel (swizzled tile, identity operand at desc)
+  int fast;              // 1: plan of the tile kernels (swizzled canonical stages)
+  int recs;              // persistent kernel: task records in shared memory
 };
 
 // A column tile: [col0, col0 + ncols) of a channel's row.
@@ -120,6 +121,7 @@ struct ReuseArgs {
   int inplace;               // 1: patch re-add on cached rows (read from and written to the pool)
   int sign;                  // inplace: +1 adds U V_m^T, -1 subtracts it
   int run_copy;              // most group members one CTA of the copy kernel writes
+  void *plan_ws;             // batch workspace: patched layers take the persistent kernel
   SmemPlan smem;
   unsigned *status;
   FreqQ64 freq;
@@ -541,6 +543,13 @@ bool fast_layout(const DevLayout &l);                               // kamera_re
 bool inplace_layout(const DevLayout &l);
 SmemPlan reuse_tile_plan(const DevLayout &l, int max_m, int max_run);
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
+// The persistent path of patched layers (kamera_reuse_tile.cu): workspace bytes for batches of
+// up to n_items items, its plan (fast == 0 when the layout, rank or run does not fit it), and
+// the launch of the planning and persistent kernels on `s` (a.plan_ws set).
+size_t persist_workspace_bytes(const DevLayout &l, long long n_items);
+SmemPlan reuse_persist_plan(const DevLayout &l, int max_m, int run);
+bool persist_batch_ok(const DevLayout &l, const SmemPlan &p, int n_items, int max_tokens);
+cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
 cudaError_t launch_reanchor(const AnchorArgs &a, cudaStream_t s);   // kamera_anchor.cu

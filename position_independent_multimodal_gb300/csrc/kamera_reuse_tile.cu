@@ -685,4 +685,692 @@ cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------
+// Persistent path of the patched layers (kamera_batch_reuse with a batch workspace; GQA/MHA
+// layouts, whose column tiles all have one width and one group rule per channel).
+//
+// The grid kernel above pays per task a prologue (group search, TMEM and barriers, phase
+// table, V_m^T, the first two tiles' loads and their latency) and ends in a tail as long as a
+// task; in a batch of shared chunks most of its CTAs only search their group and exit. Here a
+// planning kernel (one CTA) forms the groups once and lists the task rows: (top-first patched
+// layer, channel, the first item of a run), each covering every column tile of its rows. The
+// persistent CTAs come in sets of `ntile`, one per column tile; a set takes a contiguous range
+// of the rows' token tiles (ranges of equal weight, a token tile of a run of r members
+// weighing 32 + 5 r, within one tile of equal), and its CTAs walk the same tiles side by side,
+// so the column pieces of each pool row are written together as in the grid kernel. Each CTA
+// walks its range with the grid kernel's two-stage pipeline, carried across task boundaries:
+// the next task's first tiles and its V_m^T (two buffers, by task parity) are loaded while the
+// previous task's last tiles are finished, and TMEM and the barriers are set up once. Each
+// tile's bytes are those of the grid kernel.
+// ---------------------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kRunCapP = 4;           // most group members of one task
+constexpr int kRecSlots = 32;         // task records held in shared memory
+constexpr int kRecFetch = 16;         // task records fetched at a time
+constexpr int kMaxPersistCtas = 1024;
+constexpr int kPlanThreads = 1024;
+constexpr int kMaxPlanItems = 2048;
+constexpr int kMaxPlanRows = 16384;   // task rows of one batch
+
+struct PlanRow {   // 16 bytes in the workspace
+  int item;        // the run's first item
+  int code;        // layer << 16 | channel << 8
+  int ntt_nmem;    // token tiles << 8 | members of the run
+  int mem;         // index of the run's member list
+};
+
+// One task (a task row at one column tile) in shared memory.
+struct TaskRec {
+  kamera_item it;    // the run's first item
+  int code, nmem;    // layer << 16 | channel << 8 | column tile; members
+  int t_lo, t_hi;    // the token tiles of this task in the CTA's range
+  int req[kRunCapP], start[kRunCapP];  // the members' requests and first tokens
+};
+static_assert(sizeof(kamera_item) == 80, "kamera_item layout");
+static_assert(sizeof(TaskRec) == 128, "task record layout");
+
+// Byte offsets of the batch workspace for n items.
+struct WsLayout {
+  size_t starts;   // int2 [kMaxPersistCtas + 1]: (row, tile) where each set's range begins
+  size_t members;  // int2 [n][2][kRunCapP]: (request, first token) of each run's members
+  size_t rows;     // PlanRow [min(n * L * 2, kMaxPlanRows)]
+  size_t total;
+};
+__host__ __device__ inline WsLayout ws_layout(const DevLayout &l, long long n) {
+  WsLayout w;
+  w.starts = 256;  // the first 256 bytes: int rows, tiles, weight
+  size_t off = w.starts + 8 * (size_t)(kMaxPersistCtas + 1);
+  off = (off + 255) & ~(size_t)255;
+  w.members = off;
+  off += (size_t)n * 2 * kRunCapP * 8;
+  off = (off + 255) & ~(size_t)255;
+  w.rows = off;
+  long long rows = n * l.L * 2;
+  if (rows > kMaxPlanRows) rows = kMaxPlanRows;
+  off += (size_t)rows * sizeof(PlanRow);
+  w.total = (off + 255) & ~(size_t)255;
+  return w;
+}
+
+// Whether item o joins item me's group on channel ch (channel 0 turns: the same offsets as
+// well): the grid kernel's group rule for GQA column tiles.
+__device__ __forceinline__ bool same_group(const kamera_item &me, const kamera_item &o, int ch,
+                                           const DevLayout &lay) {
+  return (ch == 0 ? o.canon_k == me.canon_k : o.canon_v == me.canon_v) &&
+         o.num_tokens == me.num_tokens && o.patch_u == me.patch_u &&
+         o.patch_vt == me.patch_vt && o.patch_m == me.patch_m && o.patch_l0 == me.patch_l0 &&
+         o.patch_l1 == me.patch_l1 && (ch != 0 || same_offsets(o, me, lay));
+}
+
+// Shared memory of the planning kernel: the items, their lengths and layers, run sizes, the
+// weight prefix of the task rows and the scan.
+size_t plan_smem_bytes(int n) {
+  return 96 * (size_t)n + (((size_t)n * 2 + 15) & ~(size_t)15) + 4 * (size_t)(kMaxPlanRows + 1) +
+         4 * 32 * 4;
+}
+
+// One CTA of kPlanThreads: the groups, the task rows and the range of each of Q sets of CTAs,
+// into the workspace a.plan_ws. Rows past kMaxPlanRows are not planned (the host sizes batches
+// below it).
+__global__ void __launch_bounds__(kPlanThreads) reuse_plan_kernel(const __grid_constant__ ReuseArgs a,
+                                                                  int Q) {
+  extern __shared__ __align__(16) unsigned char psm[];
+  const DevLayout &lay = a.lay;
+  const int n = a.n_items, tid = threadIdx.x, run = a.smem.run;
+  const int warp = tid >> 5, lane = tid & 31;
+  unsigned char *ws = static_cast<unsigned char *>(a.plan_ws);
+  const WsLayout W = ws_layout(lay, n);
+  int *head = reinterpret_cast<int *>(ws);
+  int2 *starts = reinterpret_cast<int2 *>(ws + W.starts);
+  int2 *members = reinterpret_cast<int2 *>(ws + W.members);
+  PlanRow *rows = reinterpret_cast<PlanRow *>(ws + W.rows);
+  kamera_item *items = reinterpret_cast<kamera_item *>(psm);  // the batch, staged once
+  int4 *info = reinterpret_cast<int4 *>(psm + 80 * n);  // (tokens, or -1 when skipped; m, l0, l1)
+  signed char *nm = reinterpret_cast<signed char *>(psm + 96 * n);  // run size per (item, ch)
+  int *wpre = reinterpret_cast<int *>(psm + 96 * n + ((2 * n + 15) & ~15));  // weight prefix
+  int *scan = wpre + kMaxPlanRows + 1;  // [4][32]
+  {  // 16-byte words (the item array is 16-byte aligned and 80 bytes an item)
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.items);
+    uint4 *dst = reinterpret_cast<uint4 *>(items);
+    for (int q = tid; q < 5 * n; q += kPlanThreads) dst[q] = src[q];
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kPlanThreads) {
+    const kamera_item &it = items[i];
+    const bool ok = item_check(it, lay, a.pool, a.max_tokens, a.max_m) == 0 &&
+                    it.num_tokens > 0 && it.patch_m > 0 && it.patch_l1 > it.patch_l0;
+    info[i] = make_int4(ok ? it.num_tokens : -1, it.patch_m, it.patch_l0, it.patch_l1);
+  }
+  __syncthreads();
+  // runs, one warp per (item, channel): the members of the item's group in its aligned block,
+  // in item order, taken `run` at a time; the first item of each run leads it
+  for (int j = warp; j < 2 * n; j += kPlanThreads / 32) {
+    const int i = j >> 1, ch = j & 1;
+    int nmem = 0;
+    if (info[i].x > 0) {
+      const kamera_item &me = items[i];
+      const int b0 = i & ~(kShareBlock - 1), o = b0 + lane;
+      const bool mem = o == i || (run > 1 && o < n && info[o].x > 0 &&
+                                  same_group(me, items[o], ch, lay));
+      const unsigned mask = __ballot_sync(0xffffffffu, mem);
+      const int f_self = __popc(mask & ((1u << (i - b0)) - 1u));
+      if (f_self % run == 0) {
+        nmem = min(run, __popc(mask) - f_self);
+        const int f = __popc(mask & ((1u << lane) - 1u)) - f_self;
+        if (mem && f >= 0 && f < nmem)
+          members[j * kRunCapP + f] = make_int2(items[o].req, items[o].start_tok);
+      }
+    }
+    if (lane == 0) nm[j] = static_cast<signed char>(nmem);
+  }
+  __syncthreads();
+  // task rows: candidates (top-first layer, channel, item), each thread a contiguous share
+  const int R = lay.L * 2 * n;
+  const int per = (R + kPlanThreads - 1) / kPlanThreads;
+  const int r0 = min(R, tid * per), r1 = min(R, r0 + per);
+  auto task_row = [&](int rr, int *i, int *layer, int *ch) {
+    const int z = rr / n;
+    *i = rr - z * n;
+    *layer = lay.L - 1 - (z >> 1);
+    *ch = z & 1;
+    const int4 in = info[*i];
+    return in.x > 0 && *layer >= in.z && *layer < in.w && nm[(*i << 1) | *ch] > 0;
+  };
+  int cnt = 0, wsum = 0, tsum = 0;
+  for (int rr = r0; rr < r1; ++rr) {
+    int i, layer, ch;
+    if (task_row(rr, &i, &layer, &ch)) {
+      const int ntt = (info[i].x + kTileRows - 1) / kTileRows;
+      ++cnt;
+      tsum += ntt;
+      wsum += ntt * (32 + 5 * nm[(i << 1) | ch]);
+    }
+  }
+  int v0 = cnt, v1 = wsum, v2 = tsum;  // inclusive scans, warp then block
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int x0 = __shfl_up_sync(0xffffffffu, v0, d), x1 = __shfl_up_sync(0xffffffffu, v1, d),
+              x2 = __shfl_up_sync(0xffffffffu, v2, d);
+    if (lane >= d) {
+      v0 += x0;
+      v1 += x1;
+      v2 += x2;
+    }
+  }
+  if (lane == 31) {
+    scan[warp] = v0;
+    scan[32 + warp] = v1;
+    scan[64 + warp] = v2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      int x = scan[32 * c + lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int px = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += px;
+      }
+      scan[32 * c + lane] = x;
+    }
+  }
+  __syncthreads();
+  const int NR = min(scan[31], kMaxPlanRows), WT = scan[63], NT = scan[95];
+  int k = (warp > 0 ? scan[warp - 1] : 0) + v0 - cnt;
+  int wp = (warp > 0 ? scan[32 + warp - 1] : 0) + v1 - wsum;
+  for (int rr = r0; rr < r1 && k < NR; ++rr) {
+    int i, layer, ch;
+    if (task_row(rr, &i, &layer, &ch)) {
+      const int ntt = (info[i].x + kTileRows - 1) / kTileRows, j = (i << 1) | ch;
+      rows[k] = PlanRow{i, (layer << 16) | (ch << 8), (ntt << 8) | nm[j], j};
+      wpre[k] = wp;
+      wp += ntt * (32 + 5 * nm[j]);
+      ++k;
+    }
+  }
+  if (tid == 0) wpre[NR] = WT;
+  __syncthreads();
+  // set q begins at the first row tile whose weight prefix is at least floor(q * WT / Q)
+  for (int q = tid; q <= Q; q += kPlanThreads) {
+    const int target = (int)((long long)q * WT / Q);
+    int lo = 0, hi = NR;  // the first row r with wpre[r + 1] > target
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (wpre[mid + 1] > target)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    int2 st = make_int2(NR, 0);
+    if (lo < NR && q < Q) {
+      const int nn = rows[lo].ntt_nmem, w = 32 + 5 * (nn & 0xff);
+      const int d = target - wpre[lo], t = d <= 0 ? 0 : (d + w - 1) / w;
+      st = t < (nn >> 8) ? make_int2(lo, t) : make_int2(lo + 1, 0);
+    }
+    starts[q] = st;
+  }
+  if (tid == 0) {
+    head[0] = NR;
+    head[1] = NT * lay.ntile;
+    head[2] = WT;
+  }
+}
+
+// What the loops need of a task record.
+struct TaskV {
+  int layer, ch, nmem, T, m, ntt, row, li, tensor;
+  Tile tile;
+};
+__device__ __forceinline__ TaskV task_v(const TaskRec &r, const DevLayout &lay, int engine) {
+  TaskV v;
+  v.layer = r.code >> 16;
+  v.ch = (r.code >> 8) & 0xff;
+  v.nmem = r.nmem;
+  v.T = r.it.num_tokens;
+  v.m = r.it.patch_m;
+  v.ntt = (v.T + kTileRows - 1) / kTileRows;
+  v.row = v.ch == 0 ? lay.row_k : lay.row_v;
+  v.li = v.layer - r.it.patch_l0;
+  v.tile = tile_of(lay, v.ch, r.code & 0xff, v.ch == 0 && item_rotates(r.it, lay));
+  v.tensor = engine == kEngineTensor && (v.m & 7) == 0 && aligned16(r.it.patch_u);
+  return v;
+}
+
+__global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_constant__ ReuseArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t s0 = (raw + 1023u) & ~1023u;  // the swizzle atoms need 1024-byte alignment
+  unsigned char *sp = smem_raw + (s0 - raw);
+  const SmemPlan &P = a.smem;
+  const DevLayout &lay = a.lay;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned char *ws = static_cast<const unsigned char *>(a.plan_ws);
+  const WsLayout W = ws_layout(lay, a.n_items);
+  const int2 *starts = reinterpret_cast<const int2 *>(ws + W.starts);
+  const int2 *memtab = reinterpret_cast<const int2 *>(ws + W.members);
+  const PlanRow *prow = reinterpret_cast<const PlanRow *>(ws + W.rows);
+  // this CTA: column tile c of set q, whose range runs from token tile b.y of task row b.x to
+  // token tile e.y of task row e.x (exclusive)
+  const int nt = lay.ntile, q = blockIdx.x / nt, c = blockIdx.x - q * nt;
+  const int2 b = starts[q], e = starts[q + 1];
+  if (b.x == e.x && b.y == e.y) return;  // an empty range
+  const int n_local = e.x - b.x + (e.y > 0 ? 1 : 0);  // tasks of the range, in order
+  TaskRec *rec = reinterpret_cast<TaskRec *>(sp + P.recs);
+  // records of the range's tasks [j0, j1) into their slots, one thread per task
+  auto fetch = [&](int j0, int j1) {
+    for (int j = j0 + tid; j < j1; j += kThrT) {
+      const int row = b.x + j;
+      const PlanRow pr = prow[row];
+      TaskRec &r = rec[j % kRecSlots];
+      r.it = a.items[pr.item];
+      r.code = pr.code | c;
+      r.nmem = pr.ntt_nmem & 0xff;
+      r.t_lo = j == 0 ? b.y : 0;
+      r.t_hi = row == e.x ? e.y : pr.ntt_nmem >> 8;
+      for (int f = 0; f < r.nmem; ++f) {
+        const int2 mm = memtab[pr.mem * kRunCapP + f];
+        r.req[f] = mm.x;
+        r.start[f] = mm.y;
+      }
+    }
+  };
+  int loaded = min(n_local, kRecFetch);
+  fetch(0, loaded);
+
+  const uint32_t x_op = s0 + P.canon, pg_op = s0 + P.pages, slots = s0 + P.slots;
+  const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
+  volatile int *flag = reinterpret_cast<volatile int *>(sp + P.misc + 4);
+  const bool u2 = P.u_bufs == 2;
+  const int ps = lay.page_size;
+  const DivMod psd(ps);
+  const int lc = tid & 7, lr = tid >> 3;  // copies: chunk of an atom row, row of each pass
+  const uint32_t swc = (uint32_t)((lc ^ (lr & 7)) << 4);
+  auto rec_of = [&](int k) -> const TaskRec & { return rec[k % kRecSlots]; };
+  auto u_buf = [&](int g) { return s0 + P.a_op + (u2 ? (g & 1) * P.a_stage : 0); };
+  auto vt_buf = [&](int k) { return s0 + P.b_op + (k & 1) * P.b_stage; };
+  auto rot_of = [&](int k) { return reinterpret_cast<float *>(sp + P.cs + (k & 1) * P.cs_stage); };
+
+  // canonical rows of tile t of task k into stage s, and the page ids of its members' tokens
+  auto issue_x = [&](int k, int t, int s) {
+    const TaskRec &R = rec_of(k);
+    const TaskV v = task_v(R, lay, a.engine);
+    const int t0 = t * kTileRows, rows = min(kTileRows, v.T - t0);
+    const int atoms = v.tile.ncols >> 6;
+    const __nv_bfloat16 *src =
+        static_cast<const __nv_bfloat16 *>(v.ch == 0 ? R.it.canon_k : R.it.canon_v) +
+        ((long long)v.layer * v.T + t0 + lr) * v.row + v.tile.col0 + 8 * lc;
+    const uint32_t dst = x_op + s * P.stage + lr * 128 + swc;
+    const long long step = 32ll * v.row;
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      if (lr + 32 * pr < rows) {
+#pragma unroll
+        for (int at = 0; at < 2; ++at)
+          if (at < atoms)
+            ptx::cp_async16(dst + at * kAtomT + pr * 32 * 128, src + pr * step + at * 64, 16u);
+      }
+    }
+    const int pgs = P.pg_per_member;
+    for (int q = tid; q < v.nmem * pgs; q += kThrT) {
+      const int f = q / pgs, kk = q - f * pgs;
+      int p_first, off0, npages, dummy;
+      psd.split(R.start[f] + t0, &p_first, &off0);
+      psd.split(off0 + rows - 1, &npages, &dummy);
+      if (kk <= npages)
+        ptx::cp_async4(pg_op + s * P.pages_stage + 4 * q,
+                       a.pool.pt + (long long)R.req[f] * a.pool.pt_stride + p_first + kk);
+    }
+  };
+  // U rows of tile t of task k as the A operand in buffer ub; rank padding zeroed
+  auto issue_u = [&](int k, int t, uint32_t ub) {
+    const TaskRec &R = rec_of(k);
+    const TaskV v = task_v(R, lay, a.engine);
+    const int t0 = t * kTileRows, rows = min(kTileRows, v.T - t0);
+    const int m = v.m, m8 = m >> 3, Kp = (m + 15) & ~15;
+    const __nv_bfloat16 *Ut = static_cast<const __nv_bfloat16 *>(R.it.patch_u) +
+                              ((long long)(v.li * 2 + v.tile.group) * v.T + t0) * m;
+    if (v.tensor) {
+      const DivMod md(m8);
+      for (int q = tid; q < rows * m8; q += kThrT) {
+        int rr, kc;
+        md.split(q, &rr, &kc);
+        ptx::cp_async16(ub + ((kc * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4),
+                        Ut + (long long)rr * m + kc * 8, 16u);
+      }
+      for (int q = tid; q < kTileRows * ((Kp >> 3) - m8); q += kThrT) {
+        const int kc = m8 + (q >> 7), rr = q & 127;
+        sts16(ub + ((kc * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4), make_uint4(0u, 0u, 0u, 0u));
+      }
+    } else {
+      for (int q = tid; q < kTileRows * Kp; q += kThrT) {
+        const int rr = q / Kp, kk = q - rr * Kp;
+        const uint32_t val = (rr < rows && kk < m) ? ldg_u16(Ut + (long long)rr * m + kk) : 0u;
+        sts_u16(ub + (((kk >> 3) * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4) + ((kk & 7) << 1), val);
+      }
+    }
+  };
+  // a new task: its phase table (plain stores) and V_m^T (copies) in the task-parity buffers
+  auto prepare = [&](int k) {
+    const TaskRec &R = rec_of(k);
+    const TaskV v = task_v(R, lay, a.engine);
+    if (v.tile.band > 0) {
+      float *rot = rot_of(k);
+      for (int i = tid; i < lay.npairs; i += kThrT) {
+        const float2 c = rope_phase(a.freq.q[i], pair_delta(R.it, lay, i));
+        rot[i] = c.x;
+        rot[lay.npairs + i] = c.y;
+        rot[2 * lay.npairs + i] = -c.y;
+      }
+    }
+    const int m = v.m, Kp = (m + 15) & ~15, ncore = v.tile.ncols >> 3;
+    const int wg = v.tile.group == 0 ? lay.w0 : lay.w1;
+    const __nv_bfloat16 *vt = static_cast<const __nv_bfloat16 *>(R.it.patch_vt) +
+                              (long long)v.li * m * (lay.w0 + lay.w1) +
+                              (v.tile.group == 0 ? 0 : (long long)m * lay.w0) + v.tile.gcol0;
+    const uint32_t vb = vt_buf(k);
+    for (int q = tid; q < Kp * ncore; q += kThrT) {
+      const int kk = q / ncore, j = q - kk * ncore;
+      const bool ok = kk < m;
+      ptx::cp_async16(vb + ((kk >> 3) * ncore + j) * 128 + (kk & 7) * 16,
+                      ok ? (const void *)(vt + (long long)kk * wg + 8 * j) : (const void *)vt,
+                      ok ? 16u : 0u);
+    }
+  };
+  uint32_t tmem = 0;
+  // MMA of tile g (task k) into accumulator g & 1 (one thread); arrives on barrier g & 1
+  auto issue_mma = [&](int k, int g) {
+    const TaskRec &R = rec_of(k);
+    const TaskV v = task_v(R, lay, a.engine);
+    const int Kp = (v.m + 15) & ~15, ncore = v.tile.ncols >> 3;
+    ptx::tc_fence_after();
+    const uint32_t ub = u_buf(g), vb = vt_buf(k), d = tmem + (g & 1) * P.acc_cols;
+    const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, v.tile.ncols) | (1u << 16);
+    for (int ks = 0; ks < Kp / 16; ++ks)
+      ptx::mma_bf16(d, ptx::smem_desc(ub + ks * 2 * 2048, 2048, 128),
+                    ptx::smem_desc(vb + ks * 2 * ncore * 128, ncore * 128, 128), idesc,
+                    ks > 0 ? 1u : 0u);
+    ptx::mma_commit(s_bar + 8 * (g & 1));
+  };
+  auto at_end = [&](int j, int) { return j == n_local; };
+  auto next = [&](int &j, int &t) {
+    if (++t == rec_of(j).t_hi) {
+      ++j;
+      t = 0;
+    }
+  };
+
+  if (warp == 0) {
+    ptx::tmem_alloc(s_tmem, P.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    ptx::mbar_init(s_bar, 1);
+    ptx::mbar_init(s_bar + 8, 1);
+    ptx::fence_mbar_init();
+    *flag = 0;
+  }
+  __syncthreads();  // task records visible
+  int ck = 0, ctl = b.y;  // the tile being finished (local task, token tile)
+  int lk = 0, lt = b.y;   // the next tile to load
+  prepare(lk);
+  issue_x(lk, lt, 0);
+  issue_u(lk, lt, u_buf(0));
+  ptx::cp_async_commit();
+  next(lk, lt);
+  if (!at_end(lk, lt)) {
+    if (lt == 0) prepare(lk);
+    issue_x(lk, lt, 1);
+    if (u2) issue_u(lk, lt, u_buf(1));
+    next(lk, lt);
+  }
+  ptx::cp_async_commit();
+  ptx::cp_async_wait_group1();  // tile 0, its U and V_m^T
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();  // TMEM address, barriers, tables, tile 0 visible
+  ptx::tc_fence_after();
+  tmem = *reinterpret_cast<volatile uint32_t *>(sp + P.misc);
+  bool timed_out = false;
+  uint32_t ph = 0;  // parity of each MMA barrier's next phase
+  if (tid == 0 && task_v(rec_of(ck), lay, a.engine).tensor) issue_mma(ck, 0);
+  const int r = ((warp & 3) << 5) + lane;  // epilogue row (TMEM lane)
+  const int half = warp >> 2;
+  const uint32_t trow0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const unsigned long long pool_k =
+      static_cast<unsigned long long>(__cvta_generic_to_global(a.pool.k));
+  const unsigned long long pool_v =
+      a.pool.v ? static_cast<unsigned long long>(__cvta_generic_to_global(a.pool.v)) : 0ull;
+
+  for (int g = 0; !at_end(ck, ctl); ++g) {
+    const int s = g & 1;
+    const TaskRec &R = rec_of(ck);
+    const TaskV v = task_v(R, lay, a.engine);
+    const int t0 = ctl * kTileRows, rows = min(kTileRows, v.T - t0);
+    int nk = ck, nt = ctl;
+    next(nk, nt);
+    const bool has_next = !at_end(nk, nt);
+    const bool use_tc = v.tensor && !timed_out;
+    if (use_tc) {  // warp 0 waits for MMA(g); the other warps sleep at the barrier
+      if (warp == 0) {
+        const bool ok = ptx::mbar_wait(s_bar + 8 * s, (ph >> s) & 1u, kWaitNsT);
+        if (lane == 0 && !ok) *flag = 1;
+      }
+      ph ^= 1u << s;
+      ptx::tc_fence_before();
+    }
+    __syncthreads();
+    if (use_tc) {
+      ptx::tc_fence_after();
+      if (*flag) {
+        timed_out = true;
+        if (tid == 0) atomicOr(a.status, KAMERA_DEVICE_TIMEOUT);
+      }
+    }
+    // one U buffer: MMA(g) has read it, so U of the next tile may land now
+    if (!u2 && v.tensor && has_next) {
+      issue_u(nk, nt, u_buf(g + 1));
+      ptx::cp_async_commit();
+    }
+    const bool write = !(v.tensor && timed_out);
+    const uint32_t xs = x_op + s * P.stage;
+    if (write) {
+      const uint32_t trow = trow0 + s * P.acc_cols;
+      const float *rot = rot_of(ck);
+      if (use_tc) {
+        if (v.tile.ncols == 128) {
+          if (v.tile.band == 0)
+            epi_add<128>(xs, r, half, trow);
+          else if (v.tile.band == 128)
+            epi_rot<128, 128>(xs, r, half, trow, rot, lay.npairs);
+          else
+            epi_rot<128, 64>(xs, r, half, trow, rot, lay.npairs);
+        } else {
+          if (v.tile.band == 0)
+            epi_add<64>(xs, r, half, trow);
+          else
+            epi_rot<64, 64>(xs, r, half, trow, rot, lay.npairs);
+        }
+      } else if (!v.tensor && r < rows) {
+        epi_fma(xs, r, half, v.tile.ncols, v.tile.band, u_buf(g), vt_buf(ck), v.m, rot,
+                lay.npairs);
+      }
+    }
+    if (r < rows)  // the row's two owners find its slot in each member (alternating)
+      for (int f = half; f < v.nmem; f += 2) {
+        int pg, in_page, p_first, off0;
+        const int st = R.start[f];
+        psd.split(st + t0 + r, &pg, &in_page);
+        psd.split(st + t0, &p_first, &off0);
+        const int page = lds_i32t(pg_op + s * P.pages_stage +
+                                  4 * (f * P.pg_per_member + pg - p_first));
+        int slot = -1;
+        if (page >= 0 && (long long)(page + 1) * ps <= a.pool.num_slots)
+          slot = page * ps + in_page;
+        else
+          atomicOr(a.status, KAMERA_DEVICE_SLOT_OOB);
+        sts_i32t(slots + 4 * (f * kTileRows + r), slot);
+      }
+    // the CUDA-core path with one U buffer reads U(g) in the epilogue: U of the next tile after
+    if (!u2 && !v.tensor && has_next) {
+      __syncthreads();
+      issue_u(nk, nt, u_buf(g + 1));
+      ptx::cp_async_commit();
+    }
+    ptx::cp_async_wait_all();  // the next tile's rows, pages, U and V_m^T
+    ptx::fence_proxy_async_smem();
+    if (use_tc) ptx::tc_fence_before();
+    __syncthreads();  // rows of tile g complete, the next tile staged
+    if (has_next && !timed_out && tid == 0 && task_v(rec_of(nk), lay, a.engine).tensor)
+      issue_mma(nk, g + 1);
+    if (write) {  // 4 rows x 128 bytes per warp instruction, once per member
+      const uint32_t src = xs + lr * 128 + swc;
+      const int atoms = v.tile.ncols >> 6;
+      const unsigned long long out_base =
+          (v.ch == 0 ? pool_k : pool_v) +
+          2ull * ((unsigned long long)v.layer * (unsigned long long)a.pool.num_slots * v.row +
+                  v.tile.col0);
+      for (int f = 0; f < v.nmem; ++f) {
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          const int rr = lr + 32 * pr;
+          if (rr < rows) {
+            const int slot = lds_i32t(slots + 4 * (f * kTileRows + rr));
+            if (slot >= 0) {
+              const unsigned long long dst = out_base + (unsigned long long)slot * (2ull * v.row);
+#pragma unroll
+              for (int at = 0; at < 2; ++at)
+                if (at < atoms)
+                  stg16_global(reinterpret_cast<void *>(dst + 128ull * at + 16ull * lc),
+                               lds16(src + at * kAtomT + pr * 32 * 128));
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // stage s is free
+    if (!at_end(lk, lt)) {  // the tile after the next one
+      if (lt == 0) {        // starts a task
+        if (lk >= loaded) {
+          const int k1 = min(n_local, lk + kRecFetch);
+          fetch(lk, k1);
+          loaded = k1;
+          __syncthreads();
+        }
+        prepare(lk);
+      }
+      issue_x(lk, lt, s);
+      if (u2) issue_u(lk, lt, u_buf(g));
+      next(lk, lt);
+    }
+    ptx::cp_async_commit();
+    ck = nk;
+    ctl = nt;
+  }
+  ptx::cp_async_wait_all();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, P.tmem_cols);
+}
+
+// Offsets of the persistent kernel's shared memory: the tile kernel's stages and U buffers,
+// two V_m^T buffers and two phase tables (by task parity), and the task records.
+SmemPlan persist_plan_with(const DevLayout &l, int max_m, int run, int u_bufs) {
+  SmemPlan p{};
+  int widest = l.tw;
+  if (l.kind == KAMERA_MLA && l.rope_d > widest) widest = l.rope_d;
+  const int kp = max_m > 0 ? ((max_m + 15) & ~15) : 16;
+  p.fast = 1;
+  p.run = run;
+  p.u_bufs = u_bufs;
+  p.pitch = widest * 2;
+  p.stage = kTileRows * widest * 2;
+  p.a_stage = align128t(kTileRows * kp * 2);
+  p.b_stage = align128t(widest * kp * 2);
+  p.cs_stage = align128t(l.npairs * 12);
+  p.pg_per_member = kTileRows / l.page_size + 2;
+  p.pages_stage = align128t(run * p.pg_per_member * 4);
+  int off = 0;
+  p.canon = off;
+  off += 2 * p.stage;
+  p.b_op = off;
+  off += 2 * p.b_stage;
+  p.a_op = off;
+  off += u_bufs * p.a_stage;
+  p.cs = off;
+  off += 2 * p.cs_stage;
+  p.pages = off;
+  off += 2 * p.pages_stage;
+  p.slots = off;
+  off += align128t(run * kTileRows * 4);
+  p.recs = off;
+  off += kRecSlots * (int)sizeof(TaskRec);
+  p.misc = off;  // TMEM address, timeout flag, two MMA barriers
+  off += 128;
+  p.total = off + 1024;
+  int cols = 32;
+  while (cols < widest) cols <<= 1;
+  p.acc_cols = cols;
+  p.tmem_cols = 2 * cols;
+  return p;
+}
+
+}  // namespace
+
+size_t persist_workspace_bytes(const DevLayout &l, long long n_items) {
+  return ws_layout(l, n_items < 0 ? 0 : n_items).total;
+}
+
+SmemPlan reuse_persist_plan(const DevLayout &l, int max_m, int run) {
+  SmemPlan p{};
+  if (!fast_layout(l) || run < 1 || run > kRunCapP) return p;
+  p = persist_plan_with(l, max_m, run, 2);
+  if (tile_ctas(p) < 2) p = persist_plan_with(l, max_m, run, 1);
+  if (tile_ctas(p) < 2) p.fast = 0;
+  return p;
+}
+
+bool persist_batch_ok(const DevLayout &l, const SmemPlan &p, int n_items, int max_tokens) {
+  const long long rows = (long long)n_items * l.L * 2;
+  const long long ntt = ((long long)max_tokens + kTileRows - 1) / kTileRows;
+  return p.fast && l.kind == KAMERA_GQA && n_items >= 1 && n_items <= kMaxPlanItems &&
+         rows <= kMaxPlanRows && rows * ntt * (32 + 5 * kRunCapP) < (1ll << 31) &&
+         l.ntile <= kMaxPersistCtas && plan_smem_bytes(n_items) <= 227 * 1024;
+}
+
+cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s) {
+  static int configured[2][64] = {{0}};
+  static int sm_count[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!sm_count[dev]) {
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int plan_smem = (int)plan_smem_bytes(a.n_items);
+  if (plan_smem > configured[0][dev] && plan_smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(reuse_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             plan_smem);
+    if (e != cudaSuccess) return e;
+    configured[0][dev] = plan_smem;
+  }
+  if (a.smem.total > configured[1][dev] && a.smem.total > 48 * 1024) {
+    e = cudaFuncSetAttribute(reuse_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             a.smem.total);
+    if (e != cudaSuccess) return e;
+    configured[1][dev] = a.smem.total;
+  }
+  // sets of ntile CTAs (one per column tile), as many as fill two CTAs per SM
+  const int Q = max(1, min(kMaxPersistCtas, tile_ctas(a.smem) * sm_count[dev]) / a.lay.ntile);
+  reuse_plan_kernel<<<1, kPlanThreads, plan_smem, s>>>(a, Q);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  reuse_persist_kernel<<<Q * a.lay.ntile, kThrT, a.smem.total, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace kamera

@@ -367,3 +367,40 @@ def test_set_option_checks_its_arguments():
         assert e.value.status == km.KAMERA_ERR_INVALID_ARG
     assert km.lib().kamera_set_option(None, km.KAMERA_OPT_PATCH_ENGINE, 0) == \
         km.KAMERA_ERR_INVALID_ARG
+
+
+class _WsFake:
+    """A device buffer's address and size; kamera_set_batch_workspace only stores them."""
+
+    def __init__(self, addr, nbytes):
+        self.addr, self.nbytes = addr, nbytes
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+def test_batch_workspace_size_and_setter(lib):
+    lay = gqa()
+    h = km.create(lay)
+    sizes = [km.kamera_batch_workspace_bytes(h, n) for n in (0, 1, 18, 1000)]
+    assert all(s % 256 == 0 for s in sizes) and sizes == sorted(sizes)
+    per_task = 16
+    c = km.make_layout(lay)
+    assert sizes[3] >= 1000 * c.num_layers * 2 * per_task  # task rows: items x layers x channels
+    assert lib.kamera_batch_workspace_bytes(None, 5) == 0
+    assert km.kamera_batch_workspace_bytes(h, -1) == 0
+    need = km.kamera_batch_workspace_bytes(h, 1)
+    for bad in (_WsFake(0x100010, need), _WsFake(0x100000, need - 256)):
+        with pytest.raises(km.KameraError) as e:
+            km.kamera_set_batch_workspace(h, bad)
+        assert e.value.status == km.KAMERA_ERR_INVALID_ARG
+    assert lib.kamera_set_batch_workspace(h.ptr, None, 64) == km.KAMERA_ERR_INVALID_ARG
+    assert lib.kamera_set_batch_workspace(None, None, 0) == km.KAMERA_ERR_INVALID_ARG
+    km.kamera_set_batch_workspace(h, _WsFake(0x100000, need))
+    km.kamera_set_batch_workspace(h, None)

@@ -1,0 +1,199 @@
+"""The persistent path of the patched layers: a handle with a batch workspace plans a GQA/MHA
+batch on the device (groups, task rows, one range of token tiles per set of CTAs) and runs the
+patched layers as a persistent kernel. Every byte it writes must equal what the grid path (the
+same handle without a workspace) writes, and the rows must match the float64 oracle of Eq. 1
+(Kamera §5 "Reorder": one orbit patch serves every ordering of a chunk).
+
+Each case also reads the plan's header (task rows and tiles) back from the workspace, so a
+silent fall-back to the grid path cannot pass for the persistent one, and the cases that must
+fall back (MLA, runs above 4) check that the header was left alone.
+
+Cases: the six orderings of three ragged chunks (GQA with 64- and 128-column tiles; MLA falls
+back) at ranks 8 and 32 and a CUDA-core rank 12; run sizes 1 to 4 (6 falls back); M-RoPE
+items that share δ but not δ_h; an invalid item ahead of its group and an out-of-range page;
+one batch mixing ranks, lengths and unpatched items; and a batch of many one-tile task rows,
+more per CTA than the kernel keeps in shared memory at once.
+"""
+import dataclasses
+import itertools
+
+import pytest
+import torch
+
+import position_independent_multimodal_gb300 as km
+import workloads as wl
+from tests import kamera_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(cuda_ok):
+    return cuda_ok
+
+
+def gqa(L=3, H=2, hd=64):
+    return wl.Layout(kind=wl.GQA, num_layers=L, page_size=16, num_kv_heads=H, head_dim=hd,
+                     rope_dim=hd, rope_style=wl.NEOX_HALF, rope_theta=1e4)
+
+
+def mla(L=3):
+    return wl.Layout(kind=wl.MLA, num_layers=L, page_size=16, latent_dim=512, rope_dim=64,
+                     rope_style=wl.NEOX_HALF, rope_theta=1e4)
+
+
+def orderings(layout, m, name, Ts=(130, 256, 77), prefix=5):
+    placements = []
+    for r, perm in enumerate(itertools.permutations(range(3))):
+        s = prefix
+        for c in perm:
+            placements.append((c, r, s, s))
+            s += Ts[c]
+    return wl.reuse_workload(name, layout, n_chunks=3, T=list(Ts), placements=placements, m=m,
+                             l0=1, l1=layout.num_layers, seed=3, strong=True, extra_pages=2)
+
+
+def run(w, items, workspace, options=None):
+    """kamera_batch_reuse of the items; with `workspace`, through a batch workspace whose
+    header is returned as (tasks, tiles), else (None, None)."""
+    h = km.create(w.layout, **(options or {}))
+    ws = None
+    if workspace:
+        ws = torch.full((km.kamera_batch_workspace_bytes(h, len(items)),), 0xFF,
+                        dtype=torch.uint8, device="cuda")
+        km.kamera_set_batch_workspace(h, ws)
+    k, v, status, _ = tl.run_batch(h, w.layout, items, w.page_table, w.num_slots)
+    head = (None, None)
+    if ws is not None:
+        hv = ws[:8].view(torch.int32).cpu().tolist()
+        head = (hv[0], hv[1])
+    return k, v, status, head
+
+
+def same_bytes(a, b):
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def compare(w, items=None, options=None, status=0, oracle_items=None, persistent=True):
+    items = items if items is not None else tl.to_device_items(w.items)
+    k, v, st, (n_tasks, n_tiles) = run(w, items, True, options)
+    k0, v0, st0, _ = run(w, items, False, options)
+    assert st == status and st0 == status
+    if persistent:
+        assert n_tasks > 0 and n_tiles >= n_tasks, "the persistent path did not run"
+    else:
+        assert (n_tasks, n_tiles) == (-1, -1), "the persistent path ran"
+    same_bytes(k, k0)
+    if v is not None:
+        same_bytes(v, v0)
+    if oracle_items is not None:
+        tl.check_full(w.layout, oracle_items, w.page_table, k, v)
+    return n_tasks, n_tiles
+
+
+@pytest.mark.parametrize("m", [8, 12, 32])
+@pytest.mark.parametrize("shape", ["gqa64", "gqa128", "mla"])
+def test_orderings_match_the_grid_path_and_the_oracle(shape, m):
+    lay = {"gqa64": gqa(), "gqa128": gqa(H=4, hd=128), "mla": mla()}[shape]
+    w = orderings(lay, m, f"pers{shape}{m}")
+    compare(w, oracle_items=w.items, persistent=shape != "mla")
+
+
+def test_task_and_tile_counts_of_the_plan():
+    # GQA, 2 heads of 128 -> 2 column tiles; layers 1 and 2 patched. K groups: placements with
+    # equal (chunk, offset); V groups: every placement of a chunk; each taken in runs of 3
+    w = orderings(gqa(H=2, hd=128), 32, "perscount")
+
+    def runs_and_tiles(key):
+        groups = {}
+        for it in w.items:
+            groups.setdefault(key(it), []).append(it)
+        runs = sum(-(-len(g) // 3) for g in groups.values())
+        tiles = sum(-(-len(g) // 3) * -(-g[0].num_tokens // 128) for g in groups.values())
+        return runs, tiles
+
+    k_runs, k_tiles = runs_and_tiles(lambda it: (id(it.canon_k), it.delta))
+    v_runs, v_tiles = runs_and_tiles(lambda it: id(it.canon_v))
+    assert (k_runs, v_runs) == (12, 6)
+    n_rows, n_tiles = compare(w)
+    assert n_rows == 2 * (k_runs + v_runs)  # task rows: 2 patched layers
+    assert n_tiles == 2 * 2 * (k_tiles + v_tiles)  # x 2 column tiles
+
+
+@pytest.mark.parametrize("run_patched", [1, 2, 4, 6])
+def test_run_sizes(run_patched):
+    w = orderings(gqa(H=4, hd=128), 16, f"persrun{run_patched}")
+    compare(w, options=dict(share_run_patched=run_patched), persistent=run_patched <= 4,
+            oracle_items=w.items if run_patched == 2 else None)
+
+
+def test_mrope_items_share_delta_but_not_delta_h():
+    lay = dataclasses.replace(gqa(L=2, H=4, hd=128), mrope_section=(16, 24, 24),
+                              mrope_style=wl.MROPE_CONTIGUOUS)
+    w = orderings(lay, 32, "persmrope")
+    w.items = [dataclasses.replace(it, delta_h=(0 if it.req == 0 else it.delta // 7),
+                                   delta_w=-it.delta) for it in w.items]
+    compare(w, oracle_items=w.items)
+
+
+def test_invalid_item_ahead_of_its_group():
+    lay = gqa(L=2, H=4, hd=128)
+    w = wl.reuse_workload("persbad", lay, n_chunks=1, T=150,
+                          placements=[(0, 0, 3, 40), (0, 1, 3, 40), (0, 2, 20, 40)], m=8,
+                          l0=1, l1=2, seed=5, strong=True, extra_pages=1)
+    items = tl.to_device_items(w.items)
+    bad = dataclasses.replace(items[0], req=99)
+    compare(w, items=[bad] + items[1:], status=km.KAMERA_DEVICE_BAD_ITEM,
+            oracle_items=w.items[1:])
+
+
+def test_out_of_range_page_in_one_member():
+    lay = gqa(L=2, H=4, hd=128)
+    w = wl.reuse_workload("persoob", lay, n_chunks=1, T=200,
+                          placements=[(0, 0, 0, 9), (0, 1, 0, 9)], m=32, l0=1, l1=2, seed=6,
+                          strong=True, extra_pages=1)
+    pt = w.page_table.clone()
+    pt[1, 3] = 10 ** 6
+    w = dataclasses.replace(w, page_table=pt)
+    compare(w, status=km.KAMERA_DEVICE_SLOT_OOB)
+
+
+def test_mixed_ranks_lengths_and_unpatched_items():
+    # one batch: ranks 8, 16, 32 (tensor cores) and 12 (CUDA cores), lengths from 1 to 300
+    # tokens, an item without a patch and one with no tokens; the persistent CTAs cross tasks of
+    # different rank, length and engine
+    lay = gqa(L=3, H=2, hd=128)
+    Ts = [300, 1, 127, 128, 129, 64]
+    placements = [(c, c, 3 + 16 * c, 1000 * c - 2500) for c in range(len(Ts))]
+    w = wl.reuse_workload("persmix", lay, n_chunks=len(Ts), T=Ts, placements=placements, m=32,
+                          l0=0, l1=3, seed=8, strong=True, extra_pages=1)
+    ranks = [8, 16, 32, 12, 0, 32]
+    items = []
+    for it, m in zip(w.items, ranks):
+        if m == 0:
+            items.append(dataclasses.replace(it, patch_m=0, patch_u=None, patch_vt=None))
+        else:
+            u = it.patch_u[..., :m].contiguous()
+            W0 = lay.num_kv_heads * lay.head_dim
+            vt = it.patch_vt.view(lay.num_layers, 2, 32, W0)[:, :, :m].contiguous()
+            vt = vt.view(lay.num_layers, -1)
+            items.append(dataclasses.replace(it, patch_m=m, patch_u=u, patch_vt=vt))
+    items.append(dataclasses.replace(items[0], num_tokens=0, req=5))
+    w = dataclasses.replace(w, items=items)
+    compare(w, items=tl.to_device_items(items), oracle_items=items[:-1])
+
+
+def test_many_one_tile_tasks_refetch_their_records():
+    # 1000 short chunks, each in its own request: 1000 x 2 patched layers x 2 channels = 4000
+    # one-tile task rows over two column tiles (4 heads of 64, two per tile); each CTA's range
+    # holds about 26 of them, more than one fetch of records
+    lay = gqa(L=3, H=4, hd=64)
+    n = 1000
+    Ts = [16 + (i * 37) % 100 for i in range(n)]
+    placements = [(i, i, 0, 7 * i - 300) for i in range(n)]
+    w = wl.reuse_workload("persmany", lay, n_chunks=n, T=Ts, placements=placements, m=8, l0=1,
+                          l1=3, seed=9, strong=False, extra_pages=0)
+    n_rows, n_tiles = compare(w)
+    assert n_rows == n * 2 * 2 and n_tiles == 2 * n_rows
+    k, v, _, _ = run(w, tl.to_device_items(w.items), True)
+    tl.check_full(lay, w.items, w.page_table, k, v)
