@@ -95,7 +95,8 @@ def accounting(w, items=None):
                 patch=out["tensor"]["patch"], meta=meta,
                 algorithmic=written + canon + out["tensor"]["patch"] + meta,
                 per_kernel={"reuse_copy_kernel": out["copy"]["algorithmic"],
-                            "reuse_tile_kernel": out["tensor"]["algorithmic"]})
+                            "reuse_tile_kernel": out["tensor"]["algorithmic"],
+                            "reuse_persist_kernel": out["tensor"]["algorithmic"]})
 
 
 def recorded_traffic(kernel: str, workload: str = "gqa_reorder"):
@@ -488,8 +489,11 @@ def kernel_fracs(kern_stats, per_kernel_bytes, peak, traffic_of=None, launches=1
     recorded DRAM traffic per launch; a step of ``launches`` launches carries that many."""
     out = {}
     for name, st in kern_stats.items():
-        kb = per_kernel_bytes[name]
+        kb = per_kernel_bytes.get(name)
         kms = st["median_ms"]
+        if kb is None:  # the planning kernel: timed, its bytes are not counted
+            out[name] = dict(st, ms=kms)
+            continue
         gbs = kb / (kms / 1e3) / 1e9 if kms > 0 else None
         out[name] = dict(st, ms=kms, algorithmic_bytes=kb, achieved_gbs=gbs,
                          frac=gbs / peak if gbs is not None else None)
@@ -500,14 +504,33 @@ def kernel_fracs(kern_stats, per_kernel_bytes, peak, traffic_of=None, launches=1
     return out
 
 
+def planned(h):
+    """Whether the handle's last batch call took the persistent path: its workspace (filled
+    with 0xFF when it was set) then holds a plan header."""
+    import torch
+    ws = getattr(h, "batch_workspace", None)
+    return ws is not None and int(ws[:4].view(torch.int32).item()) >= 0
+
+
+def split_stats(marks_per_pass, persistent):
+    """Per-kernel spreads from event quads (before, between, after planning, after) per call,
+    summed over a pass's calls: the copy kernel, then the planning kernel and the persistent
+    kernel, or the grid tile kernel."""
+    def tot(i, j):
+        return spread([sum(q[i].elapsed_time(q[j]) for q in per) for per in marks_per_pass])
+    if persistent:
+        return {"reuse_copy_kernel": tot(0, 1), "reuse_plan_kernel": tot(1, 2),
+                "reuse_persist_kernel": tot(2, 3)}
+    return {"reuse_copy_kernel": tot(0, 1), "reuse_tile_kernel": tot(1, 3)}
+
+
 def time_split(h, launches, pool, st, runs, flush, stream):
     """``runs`` passes of a reuse step (one kamera_batch_reuse per launch), each after an L2
-    flush, with event marks between every call's two kernels (which then run one after the
-    other). Returns the spread of the per-pass time of each kernel, summed over the launches,
-    and of the whole pass."""
+    flush, with event marks between every call's kernels (which then run one after the
+    other). Returns the spread of the per-pass time of each kernel, summed over the launches."""
     import torch
     import position_independent_multimodal_gb300 as km
-    marks = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in launches]
+    marks = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in launches]
              for _ in range(runs)]
     for per in marks:
         for trio in per:
@@ -523,9 +546,7 @@ def time_split(h, launches, pool, st, runs, flush, stream):
     torch.cuda.synchronize()
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
-    copy = [sum(t[0].elapsed_time(t[1]) for t in per) for per in marks]
-    tile = [sum(t[1].elapsed_time(t[2]) for t in per) for per in marks]
-    return {"reuse_copy_kernel": spread(copy), "reuse_tile_kernel": spread(tile)}
+    return split_stats(marks, planned(h))
 
 
 def time_steps(fn, runs, flush, stream, warmup=1):
@@ -554,7 +575,8 @@ def batch_handle(km, lay, n_items, dev):
     its per-tile grid kernel for batches that do not fit that path)."""
     import torch
     h = km.create(lay)
-    ws = torch.empty(km.kamera_batch_workspace_bytes(h, n_items), dtype=torch.uint8, device=dev)
+    ws = torch.full((km.kamera_batch_workspace_bytes(h, n_items),), 0xFF, dtype=torch.uint8,
+                    device=dev)
     km.kamera_set_batch_workspace(h, ws)
     return h
 
@@ -583,7 +605,7 @@ def kamera_arm(args, rank, world, local_rank):
     flush = L2Flush(dev)
     step_ev = event_pairs(args.steps, stream)
     # three events per split step: before, between and after the call's two kernels
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_split)]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_split)]
     for trio in marks:
         for e in trio:
             e.record(stream)  # creates the event handles
@@ -635,9 +657,9 @@ def kamera_arm(args, rank, world, local_rank):
     clk = clocks.stop()
     step_stats = spread([a.elapsed_time(b) for a, b in step_ev])
     b2b_ms = e0.elapsed_time(e1) / args.steps
-    kern_stats = {"reuse_copy_kernel": spread([t[0].elapsed_time(t[1]) for t in marks]),
-                  "reuse_tile_kernel": spread([t[1].elapsed_time(t[2]) for t in marks])}
-    kern_ms = {k: v["median_ms"] for k, v in kern_stats.items()}
+    persistent = planned(h)
+    kern_stats = split_stats([[q] for q in marks], persistent)
+    kern_ms = {k: v["median_ms"] for k, v in kern_stats.items() if k in acc["per_kernel"]}
     ms = job_time_ms(step_stats["median_ms"], world, dev)
     b2b_ms = job_time_ms(b2b_ms, world, dev)
     if int(status.item()) != 0:
@@ -692,11 +714,15 @@ def kamera_arm(args, rank, world, local_rank):
                      "peak_source": (f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                                      else "fallback 6.8 TB/s")},
         "kernels": kernels,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if persistent else 2) * args.steps,
         "kernel_split": (f"per-kernel medians (p10, p90) of {len(marks)} further steps, each "
-                         f"after an L2 flush, with event marks between the two kernels (run one "
-                         f"after the other); the headline step runs them side by side; frac "
-                         f"from the median"),
+                         f"after an L2 flush, with event marks between the kernels (run one "
+                         f"after the other); the headline step runs the copy kernel beside the "
+                         f"patched layers' kernels; frac from the median"
+                         + ("; the patched layers take the planning kernel (one CTA: groups, "
+                            "task rows, CTA ranges; its time is reported, its bytes are not "
+                            "counted) and the persistent kernel, the roofline's kernel"
+                            if persistent else "")),
         "clocks": clk,
     }
     if e2e:

@@ -203,7 +203,7 @@ kamera_status kamera_set_option(kamera_handle *handle, int32_t option, int32_t v
  * either way.
  * Batches that take the persistent path: GQA/MHA layouts whose patched layers run on the
  * tensor-core tile kernel (NeoX-half pairing, column tiles of 64 or 128 whole-head columns),
- * d_items 16-byte aligned, at most 2048 items and num_items x num_layers x 2 <= 16384,
+ * d_items 16-byte aligned, at most 512 items and num_items x num_layers x 2 <= 8192,
  * KAMERA_OPT_SHARE_RUN_PATCHED at most 4, and a rank small enough for two V_m^T buffers and
  * two CTAs per SM in shared memory (max_patch_m <= 48 where a column tile is 128 wide).
  * kamera_batch_workspace_bytes: bytes for batches of up to num_items items (0 for a NULL
@@ -258,16 +258,18 @@ kamera_status kamera_batch_reuse(const kamera_handle *handle, const kamera_item 
                                  kamera_stream_t stream);
 
 /*
- * kamera_batch_reuse with timing marks. The call runs two kernels on the stream: one for the
- * layers without a patch (rotation and copies), then one for the patched layers (tensor-core
- * patch). events[0..2] are CUDA events (cudaEvent_t) recorded before the first kernel,
- * between the two, and after the second; any entry may be NULL. The work done is identical
- * to kamera_batch_reuse.
+ * kamera_batch_reuse with timing marks. The call runs its kernels one after the other on the
+ * stream: the layers without a patch (rotation and copies), then the patched layers (tensor-core
+ * patch; with a batch workspace, the planning kernel and then the persistent kernel).
+ * events[0..3] are CUDA events (cudaEvent_t) recorded before the first kernel, between the
+ * unpatched and the patched layers, after the planning kernel (recorded together with events[1]
+ * when the batch does not take the persistent path), and after the last kernel; any entry may
+ * be NULL. The work done is identical to kamera_batch_reuse.
  */
 kamera_status kamera_batch_reuse_timed(const kamera_handle *handle, const kamera_item *d_items,
                                        int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
                                        const kamera_pool *pool, uint32_t *d_status,
-                                       kamera_stream_t stream, void *const events[3]);
+                                       kamera_stream_t stream, void *const events[4]);
 
 /*
  * Conditioning switched back on in place (App. E "Context management as reversible state

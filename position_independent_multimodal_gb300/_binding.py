@@ -346,9 +346,13 @@ def kamera_rope_phases(handle: Handle, d_deltas: torch.Tensor, d_out: torch.Tens
 def kamera_batch_reuse_timed(handle: Handle, d_items: torch.Tensor, num_items: int,
                              max_tokens: int, max_patch_m: int, pool: Pool, status: torch.Tensor,
                              events, stream=None) -> None:
-    """kamera_batch_reuse recording three torch.cuda.Event objects (or None) before, between
-    and after its two kernels."""
-    arr = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in events])
+    """kamera_batch_reuse recording torch.cuda.Event objects (or None): before its first kernel,
+    between the unpatched and the patched layers, after the planning kernel of the persistent
+    path, and after its last kernel (a list of three leaves out the third)."""
+    ev = list(events)
+    if len(ev) == 3:
+        ev = [ev[0], ev[1], None, ev[2]]
+    arr = (ctypes.c_void_p * 4)(*[None if e is None else e.cuda_event for e in ev])
     p = pool.c()
     _check(lib().kamera_batch_reuse_timed(handle.ptr, _ptr(d_items), int(num_items),
                                           int(max_tokens), int(max_patch_m), ctypes.byref(p),

@@ -175,10 +175,17 @@ SideStream *side_stream() {
 // copy kernel would have nothing to do, so only the patched-layer kernel is launched.
 // Patched layers: the persistent kernel when the batch has a workspace, else the grid kernel
 // on the layouts it serves, else the general pipeline.
-cudaError_t launch_patched(const kamera::ReuseArgs &a, int n_items, cudaStream_t s) {
-  if (!a.smem.fast) return kamera::launch_reuse(a, n_items, s);
-  return a.plan_ws ? kamera::launch_reuse_persist(a, s)
-                   : kamera::launch_reuse_tile(a, n_items, s);
+// `planned` (may be null) is recorded after the planning kernel of the persistent path, or
+// before the patched-layer kernel on the other paths.
+cudaError_t launch_patched(const kamera::ReuseArgs &a, int n_items, cudaStream_t s,
+                           cudaEvent_t planned = nullptr) {
+  if (a.smem.fast && a.plan_ws) return kamera::launch_reuse_persist(a, s, planned);
+  if (planned) {
+    const cudaError_t e = cudaEventRecord(planned, s);
+    if (e != cudaSuccess) return e;
+  }
+  return a.smem.fast ? kamera::launch_reuse_tile(a, n_items, s)
+                     : kamera::launch_reuse(a, n_items, s);
 }
 
 cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, cudaStream_t s,
@@ -390,8 +397,11 @@ kamera_status batch_reuse(const kamera_handle *h, const kamera_item *d_items, in
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = kamera::launch_reuse_copy(a, strm);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess && max_patch_m > 0) e = launch_patched(a, num_items, strm);
-  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess && max_patch_m > 0)
+    e = launch_patched(a, num_items, strm, static_cast<cudaEvent_t>(events[2]));
+  else if (e == cudaSuccess)
+    e = mark(2);
+  if (e == cudaSuccess) e = mark(3);
   return from_cuda(e);
 }
 
@@ -408,7 +418,7 @@ kamera_status kamera_batch_reuse(const kamera_handle *h, const kamera_item *d_it
 kamera_status kamera_batch_reuse_timed(const kamera_handle *h, const kamera_item *d_items,
                                        int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
                                        const kamera_pool *pool, uint32_t *d_status,
-                                       kamera_stream_t stream, void *const events[3]) {
+                                       kamera_stream_t stream, void *const events[4]) {
   return batch_reuse(h, d_items, num_items, max_tokens, max_patch_m, pool, d_status, stream,
                      events);
 }

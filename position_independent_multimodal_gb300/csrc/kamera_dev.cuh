@@ -545,11 +545,13 @@ SmemPlan reuse_tile_plan(const DevLayout &l, int max_m, int max_run);
 cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s);
 // The persistent path of patched layers (kamera_reuse_tile.cu): workspace bytes for batches of
 // up to n_items items, its plan (fast == 0 when the layout, rank or run does not fit it), and
-// the launch of the planning and persistent kernels on `s` (a.plan_ws set).
+// the launch of the planning and persistent kernels on `s` (a.plan_ws set; `planned`, when
+// not null, recorded between them).
 size_t persist_workspace_bytes(const DevLayout &l, long long n_items);
 SmemPlan reuse_persist_plan(const DevLayout &l, int max_m, int run);
 bool persist_batch_ok(const DevLayout &l, const SmemPlan &p, int n_items, int max_tokens);
-cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s);
+cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s,
+                                 cudaEvent_t planned = nullptr);
 cudaError_t launch_relocate(const RelocArgs &a, cudaStream_t s);   // kamera_stream.cu
 cudaError_t launch_reuse_copy(const ReuseArgs &a, cudaStream_t s);  // kamera_stream.cu
 cudaError_t launch_reanchor(const AnchorArgs &a, cudaStream_t s);   // kamera_anchor.cu

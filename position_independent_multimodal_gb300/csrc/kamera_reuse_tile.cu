@@ -693,15 +693,17 @@ cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s) {
 // table, V_m^T, the first two tiles' loads and their latency) and ends in a tail as long as a
 // task; in a batch of shared chunks most of its CTAs only search their group and exit. Here a
 // planning kernel (one CTA) forms the groups once and lists the task rows: (top-first patched
-// layer, channel, the first item of a run), each covering every column tile of its rows. The
-// persistent CTAs come in sets of `ntile`, one per column tile; a set takes a contiguous range
-// of the rows' token tiles (ranges of equal weight, a token tile of a run of r members
-// weighing 32 + 5 r, within one tile of equal), and its CTAs walk the same tiles side by side,
-// so the column pieces of each pool row are written together as in the grid kernel. Each CTA
-// walks its range with the grid kernel's two-stage pipeline, carried across task boundaries:
-// the next task's first tiles and its V_m^T (two buffers, by task parity) are loaded while the
-// previous task's last tiles are finished, and TMEM and the barriers are set up once. Each
-// tile's bytes are those of the grid kernel.
+// layer, channel, the first item of a run), each covering every column tile of its rows, as
+// self-contained 128-byte records. The persistent CTAs come in sets of `ntile`, one per
+// column tile. Most of the rows' token tiles are split into one contiguous range per set, of
+// equal weight (a token tile of a run of r members weighing 5 + r); the sets' CTAs walk the
+// same tiles side by side, so the column pieces of each pool row are written together, as in
+// the grid kernel. When every task row has the same number of token tiles, the last part is
+// handed out one tile at a time from a counter per column tile, so CTAs that ran slower take
+// less of it. Each CTA walks its tiles with the grid kernel's two-stage pipeline, carried
+// across task boundaries: the next task's record, first tiles and V_m^T (two buffers, by task
+// parity) are loaded while the previous task's last tiles are finished, and TMEM and the
+// barriers are set up once. Each tile's bytes are those of the grid kernel.
 // ---------------------------------------------------------------------------------------
 
 namespace {
@@ -711,45 +713,51 @@ constexpr int kRecSlots = 32;         // task records held in shared memory
 constexpr int kRecFetch = 16;         // task records fetched at a time
 constexpr int kMaxPersistCtas = 1024;
 constexpr int kPlanThreads = 1024;
-constexpr int kMaxPlanItems = 2048;
-constexpr int kMaxPlanRows = 16384;   // task rows of one batch
+constexpr int kMaxPlanItems = 512;
+constexpr int kMaxPlanRows = 8192;    // task rows of one batch
 
-struct PlanRow {   // 16 bytes in the workspace
-  int item;        // the run's first item
-  int code;        // layer << 16 | channel << 8
-  int ntt_nmem;    // token tiles << 8 | members of the run
-  int mem;         // index of the run's member list
-};
-
-// One task (a task row at one column tile) in shared memory.
+// A task row in the workspace and in shared memory (128 bytes): the run's first item, the
+// row's layer and channel, its members' requests and first tokens.
 struct TaskRec {
-  kamera_item it;    // the run's first item
-  int code, nmem;    // layer << 16 | channel << 8 | column tile; members
-  int t_lo, t_hi;    // the token tiles of this task in the CTA's range
-  int req[kRunCapP], start[kRunCapP];  // the members' requests and first tokens
+  kamera_item it;
+  int code;        // layer << 16 | channel << 8 (the CTA adds its column tile)
+  int nmem;        // members of the run
+  int ntt;         // token tiles
+  int pad;
+  int req[kRunCapP], start[kRunCapP];
 };
 static_assert(sizeof(kamera_item) == 80, "kamera_item layout");
 static_assert(sizeof(TaskRec) == 128, "task record layout");
 
+// Plan header, the first 256 bytes of the workspace.
+struct PlanHead {
+  int rows;      // task rows
+  int tiles;     // tiles of all tasks (rows' token tiles x column tiles)
+  int weight;    // total weight of the rows' token tiles
+  int s1;        // token-tile positions [0, s1) go to the sets
+  int n_dyn;     // positions [s1, s1 + n_dyn) are handed out one at a time
+  int ntt;       // token tiles of every row (0: rows differ)
+  int stride;    // when ntt > 0, set q owns rows q, q + Q, ..., `stride` of them (otherwise set
+                 // q owns the range of row tiles starts[q] .. starts[q + 1])
+};
+
 // Byte offsets of the batch workspace for n items.
 struct WsLayout {
-  size_t starts;   // int2 [kMaxPersistCtas + 1]: (row, tile) where each set's range begins
-  size_t members;  // int2 [n][2][kRunCapP]: (request, first token) of each run's members
-  size_t rows;     // PlanRow [min(n * L * 2, kMaxPlanRows)]
+  size_t counters;  // int [kMaxPersistCtas]: handed-out positions per column tile
+  size_t starts;    // int2 [kMaxPersistCtas + 1]: (row, tile) where each set's range begins
+  size_t rows;      // TaskRec [min(n * L * 2, kMaxPlanRows)]
   size_t total;
 };
 __host__ __device__ inline WsLayout ws_layout(const DevLayout &l, long long n) {
   WsLayout w;
-  w.starts = 256;  // the first 256 bytes: int rows, tiles, weight
+  w.counters = 256;
+  w.starts = w.counters + 4 * (size_t)kMaxPersistCtas;
   size_t off = w.starts + 8 * (size_t)(kMaxPersistCtas + 1);
-  off = (off + 255) & ~(size_t)255;
-  w.members = off;
-  off += (size_t)n * 2 * kRunCapP * 8;
   off = (off + 255) & ~(size_t)255;
   w.rows = off;
   long long rows = n * l.L * 2;
   if (rows > kMaxPlanRows) rows = kMaxPlanRows;
-  off += (size_t)rows * sizeof(PlanRow);
+  off += (size_t)rows * sizeof(TaskRec);
   w.total = (off + 255) & ~(size_t)255;
   return w;
 }
@@ -764,16 +772,24 @@ __device__ __forceinline__ bool same_group(const kamera_item &me, const kamera_i
          o.patch_l1 == me.patch_l1 && (ch != 0 || same_offsets(o, me, lay));
 }
 
-// Shared memory of the planning kernel: the items, their lengths and layers, run sizes, the
-// weight prefix of the task rows and the scan.
-size_t plan_smem_bytes(int n) {
-  return 96 * (size_t)n + (((size_t)n * 2 + 15) & ~(size_t)15) + 4 * (size_t)(kMaxPlanRows + 1) +
-         4 * 32 * 4;
+__host__ __device__ __forceinline__ int tile_weight(int nmem) { return 5 + nmem; }
+
+// Candidate rows of a batch of n items (every layer, both channels), at most kMaxPlanRows.
+__host__ __device__ inline int plan_rows(const DevLayout &l, int n) {
+  const long long r = (long long)n * l.L * 2;
+  return r < kMaxPlanRows ? (int)r : kMaxPlanRows;
 }
 
-// One CTA of kPlanThreads: the groups, the task rows and the range of each of Q sets of CTAs,
-// into the workspace a.plan_ws. Rows past kMaxPlanRows are not planned (the host sizes batches
-// below it).
+// Shared memory of the planning kernel: the items, their lengths and layers, run sizes and
+// members, then per task row its weight prefix and (token tiles << 8 | members), and the scan.
+size_t plan_smem_bytes(const DevLayout &l, int n) {
+  return 96 * (size_t)n + (((size_t)n * 2 + 15) & ~(size_t)15) + 64 * (size_t)n +
+         8 * (size_t)(plan_rows(l, n) + 1) + 6 * 32 * 4;
+}
+
+// One CTA of kPlanThreads: the groups, the task rows, the range of each of Q sets of CTAs and
+// the handed-out tail, into the workspace a.plan_ws. Rows past kMaxPlanRows are not planned
+// (the host sizes batches below it).
 __global__ void __launch_bounds__(kPlanThreads) reuse_plan_kernel(const __grid_constant__ ReuseArgs a,
                                                                   int Q) {
   extern __shared__ __align__(16) unsigned char psm[];
@@ -782,19 +798,27 @@ __global__ void __launch_bounds__(kPlanThreads) reuse_plan_kernel(const __grid_c
   const int warp = tid >> 5, lane = tid & 31;
   unsigned char *ws = static_cast<unsigned char *>(a.plan_ws);
   const WsLayout W = ws_layout(lay, n);
-  int *head = reinterpret_cast<int *>(ws);
+  PlanHead *head = reinterpret_cast<PlanHead *>(ws);
+  int *counters = reinterpret_cast<int *>(ws + W.counters);
   int2 *starts = reinterpret_cast<int2 *>(ws + W.starts);
-  int2 *members = reinterpret_cast<int2 *>(ws + W.members);
-  PlanRow *rows = reinterpret_cast<PlanRow *>(ws + W.rows);
+  TaskRec *rows = reinterpret_cast<TaskRec *>(ws + W.rows);
+  const int RC = plan_rows(lay, n);
   kamera_item *items = reinterpret_cast<kamera_item *>(psm);  // the batch, staged once
   int4 *info = reinterpret_cast<int4 *>(psm + 80 * n);  // (tokens, or -1 when skipped; m, l0, l1)
   signed char *nm = reinterpret_cast<signed char *>(psm + 96 * n);  // run size per (item, ch)
-  int *wpre = reinterpret_cast<int *>(psm + 96 * n + ((2 * n + 15) & ~15));  // weight prefix
-  int *scan = wpre + kMaxPlanRows + 1;  // [4][32]
+  int2 *members = reinterpret_cast<int2 *>(psm + 96 * n + ((2 * n + 15) & ~15));  // [2n][4]
+  int *wpre = reinterpret_cast<int *>(members + 8 * n);  // weight prefix of the task rows
+  int *rinfo = wpre + RC + 1;                            // token tiles << 8 | members
+  int *scan = rinfo + RC;  // [3][32], then min and max token tiles
   {  // 16-byte words (the item array is 16-byte aligned and 80 bytes an item)
     const uint4 *src = reinterpret_cast<const uint4 *>(a.items);
     uint4 *dst = reinterpret_cast<uint4 *>(items);
     for (int q = tid; q < 5 * n; q += kPlanThreads) dst[q] = src[q];
+  }
+  for (int c = tid; c < lay.ntile; c += kPlanThreads) counters[c] = 0;
+  if (tid == 0) {
+    scan[96] = 0x7fffffff;
+    scan[97] = 0;
   }
   __syncthreads();
   for (int i = tid; i < n; i += kPlanThreads) {
@@ -838,15 +862,21 @@ __global__ void __launch_bounds__(kPlanThreads) reuse_plan_kernel(const __grid_c
     const int4 in = info[*i];
     return in.x > 0 && *layer >= in.z && *layer < in.w && nm[(*i << 1) | *ch] > 0;
   };
-  int cnt = 0, wsum = 0, tsum = 0;
+  int cnt = 0, wsum = 0, tsum = 0, tmin = 0x7fffffff, tmax = 0;
   for (int rr = r0; rr < r1; ++rr) {
     int i, layer, ch;
     if (task_row(rr, &i, &layer, &ch)) {
       const int ntt = (info[i].x + kTileRows - 1) / kTileRows;
       ++cnt;
       tsum += ntt;
-      wsum += ntt * (32 + 5 * nm[(i << 1) | ch]);
+      wsum += ntt * tile_weight(nm[(i << 1) | ch]);
+      tmin = min(tmin, ntt);
+      tmax = max(tmax, ntt);
     }
+  }
+  if (cnt > 0) {
+    atomicMin(&scan[96], tmin);
+    atomicMax(&scan[97], tmax);
   }
   int v0 = cnt, v1 = wsum, v2 = tsum;  // inclusive scans, warp then block
 #pragma unroll
@@ -878,24 +908,52 @@ __global__ void __launch_bounds__(kPlanThreads) reuse_plan_kernel(const __grid_c
     }
   }
   __syncthreads();
-  const int NR = min(scan[31], kMaxPlanRows), WT = scan[63], NT = scan[95];
+  const int NR = min(scan[31], RC), WT = scan[63], NT = scan[95];
   int k = (warp > 0 ? scan[warp - 1] : 0) + v0 - cnt;
   int wp = (warp > 0 ? scan[32 + warp - 1] : 0) + v1 - wsum;
   for (int rr = r0; rr < r1 && k < NR; ++rr) {
     int i, layer, ch;
     if (task_row(rr, &i, &layer, &ch)) {
       const int ntt = (info[i].x + kTileRows - 1) / kTileRows, j = (i << 1) | ch;
-      rows[k] = PlanRow{i, (layer << 16) | (ch << 8), (ntt << 8) | nm[j], j};
+      TaskRec rec;
+      rec.it = items[i];
+      rec.code = (layer << 16) | (ch << 8);
+      rec.nmem = nm[j];
+      rec.ntt = ntt;
+      rec.pad = 0;
+#pragma unroll
+      for (int f = 0; f < kRunCapP; ++f) {
+        const int2 mm = f < rec.nmem ? members[j * kRunCapP + f] : make_int2(0, 0);
+        rec.req[f] = mm.x;
+        rec.start[f] = mm.y;
+      }
+      rows[k] = rec;
       wpre[k] = wp;
-      wp += ntt * (32 + 5 * nm[j]);
+      rinfo[k] = (ntt << 8) | rec.nmem;
+      wp += ntt * tile_weight(nm[j]);
       ++k;
     }
   }
   if (tid == 0) wpre[NR] = WT;
   __syncthreads();
-  // set q begins at the first row tile whose weight prefix is at least floor(q * WT / Q)
+  // When every row has the same token tiles, set q owns whole rows q, q + Q, q + 2Q, ... (the
+  // sets work through neighbouring rows at the same time, so the runs of one chunk, which are
+  // neighbouring rows, read its canonical rows from L2 after the first), about five sixths of
+  // all rows, and the tiles of the rows left over are handed out one at a time, in order (a
+  // position names its row and tile by division). Otherwise each set owns one contiguous range
+  // of row tiles of equal weight and nothing is handed out.
+  const int uni = (NR > 0 && scan[96] == scan[97]) ? scan[97] : 0;
+  const int stride = uni > 0 ? (int)((long long)NR * 5 / (6ll * Q)) : 0;
+  const int s1 = uni > 0 ? Q * stride * uni : NT;
+  const int n_dyn = NT - s1;
+  const int w1 = uni > 0 ? wpre[s1 / uni] + (s1 % uni) * (s1 / uni < NR
+                                                                ? tile_weight(rinfo[s1 / uni] & 0xff)
+                                                                : 0)
+                         : WT;
+  const int2 s1pos = uni > 0 ? make_int2(s1 / uni, s1 % uni) : make_int2(NR, 0);
+  // set q begins at the first row tile whose weight prefix is at least floor(q * w1 / Q)
   for (int q = tid; q <= Q; q += kPlanThreads) {
-    const int target = (int)((long long)q * WT / Q);
+    const int target = (int)((long long)q * w1 / Q);
     int lo = 0, hi = NR;  // the first row r with wpre[r + 1] > target
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -904,37 +962,42 @@ __global__ void __launch_bounds__(kPlanThreads) reuse_plan_kernel(const __grid_c
       else
         lo = mid + 1;
     }
-    int2 st = make_int2(NR, 0);
+    int2 st = s1pos;
     if (lo < NR && q < Q) {
-      const int nn = rows[lo].ntt_nmem, w = 32 + 5 * (nn & 0xff);
+      const int ntt = rinfo[lo] >> 8, w = tile_weight(rinfo[lo] & 0xff);
       const int d = target - wpre[lo], t = d <= 0 ? 0 : (d + w - 1) / w;
-      st = t < (nn >> 8) ? make_int2(lo, t) : make_int2(lo + 1, 0);
+      st = t < ntt ? make_int2(lo, t) : make_int2(lo + 1, 0);
+      if (st.x > s1pos.x || (st.x == s1pos.x && st.y > s1pos.y)) st = s1pos;
     }
     starts[q] = st;
   }
   if (tid == 0) {
-    head[0] = NR;
-    head[1] = NT * lay.ntile;
-    head[2] = WT;
+    head->rows = NR;
+    head->tiles = NT * lay.ntile;
+    head->weight = WT;
+    head->s1 = s1;
+    head->n_dyn = n_dyn;
+    head->ntt = uni;
+    head->stride = stride;
   }
 }
 
-// What the loops need of a task record.
+// What the loops need of a task record at column tile ct.
 struct TaskV {
-  int layer, ch, nmem, T, m, ntt, row, li, tensor;
+  int layer, ch, nmem, T, m, row, li, tensor;
   Tile tile;
 };
-__device__ __forceinline__ TaskV task_v(const TaskRec &r, const DevLayout &lay, int engine) {
+__device__ __forceinline__ TaskV task_v(const TaskRec &r, const DevLayout &lay, int engine,
+                                        int ct) {
   TaskV v;
   v.layer = r.code >> 16;
   v.ch = (r.code >> 8) & 0xff;
   v.nmem = r.nmem;
   v.T = r.it.num_tokens;
   v.m = r.it.patch_m;
-  v.ntt = (v.T + kTileRows - 1) / kTileRows;
   v.row = v.ch == 0 ? lay.row_k : lay.row_v;
   v.li = v.layer - r.it.patch_l0;
-  v.tile = tile_of(lay, v.ch, r.code & 0xff, v.ch == 0 && item_rotates(r.it, lay));
+  v.tile = tile_of(lay, v.ch, ct, v.ch == 0 && item_rotates(r.it, lay));
   v.tensor = engine == kEngineTensor && (v.m & 7) == 0 && aligned16(r.it.patch_u);
   return v;
 }
@@ -947,56 +1010,125 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
   const SmemPlan &P = a.smem;
   const DevLayout &lay = a.lay;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const unsigned char *ws = static_cast<const unsigned char *>(a.plan_ws);
+  unsigned char *ws = static_cast<unsigned char *>(a.plan_ws);
   const WsLayout W = ws_layout(lay, a.n_items);
-  const int2 *starts = reinterpret_cast<const int2 *>(ws + W.starts);
-  const int2 *memtab = reinterpret_cast<const int2 *>(ws + W.members);
-  const PlanRow *prow = reinterpret_cast<const PlanRow *>(ws + W.rows);
-  // this CTA: column tile c of set q, whose range runs from token tile b.y of task row b.x to
-  // token tile e.y of task row e.x (exclusive)
-  const int nt = lay.ntile, q = blockIdx.x / nt, c = blockIdx.x - q * nt;
-  const int2 b = starts[q], e = starts[q + 1];
-  if (b.x == e.x && b.y == e.y) return;  // an empty range
-  const int n_local = e.x - b.x + (e.y > 0 ? 1 : 0);  // tasks of the range, in order
-  TaskRec *rec = reinterpret_cast<TaskRec *>(sp + P.recs);
-  // records of the range's tasks [j0, j1) into their slots, one thread per task
-  auto fetch = [&](int j0, int j1) {
-    for (int j = j0 + tid; j < j1; j += kThrT) {
-      const int row = b.x + j;
-      const PlanRow pr = prow[row];
-      TaskRec &r = rec[j % kRecSlots];
-      r.it = a.items[pr.item];
-      r.code = pr.code | c;
-      r.nmem = pr.ntt_nmem & 0xff;
-      r.t_lo = j == 0 ? b.y : 0;
-      r.t_hi = row == e.x ? e.y : pr.ntt_nmem >> 8;
-      for (int f = 0; f < r.nmem; ++f) {
-        const int2 mm = memtab[pr.mem * kRunCapP + f];
-        r.req[f] = mm.x;
-        r.start[f] = mm.y;
-      }
-    }
-  };
-  int loaded = min(n_local, kRecFetch);
-  fetch(0, loaded);
-
-  const uint32_t x_op = s0 + P.canon, pg_op = s0 + P.pages, slots = s0 + P.slots;
   const uint32_t s_tmem = s0 + P.misc, s_bar = s0 + P.misc + 8;  // two MMA barriers
   volatile int *flag = reinterpret_cast<volatile int *>(sp + P.misc + 4);
+  if (warp == 0) {
+    ptx::tmem_alloc(s_tmem, P.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    ptx::mbar_init(s_bar, 1);
+    ptx::mbar_init(s_bar + 8, 1);
+    ptx::fence_mbar_init();
+    *flag = 0;
+  }
+  const PlanHead head = *reinterpret_cast<const PlanHead *>(ws);
+  int *counter = reinterpret_cast<int *>(ws + W.counters);
+  const int2 *starts = reinterpret_cast<const int2 *>(ws + W.starts);
+  const TaskRec *grow = reinterpret_cast<const TaskRec *>(ws + W.rows);
+  // this CTA: column tile c of set q; its own range runs from token tile b.y of task row b.x
+  // to token tile e.y of row e.x (exclusive), then it takes tail positions of column c
+  const int nt = lay.ntile, q = blockIdx.x / nt, c = blockIdx.x - q * nt;
+  const int Q = gridDim.x / nt;
+  const int2 b = starts[q], e = starts[q + 1];
+  const bool own = head.ntt > 0 ? head.stride > 0 : !(b.x == e.x && b.y == e.y);
+  // nothing to do: free TMEM (the barrier orders the allocation's write of its address)
+  auto leave = [&]() {
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(*reinterpret_cast<volatile uint32_t *>(sp + P.misc),
+                                     P.tmem_cols);
+  };
+  if (!own && head.n_dyn == 0) {
+    leave();
+    return;
+  }
+  // tasks of the own rows (every stride-th row) or of the own range
+  const int n_own = !own ? 0 : head.ntt > 0 ? head.stride : e.x - b.x + (e.y > 0 ? 1 : 0);
+  auto own_row = [&](int j) { return head.ntt > 0 ? q + j * Q : b.x + j; };
+  TaskRec *rec = reinterpret_cast<TaskRec *>(sp + P.recs);
+  // local task j: record slot j % kRecSlots; its row and token tiles [t_lo, t_hi)
+  int *l_row = reinterpret_cast<int *>(sp + P.misc + 128);
+  int *l_lo = l_row + kRecSlots, *l_hi = l_lo + kRecSlots;
+  volatile int *s_nlocal = reinterpret_cast<volatile int *>(sp + P.misc + 32);
+  volatile int *s_final = reinterpret_cast<volatile int *>(sp + P.misc + 36);
+  // copies of task rows into record slots: 8 threads per record (16-byte words)
+  auto copy_rec = [&](int j, int row, int part) {
+    ptx::cp_async16(s0 + P.recs + (j % kRecSlots) * 128 + 16 * part,
+                    reinterpret_cast<const unsigned char *>(grow + row) + 16 * part, 16u);
+  };
+  // own-range tasks [j0, j1): records and tile ranges, then wait (every thread calls)
+  auto fetch_own = [&](int j0, int j1) {
+    for (int x = tid; x < 8 * (j1 - j0); x += kThrT)
+      copy_rec(j0 + (x >> 3), own_row(j0 + (x >> 3)), x & 7);
+    ptx::cp_async_commit();
+    ptx::cp_async_wait_all();
+    __syncthreads();
+    for (int j = j0 + tid; j < j1; j += kThrT) {
+      const int row = own_row(j);
+      const bool ranged = head.ntt == 0;
+      l_row[j % kRecSlots] = row;
+      l_lo[j % kRecSlots] = ranged && j == 0 ? b.y : 0;
+      l_hi[j % kRecSlots] = ranged && row == e.x ? e.y : rec[j % kRecSlots].ntt;
+    }
+    __syncthreads();
+  };
+  // tail positions of column c (thread 0): `res` is the position reserved by the last
+  // increment; taking it appends a one-tile task (its record copied by thread 0) or ends the
+  // list
+  int res = 0;
+  auto take = [&](int n_local) -> bool {  // thread 0; returns false when the tail is used up
+    const int pos = res;
+    if (pos >= head.n_dyn) return false;
+    const int p = head.s1 + pos, row = p / head.ntt, j = n_local;
+    l_row[j % kRecSlots] = row;
+    l_lo[j % kRecSlots] = p - row * head.ntt;
+    l_hi[j % kRecSlots] = p - row * head.ntt + 1;
+    for (int part = 0; part < 8; ++part) copy_rec(j, row, part);
+    ptx::cp_async_commit();
+    res = atomicAdd(counter + c, 1);
+    return true;
+  };
+  if (tid == 0 && head.n_dyn > 0) res = atomicAdd(counter + c, 1);
+  int loaded = min(n_own, kRecFetch);
+  if (loaded > 0) fetch_own(0, loaded);
+  if (tid == 0) {
+    int nl = n_own, fin = head.n_dyn == 0 ? 1 : 0;
+    while (!fin && nl < 3) {  // no own range (or a short one): start on the tail
+      if (take(nl))
+        ++nl;
+      else
+        fin = 1;
+    }
+    *s_nlocal = nl;
+    *s_final = fin;
+  }
+  ptx::cp_async_wait_all();
+  __syncthreads();
+  int n_local = *s_nlocal;
+  if (n_local == 0) {  // the tail was used up before this CTA started
+    leave();
+    return;
+  }
+
+  const uint32_t x_op = s0 + P.canon, pg_op = s0 + P.pages, slots = s0 + P.slots;
   const bool u2 = P.u_bufs == 2;
   const int ps = lay.page_size;
   const DivMod psd(ps);
   const int lc = tid & 7, lr = tid >> 3;  // copies: chunk of an atom row, row of each pass
   const uint32_t swc = (uint32_t)((lc ^ (lr & 7)) << 4);
-  auto rec_of = [&](int k) -> const TaskRec & { return rec[k % kRecSlots]; };
+  auto rec_of = [&](int j) -> const TaskRec & { return rec[j % kRecSlots]; };
   auto u_buf = [&](int g) { return s0 + P.a_op + (u2 ? (g & 1) * P.a_stage : 0); };
-  auto vt_buf = [&](int k) { return s0 + P.b_op + (k & 1) * P.b_stage; };
-  auto rot_of = [&](int k) { return reinterpret_cast<float *>(sp + P.cs + (k & 1) * P.cs_stage); };
+  auto vt_buf = [&](int j) { return s0 + P.b_op + (j & 1) * P.b_stage; };
+  auto rot_of = [&](int j) { return reinterpret_cast<float *>(sp + P.cs + (j & 1) * P.cs_stage); };
 
-  // canonical rows of tile t of task k into stage s, and the page ids of its members' tokens
-  auto issue_x = [&](int k, int t, int s) {
-    const TaskRec &R = rec_of(k);
-    const TaskV v = task_v(R, lay, a.engine);
+  // canonical rows of token tile t of task j into stage s, and the page ids of its members
+  auto issue_x = [&](int j, int t, int s) {
+    const TaskRec &R = rec_of(j);
+    const TaskV v = task_v(R, lay, a.engine, c);
     const int t0 = t * kTileRows, rows = min(kTileRows, v.T - t0);
     const int atoms = v.tile.ncols >> 6;
     const __nv_bfloat16 *src =
@@ -1014,55 +1146,55 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
       }
     }
     const int pgs = P.pg_per_member;
-    for (int q = tid; q < v.nmem * pgs; q += kThrT) {
-      const int f = q / pgs, kk = q - f * pgs;
+    for (int x = tid; x < v.nmem * pgs; x += kThrT) {
+      const int f = x / pgs, kk = x - f * pgs;
       int p_first, off0, npages, dummy;
       psd.split(R.start[f] + t0, &p_first, &off0);
       psd.split(off0 + rows - 1, &npages, &dummy);
       if (kk <= npages)
-        ptx::cp_async4(pg_op + s * P.pages_stage + 4 * q,
+        ptx::cp_async4(pg_op + s * P.pages_stage + 4 * x,
                        a.pool.pt + (long long)R.req[f] * a.pool.pt_stride + p_first + kk);
     }
   };
-  // U rows of tile t of task k as the A operand in buffer ub; rank padding zeroed
-  auto issue_u = [&](int k, int t, uint32_t ub) {
-    const TaskRec &R = rec_of(k);
-    const TaskV v = task_v(R, lay, a.engine);
+  // U rows of token tile t of task j as the A operand in buffer ub; rank padding zeroed
+  auto issue_u = [&](int j, int t, uint32_t ub) {
+    const TaskRec &R = rec_of(j);
+    const TaskV v = task_v(R, lay, a.engine, c);
     const int t0 = t * kTileRows, rows = min(kTileRows, v.T - t0);
     const int m = v.m, m8 = m >> 3, Kp = (m + 15) & ~15;
     const __nv_bfloat16 *Ut = static_cast<const __nv_bfloat16 *>(R.it.patch_u) +
                               ((long long)(v.li * 2 + v.tile.group) * v.T + t0) * m;
     if (v.tensor) {
       const DivMod md(m8);
-      for (int q = tid; q < rows * m8; q += kThrT) {
+      for (int x = tid; x < rows * m8; x += kThrT) {
         int rr, kc;
-        md.split(q, &rr, &kc);
+        md.split(x, &rr, &kc);
         ptx::cp_async16(ub + ((kc * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4),
                         Ut + (long long)rr * m + kc * 8, 16u);
       }
-      for (int q = tid; q < kTileRows * ((Kp >> 3) - m8); q += kThrT) {
-        const int kc = m8 + (q >> 7), rr = q & 127;
+      for (int x = tid; x < kTileRows * ((Kp >> 3) - m8); x += kThrT) {
+        const int kc = m8 + (x >> 7), rr = x & 127;
         sts16(ub + ((kc * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4), make_uint4(0u, 0u, 0u, 0u));
       }
     } else {
-      for (int q = tid; q < kTileRows * Kp; q += kThrT) {
-        const int rr = q / Kp, kk = q - rr * Kp;
+      for (int x = tid; x < kTileRows * Kp; x += kThrT) {
+        const int rr = x / Kp, kk = x - rr * Kp;
         const uint32_t val = (rr < rows && kk < m) ? ldg_u16(Ut + (long long)rr * m + kk) : 0u;
         sts_u16(ub + (((kk >> 3) * 16 + (rr >> 3)) << 7) + ((rr & 7) << 4) + ((kk & 7) << 1), val);
       }
     }
   };
   // a new task: its phase table (plain stores) and V_m^T (copies) in the task-parity buffers
-  auto prepare = [&](int k) {
-    const TaskRec &R = rec_of(k);
-    const TaskV v = task_v(R, lay, a.engine);
+  auto prepare = [&](int j) {
+    const TaskRec &R = rec_of(j);
+    const TaskV v = task_v(R, lay, a.engine, c);
     if (v.tile.band > 0) {
-      float *rot = rot_of(k);
+      float *rot = rot_of(j);
       for (int i = tid; i < lay.npairs; i += kThrT) {
-        const float2 c = rope_phase(a.freq.q[i], pair_delta(R.it, lay, i));
-        rot[i] = c.x;
-        rot[lay.npairs + i] = c.y;
-        rot[2 * lay.npairs + i] = -c.y;
+        const float2 cs = rope_phase(a.freq.q[i], pair_delta(R.it, lay, i));
+        rot[i] = cs.x;
+        rot[lay.npairs + i] = cs.y;
+        rot[2 * lay.npairs + i] = -cs.y;
       }
     }
     const int m = v.m, Kp = (m + 15) & ~15, ncore = v.tile.ncols >> 3;
@@ -1070,23 +1202,23 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
     const __nv_bfloat16 *vt = static_cast<const __nv_bfloat16 *>(R.it.patch_vt) +
                               (long long)v.li * m * (lay.w0 + lay.w1) +
                               (v.tile.group == 0 ? 0 : (long long)m * lay.w0) + v.tile.gcol0;
-    const uint32_t vb = vt_buf(k);
-    for (int q = tid; q < Kp * ncore; q += kThrT) {
-      const int kk = q / ncore, j = q - kk * ncore;
+    const uint32_t vb = vt_buf(j);
+    for (int x = tid; x < Kp * ncore; x += kThrT) {
+      const int kk = x / ncore, jj = x - kk * ncore;
       const bool ok = kk < m;
-      ptx::cp_async16(vb + ((kk >> 3) * ncore + j) * 128 + (kk & 7) * 16,
-                      ok ? (const void *)(vt + (long long)kk * wg + 8 * j) : (const void *)vt,
+      ptx::cp_async16(vb + ((kk >> 3) * ncore + jj) * 128 + (kk & 7) * 16,
+                      ok ? (const void *)(vt + (long long)kk * wg + 8 * jj) : (const void *)vt,
                       ok ? 16u : 0u);
     }
   };
   uint32_t tmem = 0;
-  // MMA of tile g (task k) into accumulator g & 1 (one thread); arrives on barrier g & 1
-  auto issue_mma = [&](int k, int g) {
-    const TaskRec &R = rec_of(k);
-    const TaskV v = task_v(R, lay, a.engine);
+  // MMA of tile g (task j) into accumulator g & 1 (one thread); arrives on barrier g & 1
+  auto issue_mma = [&](int j, int g) {
+    const TaskRec &R = rec_of(j);
+    const TaskV v = task_v(R, lay, a.engine, c);
     const int Kp = (v.m + 15) & ~15, ncore = v.tile.ncols >> 3;
     ptx::tc_fence_after();
-    const uint32_t ub = u_buf(g), vb = vt_buf(k), d = tmem + (g & 1) * P.acc_cols;
+    const uint32_t ub = u_buf(g), vb = vt_buf(j), d = tmem + (g & 1) * P.acc_cols;
     const uint32_t idesc = ptx::idesc_bf16_f32(kTileRows, v.tile.ncols) | (1u << 16);
     for (int ks = 0; ks < Kp / 16; ++ks)
       ptx::mma_bf16(d, ptx::smem_desc(ub + ks * 2 * 2048, 2048, 128),
@@ -1094,37 +1226,34 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
                     ks > 0 ? 1u : 0u);
     ptx::mma_commit(s_bar + 8 * (g & 1));
   };
-  auto at_end = [&](int j, int) { return j == n_local; };
-  auto next = [&](int &j, int &t) {
-    if (++t == rec_of(j).t_hi) {
+  // the tile after (j, t); true when it begins task j + 1 (whose first tile is read from the
+  // task list when that task is reached)
+  auto next = [&](int &j, int &t) -> bool {
+    if (++t == l_hi[j % kRecSlots]) {
       ++j;
-      t = 0;
+      return true;
     }
+    return false;
   };
 
-  if (warp == 0) {
-    ptx::tmem_alloc(s_tmem, P.tmem_cols);
-    ptx::tmem_relinquish();
-  }
-  if (tid == 0) {
-    ptx::mbar_init(s_bar, 1);
-    ptx::mbar_init(s_bar + 8, 1);
-    ptx::fence_mbar_init();
-    *flag = 0;
-  }
-  __syncthreads();  // task records visible
-  int ck = 0, ctl = b.y;  // the tile being finished (local task, token tile)
-  int lk = 0, lt = b.y;   // the next tile to load
+  int ck = 0, ctl = l_lo[0];  // the tile being finished (local task, token tile)
+  int lk = 0, lt = ctl;       // the next tile to load
+  // tasks below n_ready have their records in shared memory (tasks of the own range past
+  // `loaded` are fetched when reached); a task taken from the tail lands one iteration later
+  int n_ready = n_local;
   prepare(lk);
   issue_x(lk, lt, 0);
   issue_u(lk, lt, u_buf(0));
   ptx::cp_async_commit();
-  next(lk, lt);
-  if (!at_end(lk, lt)) {
-    if (lt == 0) prepare(lk);
+  bool fresh = next(lk, lt);
+  if (lk < n_local) {
+    if (fresh) {
+      lt = l_lo[lk % kRecSlots];
+      prepare(lk);
+    }
     issue_x(lk, lt, 1);
     if (u2) issue_u(lk, lt, u_buf(1));
-    next(lk, lt);
+    fresh = next(lk, lt);
   }
   ptx::cp_async_commit();
   ptx::cp_async_wait_group1();  // tile 0, its U and V_m^T
@@ -1135,7 +1264,7 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
   tmem = *reinterpret_cast<volatile uint32_t *>(sp + P.misc);
   bool timed_out = false;
   uint32_t ph = 0;  // parity of each MMA barrier's next phase
-  if (tid == 0 && task_v(rec_of(ck), lay, a.engine).tensor) issue_mma(ck, 0);
+  if (tid == 0 && task_v(rec_of(ck), lay, a.engine, c).tensor) issue_mma(ck, 0);
   const int r = ((warp & 3) << 5) + lane;  // epilogue row (TMEM lane)
   const int half = warp >> 2;
   const uint32_t trow0 = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -1144,14 +1273,14 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
   const unsigned long long pool_v =
       a.pool.v ? static_cast<unsigned long long>(__cvta_generic_to_global(a.pool.v)) : 0ull;
 
-  for (int g = 0; !at_end(ck, ctl); ++g) {
+  for (int g = 0; ck < n_local; ++g) {
     const int s = g & 1;
     const TaskRec &R = rec_of(ck);
-    const TaskV v = task_v(R, lay, a.engine);
+    const TaskV v = task_v(R, lay, a.engine, c);
     const int t0 = ctl * kTileRows, rows = min(kTileRows, v.T - t0);
-    int nk = ck, nt = ctl;
-    next(nk, nt);
-    const bool has_next = !at_end(nk, nt);
+    int nk = ck, ntl = ctl;
+    if (next(nk, ntl) && nk < n_local) ntl = l_lo[nk % kRecSlots];
+    const bool has_next = nk < n_local;
     const bool use_tc = v.tensor && !timed_out;
     if (use_tc) {  // warp 0 waits for MMA(g); the other warps sleep at the barrier
       if (warp == 0) {
@@ -1171,7 +1300,7 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
     }
     // one U buffer: MMA(g) has read it, so U of the next tile may land now
     if (!u2 && v.tensor && has_next) {
-      issue_u(nk, nt, u_buf(g + 1));
+      issue_u(nk, ntl, u_buf(g + 1));
       ptx::cp_async_commit();
     }
     const bool write = !(v.tensor && timed_out);
@@ -1216,14 +1345,14 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
     // the CUDA-core path with one U buffer reads U(g) in the epilogue: U of the next tile after
     if (!u2 && !v.tensor && has_next) {
       __syncthreads();
-      issue_u(nk, nt, u_buf(g + 1));
+      issue_u(nk, ntl, u_buf(g + 1));
       ptx::cp_async_commit();
     }
-    ptx::cp_async_wait_all();  // the next tile's rows, pages, U and V_m^T
+    ptx::cp_async_wait_all();  // the next tile's rows, pages, U and V_m^T; new task records
     ptx::fence_proxy_async_smem();
     if (use_tc) ptx::tc_fence_before();
     __syncthreads();  // rows of tile g complete, the next tile staged
-    if (has_next && !timed_out && tid == 0 && task_v(rec_of(nk), lay, a.engine).tensor)
+    if (has_next && !timed_out && tid == 0 && task_v(rec_of(nk), lay, a.engine, c).tensor)
       issue_mma(nk, g + 1);
     if (write) {  // 4 rows x 128 bytes per warp instruction, once per member
       const uint32_t src = xs + lr * 128 + swc;
@@ -1250,24 +1379,36 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
         }
       }
     }
-    __syncthreads();  // stage s is free
-    if (!at_end(lk, lt)) {  // the tile after the next one
-      if (lt == 0) {        // starts a task
-        if (lk >= loaded) {
-          const int k1 = min(n_local, lk + kRecFetch);
-          fetch(lk, k1);
-          loaded = k1;
-          __syncthreads();
+    // keep two tasks past the load cursor listed: take a tail position (thread 0); lk moves
+    // by at most one task an iteration, so the task it loads next was listed (and its record
+    // landed) at least one iteration before
+    if (tid == 0 && !*s_final && n_local - lk < 2) {
+      if (take(n_local))
+        *s_nlocal = n_local + 1;
+      else
+        *s_final = 1;
+    }
+    __syncthreads();  // stage s is free; the task list as thread 0 left it
+    const int n_now = *s_nlocal;
+    if (lk < n_ready) {  // the tile after the next one
+      if (fresh) {       // starts a task
+        if (lk < n_own && lk >= loaded) {
+          const int j1 = min(n_own, lk + kRecFetch);
+          fetch_own(lk, j1);
+          loaded = j1;
         }
+        lt = l_lo[lk % kRecSlots];
         prepare(lk);
       }
       issue_x(lk, lt, s);
       if (u2) issue_u(lk, lt, u_buf(g));
-      next(lk, lt);
+      fresh = next(lk, lt);
     }
+    n_ready = n_now;
+    n_local = n_now;
     ptx::cp_async_commit();
     ck = nk;
-    ctl = nt;
+    ctl = ntl;
   }
   ptx::cp_async_wait_all();
   ptx::tc_fence_before();
@@ -1276,7 +1417,7 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
 }
 
 // Offsets of the persistent kernel's shared memory: the tile kernel's stages and U buffers,
-// two V_m^T buffers and two phase tables (by task parity), and the task records.
+// two V_m^T buffers and two phase tables (by task parity), the task records and the task list.
 SmemPlan persist_plan_with(const DevLayout &l, int max_m, int run, int u_bufs) {
   SmemPlan p{};
   int widest = l.tw;
@@ -1307,8 +1448,10 @@ SmemPlan persist_plan_with(const DevLayout &l, int max_m, int run, int u_bufs) {
   off += align128t(run * kTileRows * 4);
   p.recs = off;
   off += kRecSlots * (int)sizeof(TaskRec);
-  p.misc = off;  // TMEM address, timeout flag, two MMA barriers
-  off += 128;
+  // TMEM address, timeout flag, two MMA barriers, the task count and end flag, and each local
+  // task's row and token tiles (three int [kRecSlots] from +128)
+  p.misc = off;
+  off += 128 + 3 * 4 * kRecSlots;
   p.total = off + 1024;
   int cols = 32;
   while (cols < widest) cols <<= 1;
@@ -1336,11 +1479,12 @@ bool persist_batch_ok(const DevLayout &l, const SmemPlan &p, int n_items, int ma
   const long long rows = (long long)n_items * l.L * 2;
   const long long ntt = ((long long)max_tokens + kTileRows - 1) / kTileRows;
   return p.fast && l.kind == KAMERA_GQA && n_items >= 1 && n_items <= kMaxPlanItems &&
-         rows <= kMaxPlanRows && rows * ntt * (32 + 5 * kRunCapP) < (1ll << 31) &&
-         l.ntile <= kMaxPersistCtas && plan_smem_bytes(n_items) <= 227 * 1024;
+         rows <= kMaxPlanRows && rows * ntt * tile_weight(kRunCapP) < (1ll << 31) &&
+         rows * ntt < (1ll << 31) / l.ntile && l.ntile <= kMaxPersistCtas &&
+         plan_smem_bytes(l, n_items) <= 227 * 1024;
 }
 
-cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s) {
+cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s, cudaEvent_t planned) {
   static int configured[2][64] = {{0}};
   static int sm_count[64] = {0};
   int dev = 0;
@@ -1351,7 +1495,7 @@ cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s) {
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
-  const int plan_smem = (int)plan_smem_bytes(a.n_items);
+  const int plan_smem = (int)plan_smem_bytes(a.lay, a.n_items);
   if (plan_smem > configured[0][dev] && plan_smem > 48 * 1024) {
     e = cudaFuncSetAttribute(reuse_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              plan_smem);
@@ -1369,6 +1513,10 @@ cudaError_t launch_reuse_persist(const ReuseArgs &a, cudaStream_t s) {
   reuse_plan_kernel<<<1, kPlanThreads, plan_smem, s>>>(a, Q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (planned) {
+    e = cudaEventRecord(planned, s);
+    if (e != cudaSuccess) return e;
+  }
   reuse_persist_kernel<<<Q * a.lay.ntile, kThrT, a.smem.total, s>>>(a);
   return cudaGetLastError();
 }

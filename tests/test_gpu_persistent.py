@@ -55,7 +55,8 @@ def orderings(layout, m, name, Ts=(130, 256, 77), prefix=5):
 
 def run(w, items, workspace, options=None):
     """kamera_batch_reuse of the items; with `workspace`, through a batch workspace whose
-    header is returned as (tasks, tiles), else (None, None)."""
+    header is returned (task rows, tiles, weight, static positions, tail positions, token tiles
+    per row when every row has the same), else Nones."""
     h = km.create(w.layout, **(options or {}))
     ws = None
     if workspace:
@@ -63,10 +64,9 @@ def run(w, items, workspace, options=None):
                         dtype=torch.uint8, device="cuda")
         km.kamera_set_batch_workspace(h, ws)
     k, v, status, _ = tl.run_batch(h, w.layout, items, w.page_table, w.num_slots)
-    head = (None, None)
+    head = (None,) * 6
     if ws is not None:
-        hv = ws[:8].view(torch.int32).cpu().tolist()
-        head = (hv[0], hv[1])
+        head = tuple(ws[:24].view(torch.int32).cpu().tolist())
     return k, v, status, head
 
 
@@ -74,13 +74,17 @@ def same_bytes(a, b):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def compare(w, items=None, options=None, status=0, oracle_items=None, persistent=True):
+def compare(w, items=None, options=None, status=0, oracle_items=None, persistent=True,
+            tail=None):
     items = items if items is not None else tl.to_device_items(w.items)
-    k, v, st, (n_tasks, n_tiles) = run(w, items, True, options)
+    k, v, st, head = run(w, items, True, options)
+    n_tasks, n_tiles = head[:2]
     k0, v0, st0, _ = run(w, items, False, options)
     assert st == status and st0 == status
     if persistent:
         assert n_tasks > 0 and n_tiles >= n_tasks, "the persistent path did not run"
+        if tail is not None:
+            assert (head[4] > 0) == tail, "tail positions handed out" if tail else "no tail"
     else:
         assert (n_tasks, n_tiles) == (-1, -1), "the persistent path ran"
     same_bytes(k, k0)
@@ -99,6 +103,16 @@ def test_orderings_match_the_grid_path_and_the_oracle(shape, m):
     compare(w, oracle_items=w.items, persistent=shape != "mla")
 
 
+@pytest.mark.parametrize("m", [12, 32])
+@pytest.mark.parametrize("shape", ["gqa64", "gqa128"])
+def test_equal_lengths_hand_out_a_tail(shape, m):
+    # every chunk 300 tokens (3 token tiles a row): the last sixth of the row tiles is handed
+    # out one at a time, here with runs of 2 (K) and 3 (V) members
+    lay = {"gqa64": gqa(), "gqa128": gqa(H=4, hd=128)}[shape]
+    w = orderings(lay, m, f"perstail{shape}{m}", Ts=(300, 300, 300))
+    compare(w, oracle_items=w.items, tail=True)
+
+
 def test_task_and_tile_counts_of_the_plan():
     # GQA, 2 heads of 128 -> 2 column tiles; layers 1 and 2 patched. K groups: placements with
     # equal (chunk, offset); V groups: every placement of a chunk; each taken in runs of 3
@@ -115,7 +129,7 @@ def test_task_and_tile_counts_of_the_plan():
     k_runs, k_tiles = runs_and_tiles(lambda it: (id(it.canon_k), it.delta))
     v_runs, v_tiles = runs_and_tiles(lambda it: id(it.canon_v))
     assert (k_runs, v_runs) == (12, 6)
-    n_rows, n_tiles = compare(w)
+    n_rows, n_tiles = compare(w, tail=False)
     assert n_rows == 2 * (k_runs + v_runs)  # task rows: 2 patched layers
     assert n_tiles == 2 * 2 * (k_tiles + v_tiles)  # x 2 column tiles
 
@@ -184,16 +198,17 @@ def test_mixed_ranks_lengths_and_unpatched_items():
 
 
 def test_many_one_tile_tasks_refetch_their_records():
-    # 1000 short chunks, each in its own request: 1000 x 2 patched layers x 2 channels = 4000
-    # one-tile task rows over two column tiles (4 heads of 64, two per tile); each CTA's range
-    # holds about 26 of them, more than one fetch of records
-    lay = gqa(L=3, H=4, hd=64)
-    n = 1000
+    # 400 short chunks, each in its own request, 10 layers (9 patched): 400 x 9 x 2 = 7200
+    # one-tile task rows over two column tiles (4 heads of 64, two per tile); each CTA's own
+    # range holds about 40 of them, more than one fetch of records, and the last sixth of the
+    # positions is handed out one tile at a time
+    lay = gqa(L=10, H=4, hd=64)
+    n = 400
     Ts = [16 + (i * 37) % 100 for i in range(n)]
     placements = [(i, i, 0, 7 * i - 300) for i in range(n)]
     w = wl.reuse_workload("persmany", lay, n_chunks=n, T=Ts, placements=placements, m=8, l0=1,
-                          l1=3, seed=9, strong=False, extra_pages=0)
-    n_rows, n_tiles = compare(w)
-    assert n_rows == n * 2 * 2 and n_tiles == 2 * n_rows
+                          l1=10, seed=9, strong=False, extra_pages=0)
+    n_rows, n_tiles = compare(w, tail=True)
+    assert n_rows == n * 9 * 2 and n_tiles == 2 * n_rows
     k, v, _, _ = run(w, tl.to_device_items(w.items), True)
     tl.check_full(lay, w.items, w.page_table, k, v)
