@@ -1238,9 +1238,6 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
 
   int ck = 0, ctl = l_lo[0];  // the tile being finished (local task, token tile)
   int lk = 0, lt = ctl;       // the next tile to load
-  // tasks below n_ready have their records in shared memory (tasks of the own range past
-  // `loaded` are fetched when reached); a task taken from the tail lands one iteration later
-  int n_ready = n_local;
   prepare(lk);
   issue_x(lk, lt, 0);
   issue_u(lk, lt, u_buf(0));
@@ -1291,6 +1288,7 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
       ptx::tc_fence_before();
     }
     __syncthreads();
+    n_local = *s_nlocal;  // the task list as thread 0 left it in the last iteration
     if (use_tc) {
       ptx::tc_fence_after();
       if (*flag) {
@@ -1379,18 +1377,20 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
         }
       }
     }
-    // keep two tasks past the load cursor listed: take a tail position (thread 0); lk moves
-    // by at most one task an iteration, so the task it loads next was listed (and its record
-    // landed) at least one iteration before
+    // keep two tasks past the load cursor listed: take a tail position (thread 0; the others
+    // read the list after the next barrier); lk moves by at most one task an iteration, so the
+    // task it loads next was listed (and its record landed) at least one iteration before
     if (tid == 0 && !*s_final && n_local - lk < 2) {
       if (take(n_local))
         *s_nlocal = n_local + 1;
       else
         *s_final = 1;
     }
-    __syncthreads();  // stage s is free; the task list as thread 0 left it
-    const int n_now = *s_nlocal;
-    if (lk < n_ready) {  // the tile after the next one
+    // The tile after the next one goes into stage s with no barrier first: each thread loads
+    // exactly the chunks of the stage that it stored from (the same row and chunk mapping),
+    // after its own reads of them; the epilogue's other mapping finished before the last
+    // barrier, and the page ids of stage s were read before it.
+    if (lk < n_local) {
       if (fresh) {       // starts a task
         if (lk < n_own && lk >= loaded) {
           const int j1 = min(n_own, lk + kRecFetch);
@@ -1404,8 +1404,6 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
       if (u2) issue_u(lk, lt, u_buf(g));
       fresh = next(lk, lt);
     }
-    n_ready = n_now;
-    n_local = n_now;
     ptx::cp_async_commit();
     ck = nk;
     ctl = ntl;
