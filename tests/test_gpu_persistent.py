@@ -9,10 +9,13 @@ silent fall-back to the grid path cannot pass for the persistent one, and the ca
 fall back (MLA, runs above 4) check that the header was left alone.
 
 Cases: the six orderings of three ragged chunks (GQA with 64- and 128-column tiles; MLA falls
-back) at ranks 8 and 32 and a CUDA-core rank 12; run sizes 1 to 4 (6 falls back); M-RoPE
-items that share δ but not δ_h; an invalid item ahead of its group and an out-of-range page;
-one batch mixing ranks, lengths and unpatched items; and a batch of many one-tile task rows,
-more per CTA than the kernel keeps in shared memory at once.
+back) at ranks 8 and 32 and a CUDA-core rank 12; equal lengths, whose last sixth of row tiles
+is handed out a tile at a time; the plan's task and tile counts; run sizes 1 to 4 (6 falls
+back); M-RoPE items that share δ but not δ_h; an invalid item ahead of its group and an
+out-of-range page; one batch mixing ranks, lengths and unpatched items; a batch of many
+one-tile task rows, more per CTA than the kernel keeps in shared memory at once; a workspace
+too small and a rank too high (both fall back); successive batches on one workspace; and a
+call replayed from a CUDA graph.
 """
 import dataclasses
 import itertools
@@ -212,3 +215,80 @@ def test_many_one_tile_tasks_refetch_their_records():
     assert n_rows == n * 9 * 2 and n_tiles == 2 * n_rows
     k, v, _, _ = run(w, tl.to_device_items(w.items), True)
     tl.check_full(lay, w.items, w.page_table, k, v)
+
+
+def test_too_small_a_workspace_or_too_high_a_rank_falls_back():
+    # a workspace sized for one item cannot hold the plan of 18 (the grid path runs and the
+    # workspace is left alone); rank 64 at 128-column tiles leaves no room for two V_m^T
+    # buffers beside two CTAs per SM
+    w = orderings(gqa(H=4, hd=128), 16, "perssmall")
+    items = tl.to_device_items(w.items)
+    h = km.create(w.layout)
+    ws = torch.full((km.kamera_batch_workspace_bytes(h, 1),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    km.kamera_set_batch_workspace(h, ws)
+    k, v, st, _ = tl.run_batch(h, w.layout, items, w.page_table, w.num_slots)
+    assert st == 0 and ws[:8].view(torch.int32).tolist() == [-1, -1]
+    k0, v0, _, _ = run(w, items, False)
+    same_bytes(k, k0)
+    same_bytes(v, v0)
+    w64 = orderings(gqa(H=4, hd=128), 64, "pers64")
+    compare(w64, persistent=False)
+
+
+def test_one_workspace_for_successive_batches():
+    # two different batches, one after the other on one handle: the second plan replaces the
+    # first in the workspace, and each call writes its own bytes
+    lay = gqa(H=4, hd=128)
+    w1 = orderings(lay, 32, "perssucc1", Ts=(300, 300, 300))
+    w2 = orderings(lay, 8, "perssucc2")
+    h = km.create(lay)
+    n = max(len(w1.items), len(w2.items))
+    ws = torch.full((km.kamera_batch_workspace_bytes(h, n),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    km.kamera_set_batch_workspace(h, ws)
+    outs = []
+    for w in (w1, w2, w1):
+        k, v, st, _ = tl.run_batch(h, lay, tl.to_device_items(w.items), w.page_table,
+                                   w.num_slots)
+        assert st == 0
+        outs.append((k, v))
+    for (k, v), w in zip(outs, (w1, w2, w1)):
+        k0, v0, _, _ = run(w, tl.to_device_items(w.items), False)
+        same_bytes(k, k0)
+        same_bytes(v, v0)
+
+
+def test_replayed_from_a_cuda_graph():
+    # the planning and persistent kernels are stream work only (the plan resets the tail
+    # counters itself), so one captured call replays to the same bytes
+    w = orderings(gqa(H=4, hd=128), 32, "persgraph", Ts=(300, 300, 300))
+    lay = w.layout
+    items = tl.to_device_items(w.items)
+    h = km.create(lay)
+    ws = torch.full((km.kamera_batch_workspace_bytes(h, len(items)),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    km.kamera_set_batch_workspace(h, ws)
+    k, v = tl.sentinel_pool(lay, w.num_slots)
+    pool = km.Pool(k, v, w.page_table.cuda(), w.num_slots)
+    d_items = km.pack_items(items).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # one call outside the graph loads the kernels
+        km.kamera_batch_reuse(h, d_items, len(items), 300, 32, pool, status, s)
+    s.synchronize()
+    k.fill_(0)
+    v.fill_(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        km.kamera_batch_reuse(h, d_items, len(items), 300, 32, pool, status, s)
+    for _ in range(2):
+        k.fill_(0)
+        v.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        k0, v0, _, _ = run(w, items, False)
+        written = k0.view(torch.int16) != wl.POOL_SENTINEL_BITS
+        assert torch.equal(k.view(torch.int16)[written], k0.view(torch.int16)[written])
+        assert torch.equal(v.view(torch.int16)[written], v0.view(torch.int16)[written])
