@@ -291,9 +291,10 @@ __global__ void __launch_bounds__(kThr, 2) attn_split_kernel(const __grid_consta
 
 // ---------------------------------------------------------------------------------------
 // Tensor-core split kernel (GQA, head_dim 128): one CTA of two warpgroups (256 threads) per
-// (split of up to four 128-token tiles, up to 16 query heads of one KV head, request).
-// Warpgroup g takes tiles g, g + 2: the two run side by side, so one's loads and MMA waits
-// overlap the other's softmax. Per tile i:
+// (split of two 128-token tiles, up to 16 query heads of one KV head, request). Warpgroup g
+// takes tile g: the two run side by side, so one's loads and MMA waits overlap the other's
+// softmax. A warpgroup's stage holds K_i, then V_i: V_i is loaded once S_i is computed, while
+// the softmax runs, so that two CTAs fit on an SM. Per tile i:
 //   S_i^T [128 tokens x 16 heads] = K_i [128 x 128] · Q^T   (tcgen05, M = 128 tokens, N = 16)
 //   softmax statistics of the tile: m_i = max_t s, P_i = bf16(exp(s - m_i)), l_i = sum_t P_i
 //   O_i^T [128 dims x 16 heads] = V_i^T · P_i              (tcgen05, M = 128 dims, N = 16)
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kThr, 2) attn_split_kernel(const __grid_consta
 constexpr int kTcWg = 2;                  // warpgroups per CTA
 constexpr int kTcThr = 128 * kTcWg;
 constexpr int kTcTok = 128;    // tokens per tile: the first MMA's M
-constexpr int kTcTiles = 4;    // tiles per split
+constexpr int kTcTiles = 2;    // tiles per split: one per warpgroup
 constexpr int kTcHeads = 16;   // query heads per CTA: both MMAs' N
 constexpr int kTcDim = 128;    // head_dim served by this path: the second MMA's M
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
@@ -321,7 +322,7 @@ struct TcPlan {
   int merge;       // float [128 dims][16] output and [16] (m, l) of warpgroup 1
   int bar;         // per warpgroup: mbarriers of S and O
   int misc;        // TMEM address, timeout flag
-  int k, v;        // per warpgroup: K and V tiles
+  int k, v;        // per warpgroup: the K tile, then the V tile in the same place
   int total;
 };
 
@@ -345,8 +346,7 @@ __host__ __device__ inline TcPlan tc_plan() {
   o = (o + 127) & ~127;
   p.k = o;
   o += kTcWg * kTcTok * kTcDim * 2;
-  p.v = o;
-  o += kTcWg * kTcTok * kTcDim * 2;
+  p.v = p.k;  // V_i lands where K_i was once S_i is computed: two CTAs fit on an SM
   p.total = o;
   return p;
 }
@@ -411,8 +411,8 @@ __global__ void __launch_bounds__(kTcThr) attn_tc_kernel(const __grid_constant__
     slots[t] = s0 + t < ctx ? slot_of(a.pool, lay.page_size, r, (long long)s0 + t, a.status) : -1;
   ptx::cp_async_commit();
   __syncthreads();
-  // K and V of tile i into this warpgroup's stage; tokens left out are zero-filled
-  auto issue_tile = [&](int i) {
+  // K of tile i into this warpgroup's stage; tokens left out are zero-filled
+  auto issue_k = [&](int i) {
     const long long *sl = slots + i * kTcTok;
     for (int e = wt; e < kTcTok * nc; e += 128) {  // K-major: a warp takes 8 tokens x 4 chunks
       const int t = (e & 7) + 8 * ((e >> 5) & 15), c = ((e >> 3) & 3) + 4 * (e >> 9);
@@ -421,6 +421,11 @@ __global__ void __launch_bounds__(kTcThr) attn_tc_kernel(const __grid_constant__
                       sl_t >= 0 ? kbase + sl_t * lay.row_k + 8 * c : a.pool.k,
                       sl_t >= 0 ? 16u : 0u);
     }
+    ptx::cp_async_commit();
+  };
+  // V of tile i into the same stage, once S_i is computed (K_i is no longer read)
+  auto issue_v = [&](int i) {
+    const long long *sl = slots + i * kTcTok;
     for (int e = wt; e < kTcTok * nc; e += 128) {  // MN-major: 8 tokens x 4 chunks
       const int t = (e & 7) + 8 * (e / (8 * nc)), c = (e >> 3) % nc;
       const long long sl_t = sl[t];
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kTcThr) attn_tc_kernel(const __grid_constant__
     }
     ptx::cp_async_commit();
   };
-  if (wg < ntile) issue_tile(wg);
+  if (wg < ntile) issue_k(wg);
 
   const float neg_inf = -__int_as_float(0x7f800000);
   float acc[kTcHeads], run_m[kTcHeads], run_l[kTcHeads];  // thread wt: dimension wt
@@ -475,6 +480,7 @@ __global__ void __launch_bounds__(kTcThr) attn_tc_kernel(const __grid_constant__
     wg_sync(wg);
     ptx::tc_fence_after();
     timed_out = misc[1] != 0;
+    issue_v(i);  // in flight during the softmax
 
     // the tile's softmax statistics; thread wt holds token wt (TMEM lane wt)
     const bool live = wt < n && slots[i * kTcTok + wt] >= 0 && !timed_out;
@@ -531,6 +537,7 @@ __global__ void __launch_bounds__(kTcThr) attn_tc_kernel(const __grid_constant__
         wsum[wq * kTcHeads + lane] = v;
       }
     }
+    ptx::cp_async_wait_all();  // V_i
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     wg_sync(wg);
@@ -551,10 +558,10 @@ __global__ void __launch_bounds__(kTcThr) attn_tc_kernel(const __grid_constant__
       if (lane == 0 && !ok) misc[1] = 1;
     }
     ptx::tc_fence_before();
-    wg_sync(wg);  // O_i complete: the stage (K_i, V_i, P_i) is free; l_i visible
+    wg_sync(wg);  // O_i complete: the stage (V_i, P_i) is free; l_i visible
     ptx::tc_fence_after();
     timed_out = misc[1] != 0;
-    if (i + kTcWg < ntile) issue_tile(i + kTcWg);  // in flight while O_i is folded
+    if (i + kTcWg < ntile) issue_k(i + kTcWg);  // in flight while O_i is folded
     uint32_t ro[kTcHeads];
     ptx::tmem_ld16(to + lane_off, ro);
     ptx::tmem_ld_wait(ro);
