@@ -694,16 +694,20 @@ cudaError_t launch_reuse_tile(const ReuseArgs &a, int n_items, cudaStream_t s) {
 // task; in a batch of shared chunks most of its CTAs only search their group and exit. Here a
 // planning kernel (one CTA) forms the groups once and lists the task rows: (top-first patched
 // layer, channel, the first item of a run), each covering every column tile of its rows, as
-// self-contained 128-byte records. The persistent CTAs come in sets of `ntile`, one per
-// column tile. Most of the rows' token tiles are split into one contiguous range per set, of
-// equal weight (a token tile of a run of r members weighing 5 + r); the sets' CTAs walk the
-// same tiles side by side, so the column pieces of each pool row are written together, as in
-// the grid kernel. When every task row has the same number of token tiles, the last part is
-// handed out one tile at a time from a counter per column tile, so CTAs that ran slower take
-// less of it. Each CTA walks its tiles with the grid kernel's two-stage pipeline, carried
-// across task boundaries: the next task's record, first tiles and V_m^T (two buffers, by task
-// parity) are loaded while the previous task's last tiles are finished, and TMEM and the
-// barriers are set up once. Each tile's bytes are those of the grid kernel.
+// self-contained 128-byte records. The persistent CTAs come in Q sets of `ntile`, one CTA per
+// column tile; a set's CTAs walk the same row tiles side by side, so the column pieces of
+// each pool row are written together, as in the grid kernel.
+// - When every task row has the same number of token tiles, set q owns whole rows q, q + Q,
+//   q + 2Q, ... (about five sixths of the rows): the sets work through neighbouring rows at
+//   the same time, so the runs of one chunk, which are neighbouring rows, read its canonical
+//   rows once from DRAM. The tiles of the rows left over are handed out one at a time from a
+//   counter per column tile, so CTAs that ran slower take fewer of them.
+// - Otherwise each set owns one contiguous range of row tiles of equal weight (a token tile
+//   of a run of r members weighing 5 + r) and nothing is handed out.
+// Each CTA walks its tiles with the grid kernel's two-stage pipeline, carried across task
+// boundaries: the next task's record, first tiles and V_m^T (two buffers, by task parity) are
+// loaded while the previous task's last tiles are finished, and TMEM and the barriers are set
+// up once. Each tile's bytes are those of the grid kernel.
 // ---------------------------------------------------------------------------------------
 
 namespace {
@@ -1060,7 +1064,8 @@ __global__ void __launch_bounds__(kThrT, 2) reuse_persist_kernel(const __grid_co
     ptx::cp_async16(s0 + P.recs + (j % kRecSlots) * 128 + 16 * part,
                     reinterpret_cast<const unsigned char *>(grow + row) + 16 * part, 16u);
   };
-  // own-range tasks [j0, j1): records and tile ranges, then wait (every thread calls)
+  // own tasks [j0, j1) (own rows or own range): records and tile ranges, then wait (every
+  // thread calls)
   auto fetch_own = [&](int j0, int j1) {
     for (int x = tid; x < 8 * (j1 - j0); x += kThrT)
       copy_rec(j0 + (x >> 3), own_row(j0 + (x >> 3)), x & 7);
