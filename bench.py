@@ -604,7 +604,8 @@ def kamera_arm(args, rank, world, local_rank):
     n_split = max(20, min(args.steps, 1000))
     flush = L2Flush(dev)
     step_ev = event_pairs(args.steps, stream)
-    # three events per split step: before, between and after the call's two kernels
+    # four events per split step: before the copy kernel, between it and the patched layers,
+    # after the planning kernel (persistent path) and after the last kernel
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_split)]
     for trio in marks:
         for e in trio:

@@ -34,3 +34,35 @@ def test_spread_gives_the_median_and_nearest_rank_percentiles():
     assert s["mean_ms"] == 10.5 and s["runs"] == 20
     one = bench.spread([3.0])
     assert one["median_ms"] == one["p10_ms"] == one["p90_ms"] == 3.0
+
+
+class _Ev:
+    """A recorded event's time in ms; elapsed_time as torch.cuda.Event gives it."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_split_stats_names_the_kernels_of_each_path():
+    # two passes of two calls each: (before, between, after planning, after) per call
+    passes = [[[_Ev(0), _Ev(1), _Ev(1.25), _Ev(3)], [_Ev(10), _Ev(12), _Ev(12.5), _Ev(14)]],
+              [[_Ev(0), _Ev(2), _Ev(2.25), _Ev(4)], [_Ev(10), _Ev(11), _Ev(11.5), _Ev(13)]]]
+    p = bench.split_stats(passes, True)
+    assert set(p) == {"reuse_copy_kernel", "reuse_plan_kernel", "reuse_persist_kernel"}
+    assert p["reuse_copy_kernel"]["median_ms"] == 3.0  # 1 + 2 and 2 + 1
+    assert p["reuse_plan_kernel"]["median_ms"] == 0.75
+    assert p["reuse_persist_kernel"]["median_ms"] == 3.25
+    g = bench.split_stats(passes, False)
+    assert set(g) == {"reuse_copy_kernel", "reuse_tile_kernel"}
+    assert g["reuse_tile_kernel"]["median_ms"] == 4.0  # (2 + 2) and (2 + 2)
+
+
+def test_kernel_fracs_times_the_planning_kernel_without_bytes():
+    st = {"median_ms": 0.5, "p10_ms": 0.5, "p90_ms": 0.5, "mean_ms": 0.5, "runs": 1}
+    out = bench.kernel_fracs({"reuse_plan_kernel": st, "reuse_persist_kernel": st},
+                             {"reuse_persist_kernel": 1e9}, peak=1000.0)
+    assert "frac" not in out["reuse_plan_kernel"] and out["reuse_plan_kernel"]["ms"] == 0.5
+    assert abs(out["reuse_persist_kernel"]["frac"] - 2.0) < 1e-12  # 1 GB in 0.5 ms = 2000 GB/s
