@@ -169,10 +169,6 @@ SideStream *side_stream() {
   return ss.stream ? &ss : nullptr;
 }
 
-// Patched layers on the caller's stream, unpatched layers on the side stream at the same time
-// (layouts served by the tile kernel); otherwise the two kernels in order on the caller's
-// stream. `unpatched` false (a single item patched on every layer, checked on the host): the
-// copy kernel would have nothing to do, so only the patched-layer kernel is launched.
 // Patched layers: the persistent kernel when the batch has a workspace, else the grid kernel
 // on the layouts it serves, else the general pipeline.
 // `planned` (may be null) is recorded after the planning kernel of the persistent path, or
@@ -188,6 +184,10 @@ cudaError_t launch_patched(const kamera::ReuseArgs &a, int n_items, cudaStream_t
                      : kamera::launch_reuse(a, n_items, s);
 }
 
+// Patched layers on the caller's stream, unpatched layers on the side stream at the same time
+// (layouts served by the tile kernel); otherwise the two kernels in order on the caller's
+// stream. `unpatched` false (a single item patched on every layer, checked on the host): the
+// copy kernel would have nothing to do, so only the patched-layer kernel is launched.
 cudaError_t launch_both(const kamera::ReuseArgs &a, int n_items, bool patched, cudaStream_t s,
                         bool unpatched = true) {
   if (patched && !unpatched) return launch_patched(a, n_items, s);
