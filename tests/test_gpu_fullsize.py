@@ -21,10 +21,17 @@ def _cuda(cuda_ok):
     torch.cuda.empty_cache()
 
 
-def run_batch(w, items):
+def run_batch(w, items, workspace=False):
+    """The batch call over the items; with `workspace`, through a batch workspace (the
+    persistent path the benchmark times), whose plan header is returned as well."""
     lay = w.layout
     k, v = tl.sentinel_pool(lay, w.num_slots)
     h = km.create(lay)
+    ws = None
+    if workspace:
+        ws = torch.full((km.kamera_batch_workspace_bytes(h, len(items)),), 0xFF,
+                        dtype=torch.uint8, device="cuda")
+        km.kamera_set_batch_workspace(h, ws)
     pt = w.page_table.cuda()
     d_items = km.pack_items(items).cuda()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -33,6 +40,8 @@ def run_batch(w, items):
     km.kamera_batch_reuse(h, d_items, len(items), max_t, max_m, km.Pool(k, v, pt, w.num_slots),
                           status)
     torch.cuda.synchronize()
+    if workspace:
+        return k, v, int(status.item()), ws[:28].view(torch.int32).cpu().tolist()
     return k, v, int(status.item())
 
 
@@ -90,6 +99,30 @@ def test_config2_gqa_reorder_full():
         sl = item_slots(w, it)
         for layer in (0, 7, 13):
             assert torch.equal(v[layer].index_select(0, sl), it.canon_v[layer])
+    del k, v, w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("make", [wl.config2, wl.config2_mrope], ids=["rope", "mrope"])
+def test_config2_reorder_full_persistent(make):
+    # the timed launch configuration: 14 patched layers x (9 K runs of 2 + 6 V runs of 3) =
+    # 210 task rows of 8 token tiles x 4 column tiles, every row the same length, so the plan
+    # deals two rows to each set and hands the tiles of the rest out one at a time
+    w = make(device="cuda")
+    k, v, status, head = run_batch(w, w.items, workspace=True)
+    rows, tiles, _weight, s1, n_dyn, ntt, stride = head
+    assert status == 0
+    assert (rows, tiles, ntt) == (210, 6720, 8)
+    # token-tile positions: whole rows to the sets, the rest claimed one at a time
+    assert stride >= 1 and s1 % ntt == 0 and n_dyn > 0 and s1 + n_dyn == rows * ntt
+    k0, v0, status0 = run_batch(w, w.items)
+    assert status0 == 0
+    assert torch.equal(k.view(torch.int16), k0.view(torch.int16))
+    assert torch.equal(v.view(torch.int16), v0.view(torch.int16))
+    del k0, v0
+    torch.cuda.empty_cache()
+    st = check_units(w, w.items, k, v, 40, seed=22, layers=range(14, 28))
+    assert st.computed > 0
     del k, v, w
     torch.cuda.empty_cache()
 
