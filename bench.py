@@ -406,13 +406,16 @@ def reference_arm(args, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_desc(acc=None):
+def config_desc(acc=None, flushed=False):
+    """The workload's description; `flushed` when every timed step follows an L2 flush."""
+    l2 = "inputs larger than L2: 176 MB of canonicals and a 1.06 GB pool per step"
+    if flushed:
+        l2 = f"flushed: a {L2Flush.NBYTES >> 20} MB write before every timed step; also " + l2
     d = {"workload": "GQA reorder, Qwen2-VL-7B-like: 28 layers, H_kv=4, head_dim=128, "
                      "theta=1e6, 3 chunks x T=1024 placed in all 6 orderings (18 placements), "
                      "rank-32 orbit patch on layers 14-27, page size 16, shuffled page table",
          "items": 18, "layers": 28, "T": 1024, "row": 512, "patch_rank": 32,
-         "patched_layers": "14-27", "page_size": 16,
-         "l2": "inputs larger than L2: 176 MB of canonicals and a 1.06 GB pool per step"}
+         "patched_layers": "14-27", "page_size": 16, "l2": l2}
     if acc:
         d["bytes_per_step"] = acc
     return d
@@ -702,7 +705,7 @@ def kamera_arm(args, rank, world, local_rank):
                                       f"{args.steps} further steps run back to back with no "
                                       f"flush")),
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_desc(acc),
+        "config": config_desc(acc, flushed=True),
         "chunks_per_s": n_items * world / s,
         "us_per_chunk": ms * 1e3 / n_items,
         "gb_s_moved": achieved * world,
