@@ -212,6 +212,8 @@ def kamera_set_batch_workspace(handle: Handle, workspace: Optional[torch.Tensor]
     if workspace is None:
         _check(lib().kamera_set_batch_workspace(handle.ptr, None, 0), "kamera_set_batch_workspace")
     else:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("the batch workspace must be a contiguous CUDA tensor")
         nbytes = workspace.numel() * workspace.element_size()
         _check(lib().kamera_set_batch_workspace(handle.ptr, workspace.data_ptr(), nbytes),
                "kamera_set_batch_workspace")
@@ -352,6 +354,11 @@ def kamera_batch_reuse_timed(handle: Handle, d_items: torch.Tensor, num_items: i
     ev = list(events)
     if len(ev) == 3:
         ev = [ev[0], ev[1], None, ev[2]]
+    if len(ev) != 4:
+        raise ValueError("kamera_batch_reuse_timed takes three or four events")
+    for e in ev:
+        if e is not None and not e.cuda_event:
+            e.record()  # torch creates an event's CUDA event at its first record
     arr = (ctypes.c_void_p * 4)(*[None if e is None else e.cuda_event for e in ev])
     p = pool.c()
     _check(lib().kamera_batch_reuse_timed(handle.ptr, _ptr(d_items), int(num_items),

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import position_independent_multimodal_gb300 as km
 from position_independent_multimodal_gb300 import _binding as kb
@@ -371,9 +372,13 @@ def test_set_option_checks_its_arguments():
 
 class _WsFake:
     """A device buffer's address and size; kamera_set_batch_workspace only stores them."""
+    is_cuda = True
 
     def __init__(self, addr, nbytes):
         self.addr, self.nbytes = addr, nbytes
+
+    def is_contiguous(self):
+        return True
 
     def data_ptr(self):
         return self.addr
@@ -404,3 +409,14 @@ def test_batch_workspace_size_and_setter(lib):
     assert lib.kamera_set_batch_workspace(None, None, 0) == km.KAMERA_ERR_INVALID_ARG
     km.kamera_set_batch_workspace(h, _WsFake(0x100000, need))
     km.kamera_set_batch_workspace(h, None)
+    # host memory or a strided view is refused before the library sees a pointer
+    for bad in (torch.zeros(need, dtype=torch.uint8), torch.zeros(2 * need, dtype=torch.uint8)[::2]):
+        with pytest.raises(ValueError):
+            km.kamera_set_batch_workspace(h, bad)
+
+
+def test_timed_batch_takes_three_or_four_events(lib):
+    h = km.create(gqa())
+    for events in ([None] * 2, [None] * 5):
+        with pytest.raises(ValueError):
+            km.kamera_batch_reuse_timed(h, None, 0, 0, 0, None, None, events)

@@ -14,8 +14,9 @@ is handed out a tile at a time; the plan's task and tile counts; run sizes 1 to 
 back); M-RoPE items that share δ but not δ_h; an invalid item ahead of its group and an
 out-of-range page; one batch mixing ranks, lengths and unpatched items; a batch of many
 one-tile task rows, more per CTA than the kernel keeps in shared memory at once; a workspace
-too small and a rank too high (both fall back); successive batches on one workspace; and a
-call replayed from a CUDA graph.
+too small and a rank too high (both fall back); successive batches on one workspace; a
+call replayed from a CUDA graph; and the timed call of the benchmark's per-kernel split, with
+and without a workspace.
 """
 import dataclasses
 import itertools
@@ -292,3 +293,36 @@ def test_replayed_from_a_cuda_graph():
         written = k0.view(torch.int16) != wl.POOL_SENTINEL_BITS
         assert torch.equal(k.view(torch.int16)[written], k0.view(torch.int16)[written])
         assert torch.equal(v.view(torch.int16)[written], v0.view(torch.int16)[written])
+
+
+@pytest.mark.parametrize("workspace", [True, False])
+def test_timed_call_writes_the_same_bytes_and_orders_its_marks(workspace):
+    # the per-kernel split of the benchmark: events never recorded before (the binding creates
+    # them), marks before the copy kernel, between the layers, after the planning kernel (on
+    # the grid path at the same point) and after the last kernel, in that order
+    w = orderings(gqa(H=4, hd=128), 32, f"perstimed{int(workspace)}")
+    lay = w.layout
+    items = tl.to_device_items(w.items)
+    h = km.create(lay)
+    ws = None
+    if workspace:
+        ws = torch.full((km.kamera_batch_workspace_bytes(h, len(items)),), 0xFF,
+                        dtype=torch.uint8, device="cuda")
+        km.kamera_set_batch_workspace(h, ws)
+    k, v = tl.sentinel_pool(lay, w.num_slots)
+    pool = km.Pool(k, v, w.page_table.cuda(), w.num_slots)
+    d_items = km.pack_items(items).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    max_t = max(it.num_tokens for it in items)
+    km.kamera_batch_reuse_timed(h, d_items, len(items), max_t, 32, pool, status, ev)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if workspace:
+        assert int(ws[:4].view(torch.int32).item()) > 0, "the persistent path did not run"
+    gaps = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(g >= 0 for g in gaps) and sum(gaps) > 0
+    k0, v0, st0, _ = run(w, items, False)
+    assert st0 == 0
+    same_bytes(k, k0)
+    same_bytes(v, v0)
