@@ -264,7 +264,8 @@ kamera_status kamera_batch_reuse(const kamera_handle *handle, const kamera_item 
  * events[0..3] are CUDA events (cudaEvent_t) recorded before the first kernel, between the
  * unpatched and the patched layers, after the planning kernel (recorded together with events[1]
  * when the batch does not take the persistent path), and after the last kernel; any entry may
- * be NULL. The work done is identical to kamera_batch_reuse.
+ * be NULL, and a NULL `events` makes this call kamera_batch_reuse itself (the kernels side by
+ * side). The work done is identical to kamera_batch_reuse.
  */
 kamera_status kamera_batch_reuse_timed(const kamera_handle *handle, const kamera_item *d_items,
                                        int32_t num_items, int32_t max_tokens, int32_t max_patch_m,
