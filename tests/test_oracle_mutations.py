@@ -6,8 +6,10 @@ transposed pairing, a patch that is rotated too, a double rounding, an off-by-on
 offsets or sections taken wrongly, a re-anchoring position of the wrong sign or with its
 coordinates reversed, attention without its scale, an unnormalised split merge, singular
 values in ascending order, the opposite sign convention, an error scale built from the product
-of the factor sums or counting a turned pair twice, a re-anchoring that skips the values, and
-a bf16 spacing that is wrong at zero or one bit short.
+of the factor sums or counting a turned pair twice, a re-anchoring that skips the values, a
+bf16 spacing that is wrong at zero or one bit short, a patch range that takes in its end
+layer, the factors of the next layer, a survivor turned by -δ, an in-place patch that ignores
+its sign, and query heads dealt to KV heads round-robin instead of in groups.
 """
 import numpy as np
 import pytest
@@ -156,6 +158,36 @@ def reanchor_skips_values(layout, item, k_pool, v_pool, page_table):
     ora_apply_reanchor_orig(layout, item, k_pool, None, page_table)
 
 
+def patched_through_l1(item, layer):
+    return item.patch_m > 0 and item.patch_l0 <= layer <= item.patch_l1
+
+
+def factors_of_the_next_layer(layout, item, layer, channel, tokens=None):
+    from types import SimpleNamespace
+    if item.patch_m > 0 and item.patch_l1 - item.patch_l0 > 1:
+        pu, pv = list(item.patch_u), list(item.patch_vt)
+        item = SimpleNamespace(**{**vars(item), "patch_u": pu[1:] + pu[:1],
+                                  "patch_vt": pv[1:] + pv[:1]})
+    return ora_reuse_layer_orig(layout, item, layer, channel, tokens)
+
+
+def relocate_backwards(layout, k_pool, page_table, req, start_tok, num_tokens, delta):
+    ora_relocate_orig(layout, k_pool, page_table, req, start_tok, num_tokens, -delta)
+
+
+def patch_inplace_ignores_sign(layout, k_pool, v_pool, page_table, req, start_tok, num_tokens,
+                               patch_u, patch_vt, m, l0, l1, sign=1):
+    ora_patch_inplace_orig(layout, k_pool, v_pool, page_table, req, start_tok, num_tokens,
+                           patch_u, patch_vt, m, l0, l1, 1)
+
+
+def heads_round_robin(layout, h, num_q_heads):
+    if layout.kind == ora.GQA:      # head h to KV head h % H_kv instead of h // (H_q / H_kv)
+        c0 = (h % layout.num_kv_heads) * layout.head_dim
+        return (c0, layout.head_dim), (c0, layout.head_dim), 1
+    return ora_head_columns_orig(layout, h, num_q_heads)
+
+
 ora_rotate_orig = ora.rotate_band
 ora_magnitude_orig = ora.magnitude_layer
 ora_apply_reanchor_orig = ora.apply_reanchor
@@ -165,6 +197,10 @@ ora_token_offsets_orig = ora.token_offsets
 ora_attend_orig = ora.attend
 ora_sign_rows_orig = ora._sign_rows
 ora_ulp_orig = ora.bf16_ulp
+ora_reuse_layer_orig = ora.reuse_layer
+ora_relocate_orig = ora.relocate
+ora_patch_inplace_orig = ora.patch_inplace
+ora_head_columns_orig = ora.head_columns
 
 
 CASES = [
@@ -202,6 +238,14 @@ CASES = [
     ("slot_of", off_by_one_slot, [pins.test_reanchored_items_land_at_their_slots]),
     ("bf16_ulp", ulp_from_frexp_alone, [pins.test_bf16_ulp_is_the_gap_to_the_next_pattern]),
     ("bf16_ulp", ulp_one_bit_short, [pins.test_bf16_ulp_is_the_gap_to_the_next_pattern]),
+    ("layer_patched", patched_through_l1, [pins.test_layers_outside_the_patch_range_are_unpatched]),
+    ("reuse_layer", factors_of_the_next_layer, [pins.test_patch_by_pure_python_sums,
+                                                pins.test_mla_kpe_band_gets_its_own_patch_group]),
+    ("relocate", relocate_backwards, [pins.test_relocate_in_place_rotates_only_rope_columns]),
+    ("patch_inplace", patch_inplace_ignores_sign,
+     [pins.test_patch_inplace_sign_symmetry_and_pure_python_sums,
+      pins.test_patch_add_then_remove_is_within_two_roundings]),
+    ("head_columns", heads_round_robin, [pins.test_decode_attention_gathers_heads_and_pages]),
 ]
 
 

@@ -277,6 +277,29 @@ def test_patch_by_pure_python_sums():
                     assert abs(vals[t, c] - want) <= 1e-12 * max(1.0, abs(want))
 
 
+def test_layers_outside_the_patch_range_are_unpatched():
+    # Eq. 1 adds U_m V_m^T only on the patched layers [l0, l1): the layers on either side are
+    # the relocated canonical alone (the same item at rank zero), bit for bit. The factor
+    # arrays hold an entry for every layer, so a boundary taken one layer off reads real
+    # factors instead of failing to index them.
+    from types import SimpleNamespace
+    rng = np.random.default_rng(77)
+    lay, it = gqa_item(L=4, T=5, H=1, hd=8, delta=777, rng=rng)
+    m = 2
+    it = SimpleNamespace(**{**vars(it), "patch_m": m, "patch_l0": 1, "patch_l1": 3,
+                            "patch_u": rand_bf16_bits((4, 2, 5, m), rng=rng),
+                            "patch_vt": rand_bf16_bits((4, m * 2 * 8), 0.5, rng=rng)})
+    bare = SimpleNamespace(**{**vars(it), "patch_m": 0, "patch_l0": 0, "patch_l1": 0})
+    for layer in range(4):
+        for ch in range(2):
+            got = ora.reuse_layer_bits(lay, it, layer, ch)
+            ref = ora.reuse_layer_bits(lay, bare, layer, ch)
+            if layer in (0, 3):
+                np.testing.assert_array_equal(got, ref)
+            else:
+                assert not np.array_equal(got, ref), f"layer {layer} channel {ch} unpatched"
+
+
 def test_full_rank_patch_reconstructs_conditioned_kv():
     # App. A: Δ = KV(B|A) - R(δ)KV(B|∅); the patch from the full SVD of Δ added after the
     # rotation gives back KV(B|A) exactly (float64).
