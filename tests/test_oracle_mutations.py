@@ -9,7 +9,9 @@ values in ascending order, the opposite sign convention, an error scale built fr
 of the factor sums or counting a turned pair twice, a re-anchoring that skips the values, a
 bf16 spacing that is wrong at zero or one bit short, a patch range that takes in its end
 layer, the factors of the next layer, a survivor turned by -δ, an in-place patch that ignores
-its sign, and query heads dealt to KV heads round-robin instead of in groups.
+its sign, query heads dealt to KV heads round-robin instead of in groups, MLA's rotation
+applied to the latent instead of k_pe, every column rounded instead of the untouched ones
+copied, and the deficit taken the wrong way round.
 """
 import numpy as np
 import pytest
@@ -188,6 +190,21 @@ def heads_round_robin(layout, h, num_q_heads):
     return ora_head_columns_orig(layout, h, num_q_heads)
 
 
+def bands_on_the_latent(layout):
+    if layout.kind == ora.MLA:      # the first rope_dim columns of the row: the c_KV latent
+        return [(0, layout.rope_dim)]
+    return ora_rope_bands_orig(layout)
+
+
+def every_column_rounded(layout, item, layer, channel, tokens=None):
+    vals, _ = ora.reuse_layer(layout, item, layer, channel, tokens)
+    return ora.f64_to_bf16(vals)    # no byte copy where nothing is computed
+
+
+def deficit_reversed(kv_cond, kv_solo_relocated, m):
+    return ora_form_patch_orig(kv_solo_relocated, kv_cond, m)
+
+
 ora_rotate_orig = ora.rotate_band
 ora_magnitude_orig = ora.magnitude_layer
 ora_apply_reanchor_orig = ora.apply_reanchor
@@ -201,6 +218,8 @@ ora_reuse_layer_orig = ora.reuse_layer
 ora_relocate_orig = ora.relocate
 ora_patch_inplace_orig = ora.patch_inplace
 ora_head_columns_orig = ora.head_columns
+ora_rope_bands_orig = ora.rope_bands
+ora_form_patch_orig = ora.form_patch
 
 
 CASES = [
@@ -246,6 +265,11 @@ CASES = [
      [pins.test_patch_inplace_sign_symmetry_and_pure_python_sums,
       pins.test_patch_add_then_remove_is_within_two_roundings]),
     ("head_columns", heads_round_robin, [pins.test_decode_attention_gathers_heads_and_pages]),
+    ("rope_bands", bands_on_the_latent, [pins.test_mla_latent_copied_byte_exact_and_only_kpe_turns,
+                                         pins.test_layout_reading_matches_printed_shapes]),
+    ("reuse_layer_bits", every_column_rounded, [pins.test_delta_zero_rank_zero_is_bitwise_identity]),
+    ("form_patch", deficit_reversed, [pins.test_full_rank_patch_reconstructs_conditioned_kv,
+                                      pins.test_eckart_young_residual]),
 ]
 
 
