@@ -66,3 +66,11 @@ def test_kernel_fracs_times_the_planning_kernel_without_bytes():
                              {"reuse_persist_kernel": 1e9}, peak=1000.0)
     assert "frac" not in out["reuse_plan_kernel"] and out["reuse_plan_kernel"]["ms"] == 0.5
     assert abs(out["reuse_persist_kernel"]["frac"] - 2.0) < 1e-12  # 1 GB in 0.5 ms = 2000 GB/s
+
+
+def test_config_names_the_l2_flush_of_the_gpu_arm():
+    # the GPU arm flushes L2 before every timed step and says so; the oracle arm does not flush
+    gpu = bench.config_desc(flushed=True)["l2"]
+    cpu = bench.config_desc()["l2"]
+    assert gpu.startswith("flushed: a 512 MB write") and "inputs larger than L2" in gpu
+    assert "flush" not in cpu and "inputs larger than L2" in cpu
